@@ -1,0 +1,462 @@
+"""Benchmark of the fused GEMM + epilogue on one GB300 (or N replicas, one per GPU).
+
+A step is one call of the fused kernel over one batch of synthetic input: by default the
+4096 x 4096 x 4096 bf16 GEMM + bias + ReLU.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py --sweep          # every workload (+ unfused chain, GROUP sweep) -> stderr + JSON
+
+Timing: inputs rotate over several independent sets whose total exceeds twice the L2 size, so
+every step reads A and B from HBM; CUDA events on the launching stream; barrier + synchronize on
+both sides of the timed region; the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+epilogue TFLOP/s and % of dense BF16 tensor peak (1 GB300)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES_DEFAULT = 129 * 1024 * 1024
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "gemm_epilogue_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.proc = None
+        self.rows = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                                  "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
+                                  "hw_slow": parts[5], "hw_therm": parts[6], "sw_therm": parts[7],
+                                  "sw_power": parts[8]})
+            except ValueError:
+                continue
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [r for r in self.rows if r["power"] > 300.0] or self.rows
+        reasons = set()
+        for r in loaded:
+            for k, name in (("hw_slow", "hw_slowdown"), ("hw_therm", "hw_thermal_slowdown"),
+                            ("sw_therm", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[k] == "Active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in loaded), "reasons": sorted(reasons),
+                "samples": len(loaded)}
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# --------------------------------------------------------------------------- our implementation
+
+class Problem:
+    """Device-resident rotating input sets of one workload, and a call of the fused kernel."""
+
+    def __init__(self, w, dev, l2_bytes, max_sets=8, with_unfused=False):
+        import torch
+        from gemm_epilogue_gb300 import inputs as gen
+        import gemm_epilogue_gb300.binding as fg
+        self.w, self.dev, self.fg = w, dev, fg
+        tdt = {gen.F16: torch.float16, gen.BF16: torch.bfloat16, gen.F32: torch.float32}
+        self.tdt = tdt
+        x = gen.make(w)
+        self.host = x
+
+        def up(a, t):
+            if a is None:
+                return None
+            if t == gen.F32:
+                return torch.from_numpy(a).to(dev)
+            return torch.from_numpy(a.view(np.int16)).view(tdt[t]).to(dev)
+
+        A, B = up(x.A, w.ab_type), up(x.B, w.ab_type)
+        bias, Y = up(x.bias, w.bias_type), up(x.Y, w.ab_type)
+        set_bytes = A.numel() * A.element_size() + B.numel() * B.element_size()
+        set_bytes += w.M * w.N * (4 if w.out_type == gen.F32 else 2) * (2 if Y is not None else 1)
+        n = max(1, min(max_sets, math.ceil(2 * l2_bytes / max(set_bytes, 1)) + 1))
+        self.sets = []
+        for i in range(n):
+            if i == 0:
+                a, b, y = A, B, Y
+            else:  # independent copies (same values, different addresses)
+                a, b = A.clone(), B.clone()
+                y = Y.clone() if Y is not None else None
+            out = torch.empty(w.M, w.N, dtype=tdt[w.out_type], device=dev)
+            self.sets.append((a, b, bias, y, out))
+        self.set_bytes = set_bytes
+        self.word = {gen.F16: fg.F16, gen.BF16: fg.BF16}[w.ab_type]
+        if w.bias_type == gen.F32:
+            self.word |= fg.BIAS_F32
+        if w.out_type == gen.F32:
+            self.word |= fg.OUT_F32
+        self.ws = None
+        if with_unfused:
+            nb = fg.fgemm_unfused_workspace_bytes(w.M, w.N, self.word, 0)
+            self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+            self.ws_bytes = nb
+
+    def call(self, i, stream, opts=None, unfused=False):
+        a, b, bias, y, out = self.sets[i % len(self.sets)]
+        w, fg = self.w, self.fg
+        if unfused:
+            if y is not None:
+                fg.fgemm_unfused_addmm_gate(a, b, bias, y, out, w.M, w.N, w.K, self.word, self.ws,
+                                            self.ws_bytes, 0, stream)
+            else:
+                fg.fgemm_unfused_bias_relu(a, b, bias, out, w.M, w.N, w.K, self.word, self.ws,
+                                           self.ws_bytes, 0, stream)
+            return None
+        if y is not None:
+            return fg.fgemm_addmm_gate_ex(a, b, bias, y, out, w.M, w.N, w.K, self.word, stream, opts)
+        return fg.fgemm_bias_relu_ex(a, b, bias, out, w.M, w.N, w.K, self.word, stream, opts)
+
+
+def time_steps(prob, steps, warmup, stream, opts=None, unfused=False, barrier=None):
+    import torch
+    path = None
+    for i in range(warmup):
+        path = prob.call(i, stream.cuda_stream, opts, unfused)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        path = prob.call(warmup + i, stream.cuda_stream, opts, unfused)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end) / steps, path
+
+
+def e2e_steps(prob, steps, stream):
+    """Host buffers in pinned memory; H2D of A, B, bias (and Y), the call, D2H of out."""
+    import torch
+    w = prob.w
+    a, b, bias, y, out = prob.sets[0]
+    hA = torch.empty_like(a, device="cpu").pin_memory()
+    hB = torch.empty_like(b, device="cpu").pin_memory()
+    hb = torch.empty_like(bias, device="cpu").pin_memory()
+    hY = torch.empty_like(y, device="cpu").pin_memory() if y is not None else None
+    hO = torch.empty_like(out, device="cpu").pin_memory()
+    hA.copy_(a)
+    hB.copy_(b)
+    hb.copy_(bias)
+    if hY is not None:
+        hY.copy_(y)
+    h2d = sum(t.numel() * t.element_size() for t in (hA, hB, hb, hY) if t is not None)
+    d2h = hO.numel() * hO.element_size()
+    fg = prob.fg
+
+    def one():
+        with torch.cuda.stream(stream):
+            a.copy_(hA, non_blocking=True)
+            b.copy_(hB, non_blocking=True)
+            bias.copy_(hb, non_blocking=True)
+            if hY is not None:
+                y.copy_(hY, non_blocking=True)
+            if y is not None:
+                fg.fgemm_addmm_gate(a, b, bias, y, out, w.M, w.N, w.K, prob.word, stream.cuda_stream)
+            else:
+                fg.fgemm_bias_relu(a, b, bias, out, w.M, w.N, w.K, prob.word, stream.cuda_stream)
+            hO.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps, h2d, d2h
+
+
+def cpu_baseline(w, target_s=12.0):
+    """The fp64 oracle as it stands, on a bounded row sample of the same workload."""
+    import oracle
+    from gemm_epilogue_gb300 import inputs as gen
+    oracle.build()
+    x = gen.make(w)
+    threads = oracle.default_threads()
+    rows = max(1, min(w.M, threads))
+    while True:
+        sel = np.arange(rows, dtype=np.int64)
+        t0 = time.perf_counter()
+        oracle.gemm_epilogue(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type,
+                             oracle.EPI_GATE if w.epilogue == "gate" else oracle.EPI_RELU,
+                             Y=x.Y, rows=sel, threads=threads, want_ref=False)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4 or rows >= w.M:
+            break
+        rows = min(w.M, max(rows + 1, int(rows * min(8.0, target_s / max(dt, 1e-3)))))
+    tflops = 2.0 * rows * w.N * w.K / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{rows} of {w.M} output rows of {w.name} (all {w.N} columns, K={w.K}), "
+                      f"{dt:.2f} s", "seconds": dt}
+
+
+def run_ours(args):
+    import torch
+    from gemm_epilogue_gb300 import build as libbuild
+    from gemm_epilogue_gb300 import inputs as gen
+    rank, world, local = env_rank()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        libbuild.build()
+    if dist:
+        dist.barrier()
+    import gemm_epilogue_gb300.binding as fg
+    fg.lib()
+    w = gen.WORKLOADS[args.workload]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_DEFAULT
+    prob = Problem(w, dev, l2)
+    stream = torch.cuda.Stream(device=dev)
+    barrier = (lambda: dist.barrier()) if dist else None
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    ms, path = time_steps(prob, args.steps, args.warmup, stream, barrier=barrier)
+    clocks = sampler.stop() if sampler else None
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    e2e_ms, h2d, d2h = e2e_steps(prob, max(3, min(args.steps, 20)), stream)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert fg.fgemm_device_status(stream) == 0
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    pk, pk_src = peaks()
+    tflops = w.flops / (ms * 1e-3) / 1e12
+    kname = {fg.PATH_TC: "tc_gemm_kernel", fg.PATH_SKINNY: "skinny_kernel",
+             fg.PATH_GENERIC: "generic_kernel"}.get(path, "?")
+    hbm_bound = w.unavoidable_bytes() / (pk["hbm_gbs"] * 1e9) > w.flops / (pk["bf16_tflops"] * 1e12)
+    if hbm_bound:
+        achieved = w.unavoidable_bytes() / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"]}
+    else:
+        roof = {"bound": "tensor", "achieved": tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tflops / pk["bf16_tflops"]}
+    roof["peak_source"] = f"{pk_src} (MEASURED_PEAKS.json burst)" if pk_src == "measured" else pk_src
+    roof["traffic"] = recorded_traffic(w.name, kname)
+    roof["kernel"] = kname
+    cpu = None if args.no_cpu else cpu_baseline(w)
+    line = {
+        "metric": METRIC, "value": tflops * world, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": gen.TYPE_NAMES[w.ab_type],
+        "data": "synthetic (seeded normal inputs, shapes of the workload)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "epilogue": w.epilogue,
+                   "out": gen.TYPE_NAMES[w.out_type], "bias": gen.TYPE_NAMES[w.bias_type],
+                   "path": fg.PATH_NAMES.get(path, str(path)), "parallelism": f"replicas{world}",
+                   "l2": f"inputs rotate over {len(prob.sets)} sets of {prob.set_bytes / 1e6:.1f} MB "
+                         f"(> 2 x L2 {l2 / 1e6:.0f} MB)"},
+        "pct_of_peak": 100.0 * tflops / pk["bf16_tflops"],
+        "roofline": roof,
+        "e2e": {"value": w.flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle (fp64 CPU) as the reference arm: each step is a bounded row sample."""
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return
+    import oracle
+    from gemm_epilogue_gb300 import inputs as gen
+    oracle.build()
+    w = gen.WORKLOADS[args.workload]
+    x = gen.make(w)
+    threads = oracle.default_threads()
+    rows = max(1, min(w.M, 2 * threads))
+    sel = np.arange(rows, dtype=np.int64)
+    epi = oracle.EPI_GATE if w.epilogue == "gate" else oracle.EPI_RELU
+
+    def step():
+        oracle.gemm_epilogue(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type,
+                             w.out_type, epi, Y=x.Y, rows=sel, threads=threads, want_ref=False)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    tflops = 2.0 * rows * w.N * w.K / dt / 1e12
+    sample = f"{rows} of {w.M} output rows of {w.name} per step (all {w.N} columns, K={w.K})"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded normal inputs, shapes of the workload)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "epilogue": w.epilogue},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_sweep(args):
+    """Every workload: fused TFLOP/s, GB/s, roofline fraction; unfused chain; GROUP sweep."""
+    import torch
+    from gemm_epilogue_gb300 import build as libbuild
+    from gemm_epilogue_gb300 import inputs as gen
+    libbuild.build()
+    import gemm_epilogue_gb300.binding as fg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_DEFAULT
+    pk, pk_src = peaks()
+    stream = torch.cuda.Stream(device=dev)
+    names = args.sweep_workloads.split(",") if args.sweep_workloads else list(gen.WORKLOADS)
+    results = []
+    for name in names:
+        w = gen.WORKLOADS[name]
+        unf = w.name in ("square_4096", "glu_gate_1024x21568x4096")
+        prob = Problem(w, dev, l2, with_unfused=unf)
+        steps = max(5, min(200, int(2e-1 / max(w.flops / 1.2e15, 1e-6))))
+        groups = [1, 4, 8] if w.name.startswith("ffn") else [None]
+        for g in groups:
+            opts = {"group_m": g} if g else None
+            ms, path = time_steps(prob, steps, 5, stream, opts=opts)
+            t = w.flops / (ms * 1e-3) / 1e12
+            gbs = w.unavoidable_bytes() / (ms * 1e-3) / 1e9
+            t_roof = max(w.flops / (pk["bf16_tflops"] * 1e12), w.unavoidable_bytes() / (pk["hbm_gbs"] * 1e9))
+            r = {"workload": name, "group_m": g or 8, "path": fg.PATH_NAMES.get(path), "us": ms * 1e3,
+                 "tflops": t, "gbs": gbs, "roofline_frac": t_roof / (ms * 1e-3),
+                 "pct_bf16_peak": 100 * t / pk["bf16_tflops"], "pct_hbm": 100 * gbs / pk["hbm_gbs"]}
+            results.append(r)
+            print(json.dumps(r), file=sys.stderr, flush=True)
+        if unf:
+            ms, _ = time_steps(prob, steps, 3, stream, unfused=True)
+            r = {"workload": name, "variant": "unfused", "us": ms * 1e3,
+                 "tflops": w.flops / (ms * 1e-3) / 1e12}
+            results.append(r)
+            print(json.dumps(r), file=sys.stderr, flush=True)
+        assert fg.fgemm_device_status(stream) == 0
+        del prob
+        torch.cuda.empty_cache()
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    with open(os.path.join(ROOT, "gpurun_out", "sweep.json"), "w") as f:
+        json.dump({"peaks": pk, "peak_source": pk_src, "results": results}, f, indent=1)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="square_4096")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--sweep-workloads", default="")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

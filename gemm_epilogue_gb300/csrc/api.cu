@@ -1,0 +1,394 @@
+// api.cu -- the C ABI (include/fgemm.h): argument validation, path choice, TMA descriptor
+// encoding and launches on the caller's stream.  Host code only, apart from the error word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "fgemm.h"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_order.h"
+
+namespace fgemm {
+
+// The device error word (one per device that loads the library).
+__device__ int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  int ok = 0;  // 1 = usable (compute capability 10.3)
+  int num_sms = 0;
+  int* err = nullptr;  // device address of g_error_word
+};
+DeviceInfo g_dev[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+// Current device, checked once: must be compute capability 10.3 (the library is built for
+// sm_103a only).  Also resolves the address of this device's error word.
+DeviceInfo* current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  DeviceInfo& d = g_dev[dev];
+  std::call_once(d.once, [&] {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    if (major != 10 || minor != 3) return;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    d.err = static_cast<int*>(p);
+    d.num_sms = sms;
+    d.ok = 1;
+  });
+  return d.ok ? &d : nullptr;
+}
+
+struct Types {
+  int ab, bias, out;  // Elem codes
+};
+
+int parse_dtype(int dtype, Types* t) {
+  const int ab = dtype & 0xF, bias = dtype & 0xF0, out = dtype & 0xF00;
+  if ((dtype & ~0xFFF) != 0) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (ab != FGEMM_F16 && ab != FGEMM_BF16) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (bias != FGEMM_BIAS_SAME && bias != FGEMM_BIAS_F32) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (out != FGEMM_OUT_SAME && out != FGEMM_OUT_F32) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  t->ab = (ab == FGEMM_BF16) ? ELEM_BF16 : ELEM_F16;
+  t->bias = (bias == FGEMM_BIAS_F32) ? ELEM_F32 : t->ab;
+  t->out = (out == FGEMM_OUT_F32) ? ELEM_F32 : t->ab;
+  return FGEMM_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+CUtensorMapDataType tma_type(int e) {
+  return e == ELEM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                       : (e == ELEM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+
+// Row-major matrix of `rows` x `cols` elements; box of box_rows x box_cols, 128-byte swizzle.
+bool encode_2d(CUtensorMap* m, int elem, const void* base, int64_t rows, int64_t cols,
+               uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes(elem)};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, tma_type(elem), 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Call {
+  const void *A, *B, *bias, *Y;
+  void* out;
+  int64_t M, N, K;
+  Types t;
+  int epi;  // Epi
+  cudaStream_t stream;
+  const fgemm_opts* opts;
+};
+
+int status_of(cudaError_t e) {
+  if (e == cudaSuccess) return FGEMM_OK;
+  cudaGetLastError();
+  return FGEMM_ERR_LAUNCH;
+}
+
+// Checks shared by the fused and unfused entries.  Returns FGEMM_OK or an error; sets *nothing
+// to true when M or N is zero.
+int validate(const Call& c, bool* nothing) {
+  *nothing = false;
+  if (c.M < 0 || c.N < 0 || c.K < 0 || c.M > 0x7fffffffLL || c.N > 0x7fffffffLL ||
+      c.K > 0x7fffffffLL)
+    return FGEMM_ERR_INVALID_VALUE;
+  if (c.M == 0 || c.N == 0) {
+    *nothing = true;
+    return FGEMM_OK;
+  }
+  if (!c.out || (c.epi != EPI_NONE && !c.bias) || (c.epi == EPI_GATE && !c.Y))
+    return FGEMM_ERR_INVALID_VALUE;
+  if (c.K > 0 && (!c.A || !c.B)) return FGEMM_ERR_INVALID_VALUE;
+  const size_t eab = elem_bytes(c.t.ab);
+  if ((c.A && !aligned(c.A, eab)) || (c.B && !aligned(c.B, eab)) ||
+      (c.Y && !aligned(c.Y, eab)) || (c.bias && !aligned(c.bias, elem_bytes(c.t.bias))) ||
+      !aligned(c.out, elem_bytes(c.t.out)))
+    return FGEMM_ERR_MISALIGNED;
+  if (c.opts) {
+    const fgemm_opts& o = *c.opts;
+    if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
+        o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0)
+      return FGEMM_ERR_INVALID_VALUE;
+  }
+  return FGEMM_OK;
+}
+
+bool tc_eligible(const Call& c) {
+  if (c.K % 8 != 0 || c.N % 8 != 0) return false;  // 16-byte row strides for TMA
+  return aligned(c.A, 16) && aligned(c.B, 16) && aligned(c.out, 16) &&
+         (c.bias == nullptr || aligned(c.bias, 16)) && (c.Y == nullptr || aligned(c.Y, 16));
+}
+
+int run_tc(const Call& c, DeviceInfo* d) {
+  const int BM = tc_block_m(), BN = tc_block_n();
+  CUtensorMap tmA, tmB, tmO;
+  const uint32_t out_box_cols = (c.t.out == ELEM_F32) ? 32 : 64;
+  if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, 64) ||
+      !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
+      !encode_2d(&tmO, c.t.out, c.out, c.M, c.N, 32, out_box_cols))
+    return FGEMM_ERR_LAUNCH;
+  TcParams p{};
+  p.M = static_cast<int>(c.M);
+  p.N = static_cast<int>(c.N);
+  p.K = static_cast<int>(c.K);
+  p.tiles_m = static_cast<int>((c.M + BM - 1) / BM);
+  p.tiles_n = static_cast<int>((c.N + BN - 1) / BN);
+  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
+  if (tiles > 0x7fffffffLL) return FGEMM_ERR_INVALID_VALUE;
+  p.num_tiles = static_cast<int>(tiles);
+  p.group = (c.opts && c.opts->group_m > 0) ? c.opts->group_m : 8;
+  p.ab_bf16 = c.t.ab == ELEM_BF16;
+  p.bias_type = c.t.bias;
+  p.out_type = c.t.out;
+  p.bias = c.bias;
+  p.Y = c.Y;
+  p.idesc = idesc_f16_f32acc(p.ab_bf16 != 0, BM, BN, /*a_mn=*/false, /*b_mn=*/true);
+  const bool swap = c.opts && c.opts->b_desc_swap;
+  p.b_lbo = swap ? 1024u : 64u * 64u * 2u;  // distance between 64-column boxes of B
+  p.b_sbo = swap ? 64u * 64u * 2u : 1024u;  // distance between 8-row groups along K
+  const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
+  p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
+  p.err = d->err;
+  int grid = d->num_sms;
+  if (c.opts && c.opts->max_ctas > 0 && c.opts->max_ctas < grid) grid = c.opts->max_ctas;
+  if (grid > p.num_tiles) grid = p.num_tiles;
+  return status_of(launch_tc(c.epi, tmA, tmB, tmO, p, grid, c.stream));
+}
+
+SimtParams simt_params(const Call& c) {
+  SimtParams p{};
+  p.A = c.A;
+  p.B = c.B;
+  p.bias = c.bias;
+  p.Y = c.Y;
+  p.out = c.out;
+  p.M = static_cast<int>(c.M);
+  p.N = static_cast<int>(c.N);
+  p.K = static_cast<int>(c.K);
+  p.ab_type = c.t.ab;
+  p.bias_type = c.t.bias;
+  p.out_type = c.t.out;
+  return p;
+}
+
+// Choose and run a path for a validated, non-empty call.
+int dispatch(const Call& c, DeviceInfo* d, int* path_taken) {
+  const int forced = c.opts ? c.opts->path : FGEMM_PATH_AUTO;
+  int path;
+  if (forced == FGEMM_PATH_AUTO) {
+    if (c.K == 0)
+      path = (c.epi == EPI_NONE) ? FGEMM_PATH_GENERIC : FGEMM_PATH_KZERO;
+    else
+      path = tc_eligible(c) ? FGEMM_PATH_TC : FGEMM_PATH_GENERIC;
+  } else {
+    path = forced;
+    if (path == FGEMM_PATH_TC && (c.K == 0 || !tc_eligible(c))) return FGEMM_ERR_INVALID_VALUE;
+    if (path == FGEMM_PATH_KZERO && (c.K != 0 || c.epi == EPI_NONE)) return FGEMM_ERR_INVALID_VALUE;
+    if (path == FGEMM_PATH_SKINNY) return FGEMM_ERR_INVALID_VALUE;  // not available for this call
+  }
+  if (path_taken) *path_taken = path;
+  switch (path) {
+    case FGEMM_PATH_TC: return run_tc(c, d);
+    case FGEMM_PATH_KZERO: return status_of(launch_kzero(c.epi, simt_params(c), d->num_sms, c.stream));
+    default: return status_of(launch_generic(c.epi, simt_params(c), c.stream));
+  }
+}
+
+int fused(const Call& c, int* path_taken) {
+  if (path_taken) *path_taken = FGEMM_PATH_NONE;
+  bool nothing = false;
+  int st = validate(c, &nothing);
+  if (st != FGEMM_OK || nothing) return st;
+  DeviceInfo* d = current_device();
+  if (!d) return FGEMM_ERR_NO_DEVICE;
+  return dispatch(c, d, path_taken);
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+}  // namespace fgemm
+
+using namespace fgemm;
+
+extern "C" {
+
+int fgemm_bias_relu_ex(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                       int64_t N, int64_t K, int dtype, void* stream, const fgemm_opts* opts,
+                       int* path_taken) {
+  Call c{A, B, bias, nullptr, out, M, N, K, {}, EPI_RELU, static_cast<cudaStream_t>(stream), opts};
+  const int st = parse_dtype(dtype, &c.t);
+  if (st != FGEMM_OK) return st;
+  return fused(c, path_taken);
+}
+
+int fgemm_addmm_gate_ex(const void* A, const void* B, const void* bias, const void* Y, void* out,
+                        int64_t M, int64_t N, int64_t K, int dtype, void* stream,
+                        const fgemm_opts* opts, int* path_taken) {
+  Call c{A, B, bias, Y, out, M, N, K, {}, EPI_GATE, static_cast<cudaStream_t>(stream), opts};
+  const int st = parse_dtype(dtype, &c.t);
+  if (st != FGEMM_OK) return st;
+  return fused(c, path_taken);
+}
+
+int fgemm_bias_relu(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                    int64_t N, int64_t K, int dtype, void* stream) {
+  return fgemm_bias_relu_ex(A, B, bias, out, M, N, K, dtype, stream, nullptr, nullptr);
+}
+
+int fgemm_addmm_gate(const void* A, const void* B, const void* bias, const void* Y, void* out,
+                     int64_t M, int64_t N, int64_t K, int dtype, void* stream) {
+  return fgemm_addmm_gate_ex(A, B, bias, Y, out, M, N, K, dtype, stream, nullptr, nullptr);
+}
+
+size_t fgemm_unfused_workspace_bytes(int64_t M, int64_t N, int dtype, int inter_f32) {
+  Types t{};
+  if (parse_dtype(dtype, &t) != FGEMM_OK || M < 0 || N < 0) return 0;
+  const size_t e = inter_f32 ? 4 : static_cast<size_t>(elem_bytes(t.out));
+  return round_up(static_cast<size_t>(M) * static_cast<size_t>(N) * e, 256);
+}
+
+static int unfused(const void* A, const void* B, const void* bias, const void* Y, void* out,
+                   int64_t M, int64_t N, int64_t K, int dtype, void* workspace,
+                   size_t workspace_bytes, int inter_f32, void* stream, int epi) {
+  Call fin{A, B, bias, Y, out, M, N, K, {}, epi, static_cast<cudaStream_t>(stream), nullptr};
+  int st = parse_dtype(dtype, &fin.t);
+  if (st != FGEMM_OK) return st;
+  bool nothing = false;
+  st = validate(fin, &nothing);
+  if (st != FGEMM_OK || nothing) return st;
+  const size_t need = fgemm_unfused_workspace_bytes(M, N, dtype, inter_f32);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return FGEMM_ERR_WORKSPACE;
+  DeviceInfo* d = current_device();
+  if (!d) return FGEMM_ERR_NO_DEVICE;
+  const int inter = inter_f32 ? ELEM_F32 : fin.t.out;
+  // step 1: plain GEMM, I = A @ B (rounded once to the intermediate type)
+  Call g = fin;
+  g.epi = EPI_NONE;
+  g.bias = nullptr;
+  g.Y = nullptr;
+  g.out = workspace;
+  g.t.out = inter;
+  st = dispatch(g, d, nullptr);
+  if (st != FGEMM_OK) return st;
+  const int m = static_cast<int>(M), n = static_cast<int>(N);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (epi == EPI_RELU) {
+    // step 2: I = I + bias (read + write I); step 3: out = ReLU(I) (read I, write out)
+    st = status_of(launch_ew_bias_inplace(workspace, inter, bias, fin.t.bias, m, n, d->num_sms, s));
+    if (st != FGEMM_OK) return st;
+    return status_of(launch_ew_relu(workspace, inter, out, fin.t.out, m, n, d->num_sms, s));
+  }
+  // step 2: out = (I + bias) + (I + bias) * Y
+  return status_of(launch_ew_bias_gate(workspace, inter, bias, fin.t.bias, Y, fin.t.ab, out,
+                                       fin.t.out, m, n, d->num_sms, s));
+}
+
+int fgemm_unfused_bias_relu(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                            int64_t N, int64_t K, int dtype, void* workspace,
+                            size_t workspace_bytes, int inter_f32, void* stream) {
+  return unfused(A, B, bias, nullptr, out, M, N, K, dtype, workspace, workspace_bytes, inter_f32,
+                 stream, EPI_RELU);
+}
+
+int fgemm_unfused_addmm_gate(const void* A, const void* B, const void* bias, const void* Y,
+                             void* out, int64_t M, int64_t N, int64_t K, int dtype,
+                             void* workspace, size_t workspace_bytes, int inter_f32,
+                             void* stream) {
+  return unfused(A, B, bias, Y, out, M, N, K, dtype, workspace, workspace_bytes, inter_f32, stream,
+                 EPI_GATE);
+}
+
+int fgemm_device_status(void* stream, int* code) {
+  if (!code) return FGEMM_ERR_INVALID_VALUE;
+  *code = 0;
+  if (!current_device()) return FGEMM_ERR_NO_DEVICE;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FGEMM_ERR_LAUNCH;
+  }
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return FGEMM_ERR_LAUNCH;
+  }
+  *code = v;
+  return FGEMM_OK;
+}
+
+const char* fgemm_status_string(int s) {
+  switch (s) {
+    case FGEMM_OK: return "FGEMM_OK";
+    case FGEMM_ERR_INVALID_VALUE: return "FGEMM_ERR_INVALID_VALUE";
+    case FGEMM_ERR_UNSUPPORTED_DTYPE: return "FGEMM_ERR_UNSUPPORTED_DTYPE";
+    case FGEMM_ERR_MISALIGNED: return "FGEMM_ERR_MISALIGNED";
+    case FGEMM_ERR_NO_DEVICE: return "FGEMM_ERR_NO_DEVICE";
+    case FGEMM_ERR_LAUNCH: return "FGEMM_ERR_LAUNCH";
+    case FGEMM_ERR_TIMEOUT: return "FGEMM_ERR_TIMEOUT";
+    case FGEMM_ERR_WORKSPACE: return "FGEMM_ERR_WORKSPACE";
+    default: return "FGEMM_ERR_UNKNOWN";
+  }
+}
+
+int fgemm_tile_of(int64_t t, int64_t tiles_m, int64_t tiles_n, int group, int64_t* m_tile,
+                  int64_t* n_tile) {
+  if (!m_tile || !n_tile || tiles_m <= 0 || tiles_n <= 0 || group <= 0 || t < 0 ||
+      tiles_m > 0x7fffffffLL || tiles_n > 0x7fffffffLL || t >= tiles_m * tiles_n)
+    return FGEMM_ERR_INVALID_VALUE;
+  int m = 0, n = 0;
+  tile_of(t, static_cast<int>(tiles_m), static_cast<int>(tiles_n), group, m, n);
+  *m_tile = m;
+  *n_tile = n;
+  return FGEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// kernels.h -- internal launch interface between the C ABI (api.cu) and the kernel files.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fgemm {
+
+enum Epi : int { EPI_RELU = 0, EPI_GATE = 1, EPI_NONE = 2 };
+enum Elem : int { ELEM_F16 = 0, ELEM_BF16 = 1, ELEM_F32 = 2 };
+
+inline int elem_bytes(int e) { return e == ELEM_F32 ? 4 : 2; }
+
+// Arguments of the persistent tensor-core kernel (tensor maps travel separately as
+// __grid_constant__ parameters).
+struct TcParams {
+  int M, N, K;
+  int tiles_m, tiles_n, num_tiles, group;
+  int ab_bf16;     // operand (and Y) type: 0 = f16, 1 = bf16
+  int bias_type;   // Elem of the bias
+  int out_type;    // Elem of out
+  const void* bias;
+  const void* Y;   // gate only, M x N operand type
+  uint32_t idesc;  // tcgen05 instruction descriptor
+  uint32_t b_lbo, b_sbo;  // B (MN-major) descriptor byte offsets
+  uint64_t timeout_ns;
+  int* err;        // device error word
+};
+
+// Generic CUDA-core kernel and elementwise kernels: plain pointers.
+struct SimtParams {
+  const void* A;
+  const void* B;
+  const void* bias;  // may be NULL for EPI_NONE
+  const void* Y;
+  void* out;
+  int M, N, K;
+  int ab_type;    // Elem
+  int bias_type;  // Elem
+  int out_type;   // Elem
+};
+
+cudaError_t launch_tc(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                      const CUtensorMap& tmOut, const TcParams& p, int grid, cudaStream_t s);
+size_t tc_smem_bytes();
+int tc_block_m();
+int tc_block_n();
+
+cudaError_t launch_generic(int epi, const SimtParams& p, cudaStream_t s);
+
+// K == 0: out[i,j] = epilogue(0 + bias[j], Y[i,j])
+cudaError_t launch_kzero(int epi, const SimtParams& p, int num_sms, cudaStream_t s);
+
+// Unfused chain pieces.  I is M x N of type inter_type.
+cudaError_t launch_ew_bias_inplace(void* I, int inter_type, const void* bias, int bias_type, int M,
+                                   int N, int num_sms, cudaStream_t s);
+cudaError_t launch_ew_relu(const void* I, int inter_type, void* out, int out_type, int M, int N,
+                           int num_sms, cudaStream_t s);
+cudaError_t launch_ew_bias_gate(const void* I, int inter_type, const void* bias, int bias_type,
+                                const void* Y, int y_type, void* out, int out_type, int M, int N,
+                                int num_sms, cudaStream_t s);
+
+}  // namespace fgemm

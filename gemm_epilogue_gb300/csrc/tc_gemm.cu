@@ -1,0 +1,393 @@
+// tc_gemm.cu -- persistent, warp-specialised TMA + tcgen05 GEMM with a fused epilogue (sm_103a).
+//
+// One CTA per SM walks output tiles of BM x BN = 128 x 256 in grouped-M order (tile_order.h).
+//   warp 0      TMA producer: A tile 128 x 64 (K-major) and B tile 64 x 256 (N-major, four
+//               64-column boxes) per stage into a STAGES-deep shared-memory ring, completion
+//               counted in bytes on full[s]; out-of-range rows / columns / K are zero-filled by
+//               TMA, which is the M/N/K tail mask of "I3. Fuse a GEMM epilogue and change tile
+//               scheduling" ("Tiles and grouped ownership": A's M/K edges, B's K/N edges).
+//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, fp32 accumulate in tensor memory,
+//               128 x 256 accumulator, double-buffered (2 x 256 of the 512 TMEM columns) so the
+//               epilogue of tile i overlaps the mainloop of tile i + 1.  tcgen05.commit releases
+//               each smem stage (empty[s]) and hands a finished accumulator over (acc_full[b]).
+//   warps 2-5   epilogue: each warp owns the 32 TMEM lanes (rows) its warp id allows, and per
+//               64-column chunk: tcgen05.ld -> + bias[j] -> ReLU (fmaxf) or the gate
+//               fma(x, y, x) -> one round-to-nearest conversion -> 128-byte-swizzled staging
+//               buffer -> one TMA store, which clips rows >= M and columns >= N (the store mask).
+//               The bias is read only here, after the reduction ("Triton: Fused Matmul + Bias +
+//               ReLU (Epilogue Fusion)", "Pitfalls": load the bias after the K loop; mask it with
+//               j < N).  The gate's Y chunk is loaded straight into registers ahead of the TMEM
+//               read ("Optimizing GEMM + Activation on CDNA4 with TLX", "Version 4": Y prefetched
+//               into registers, not staged through shared memory) with a streaming hint.
+// The accumulator goes from TMEM to registers to the single store; it never touches HBM.
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_order.h"
+
+namespace fgemm {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;    // 8 KB: 64 K-rows x 64 N-columns
+constexpr uint32_t B_STAGE_BYTES = BK * BN * 2;  // 32 KB
+constexpr uint32_t STAGE_TX = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr uint32_t EPI_BUF_BYTES = 32 * 128;     // 32 rows x 128 bytes
+constexpr uint32_t SMEM_A = 0;
+constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
+constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
+constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
+constexpr uint32_t SMEM_USED = SMEM_BAR + 256;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// barrier slots (uint64 each) inside the SMEM_BAR area
+constexpr int BAR_FULL = 0;
+constexpr int BAR_EMPTY = STAGES;
+constexpr int BAR_ACC_FULL = 2 * STAGES;
+constexpr int BAR_ACC_EMPTY = 2 * STAGES + 2;
+constexpr int BAR_MMA_DONE = 2 * STAGES + 4;
+constexpr uint32_t OFF_TMEM_SLOT = 128;
+constexpr uint32_t OFF_ABORT = 136;
+
+// wait sites recorded with a timeout
+enum { SITE_PROD_EMPTY = 1, SITE_MMA_ACC_EMPTY, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN };
+
+// Bounded wait that ignores the abort flag: used only to drain copies / MMAs already in flight.
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                           int* err) {
+  volatile int never = 0;
+  return mbar_wait(bar, parity, &never, timeout_ns, err, SITE_DRAIN);
+}
+
+template <int OUT_BYTES>
+__device__ __forceinline__ void load_bias_granule(const TcParams& p, int col, float (&b)[16 / OUT_BYTES]) {
+  constexpr int G = 16 / OUT_BYTES;
+  if (col >= p.N) {
+#pragma unroll
+    for (int e = 0; e < G; ++e) b[e] = 0.f;
+    return;
+  }
+  if (p.bias_type == ELEM_F32) {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + col);
+#pragma unroll
+    for (int v = 0; v < G / 4; ++v) {
+      const float4 f = __ldg(src + v);
+      b[4 * v + 0] = f.x; b[4 * v + 1] = f.y; b[4 * v + 2] = f.z; b[4 * v + 3] = f.w;
+    }
+  } else {
+    const bool bf = p.bias_type == ELEM_BF16;
+    const uint16_t* src = static_cast<const uint16_t*>(p.bias) + col;
+    if (G == 8) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int v = 0; v < 4 && v < G / 2; ++v) {
+        const float2 f = unpack2(w[v], bf);
+        b[2 * v] = f.x; b[2 * v + 1] = f.y;
+      }
+    } else {  // G == 4: 4 x 16-bit = 8 bytes
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+      const float2 f0 = unpack2(u.x, bf), f1 = unpack2(u.y, bf);
+      b[0] = f0.x; b[1] = f0.y; b[2 % G] = f1.x; b[3 % G] = f1.y;
+    }
+  }
+}
+
+template <int EPI, int OUT_BYTES>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmOut, const TcParams p) {
+  constexpr int CH = 128 / OUT_BYTES;  // output columns per 128-byte staging row
+  constexpr int NCH = BN / CH;         // chunks per tile
+  constexpr int G = 16 / OUT_BYTES;    // columns per 16-byte granule
+  constexpr int NG = CH / G;           // granules per chunk (8)
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + SMEM_BAR;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + OFF_TMEM_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + OFF_ABORT);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(BAR_FULL + s), 1);
+      mbar_init(bar(BAR_EMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(BAR_ACC_FULL + b), 1);
+      mbar_init(bar(BAR_ACC_EMPTY + b), EPI_WARPS);
+    }
+    mbar_init(bar(BAR_MMA_DONE), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_kb = (p.K + BK - 1) / BK;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_normal();
+      uint32_t stage = 0, phase = 0;
+      uint32_t issued = 0, issued_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_of(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
+        const int m0 = tm * BM, n0 = tn * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err,
+                         SITE_PROD_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar(BAR_FULL + stage);
+          mbar_arrive_expect_tx(fb, STAGE_TX);
+          const uint32_t a_dst = sbase + SMEM_A + stage * A_STAGE_BYTES;
+          const uint32_t b_dst = sbase + SMEM_B + stage * B_STAGE_BYTES;
+          tma_load_2d(a_dst, &tmA, fb, kb * BK, m0, pol);
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_2d(b_dst + c * B_BOX_BYTES, &tmB, fb, n0 + 64 * c, kb * BK, pol);
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every load issued must land before the CTA may exit (also after an abort).
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u) drain_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, tmo, p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      int it = 0;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+        const int b = it & 1;
+        const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
+        if (!mbar_wait(bar(BAR_ACC_EMPTY + b), acc_phase ^ 1u, abort_flag, tmo, p.err,
+                       SITE_MMA_ACC_EMPTY))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(bar(BAR_FULL + stage), phase, abort_flag, tmo, p.err, SITE_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + SMEM_A + stage * A_STAGE_BYTES;
+          const uint32_t b_addr = sbase + SMEM_B + stage * B_STAGE_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
+            const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, p.b_lbo, p.b_sbo);
+            umma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(bar(BAR_EMPTY + stage));  // stage free once these MMAs have read it
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(bar(BAR_ACC_FULL + b));  // accumulator complete: hand it to the epilogue
+      }
+      // All MMAs issued by this thread must finish before TMEM is released.
+      umma_commit(bar(BAR_MMA_DONE));
+      drain_wait(bar(BAR_MMA_DONE), 0, tmo, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int ew = warp - 2;
+    const uint32_t ebuf = sbase + SMEM_EPI + static_cast<uint32_t>(ew) * 2u * EPI_BUF_BYTES;
+    const bool out_bf = p.out_type == ELEM_BF16;
+    const bool y_bf = p.ab_bf16 != 0;
+    const uint64_t pol_out = policy_evict_first();
+    uint32_t nstore = 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+      int tm, tn;
+      tile_of(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
+      const int m0 = tm * BM, n0 = tn * BN;
+      const int b = it & 1;
+      const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
+      const int row0 = m0 + 32 * q;
+      const int row = row0 + lane;
+      const bool rows_live = row0 < p.M;  // warp-uniform
+
+      if (!mbar_wait(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
+        break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
+
+#pragma unroll 1
+      for (int c = 0; c < NCH; ++c) {
+        const int col0 = n0 + c * CH;
+        if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
+
+        // Gate: this thread's row of Y for the chunk, loaded before the TMEM read.
+        uint4 yv[EPI == EPI_GATE ? NG * G / 8 : 1];
+        if constexpr (EPI == EPI_GATE) {
+          const uint16_t* yrow = static_cast<const uint16_t*>(p.Y) + static_cast<int64_t>(row) * p.N;
+#pragma unroll
+          for (int v = 0; v < NG * G / 8; ++v) {
+            const int col = col0 + 8 * v;
+            if (row < p.M && col < p.N)
+              yv[v] = __ldcs(reinterpret_cast<const uint4*>(yrow + col));
+            else
+              yv[v] = make_uint4(0, 0, 0, 0);
+          }
+        }
+
+        uint32_t acc[CH];
+        __syncwarp();  // tcgen05.ld is warp-collective
+        {
+          uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[0]);
+          tmem_ld32(taddr, a0, c * CH);
+          if constexpr (CH == 64) {
+            uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[32]);
+            tmem_ld32(taddr, a1, c * CH + 32);
+          }
+          tmem_ld_wait();
+        }
+
+        // Staging buffer: wait until the store that last read it has finished reading.
+        const uint32_t sb = ebuf + (nstore & 1u) * EPI_BUF_BYTES;
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          float bv[G];
+          if constexpr (EPI != EPI_NONE) load_bias_granule<OUT_BYTES>(p, col0 + g * G, bv);
+          float v[G];
+#pragma unroll
+          for (int e = 0; e < G; ++e) {
+            v[e] = __uint_as_float(acc[g * G + e]);
+            if constexpr (EPI != EPI_NONE) v[e] += bv[e];  // bias once, after the full sum
+          }
+          if constexpr (EPI == EPI_RELU) {
+#pragma unroll
+            for (int e = 0; e < G; ++e) v[e] = fmaxf(v[e], 0.0f);  // branchless clamp
+          }
+          if constexpr (EPI == EPI_GATE) {
+            // 16-bit Y: granule g covers columns g*G .. g*G+G-1 of the chunk
+#pragma unroll
+            for (int e = 0; e < G; e += 2) {
+              const int idx = g * G + e;  // column within the chunk
+              const uint4 u = yv[idx / 8];
+              const uint32_t w = (idx % 8 < 2) ? u.x : (idx % 8 < 4) ? u.y : (idx % 8 < 6) ? u.z : u.w;
+              const float2 y2 = unpack2(w, y_bf);
+              v[e] = fmaf(v[e], y2.x, v[e]);          // X + X * Y
+              v[e + 1] = fmaf(v[e + 1], y2.y, v[e + 1]);
+            }
+          }
+          uint4 packed;
+          if constexpr (OUT_BYTES == 2) {
+            packed.x = pack2(v[0], v[1], out_bf);
+            packed.y = pack2(v[2], v[3], out_bf);
+            packed.z = pack2(v[4 % G], v[5 % G], out_bf);
+            packed.w = pack2(v[6 % G], v[7 % G], out_bf);
+          } else {
+            packed.x = __float_as_uint(v[0]);
+            packed.y = __float_as_uint(v[1]);
+            packed.z = __float_as_uint(v[2 % G]);
+            packed.w = __float_as_uint(v[3 % G]);
+          }
+          // 128-byte swizzle: granule g of row `lane` sits at slot g ^ (lane & 7)
+          const uint32_t dst = sb + static_cast<uint32_t>(lane) * 128u +
+                               (static_cast<uint32_t>(g ^ (lane & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed.x),
+                       "r"(packed.y), "r"(packed.z), "r"(packed.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmOut, sb, col0, row0, pol_out);
+          bulk_commit();
+        }
+        ++nstore;
+      }
+      // This warp has finished reading accumulator b: release it to the MMA warp.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + b));
+    }
+    if (lane == 0) bulk_wait<0>();
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int EPI, int OUT_BYTES>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                       const TcParams& p, int grid, cudaStream_t s) {
+  auto k = tc_gemm_kernel<EPI, OUT_BYTES>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  k<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, o, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+size_t tc_smem_bytes() { return tc::SMEM_BYTES; }
+int tc_block_m() { return tc::BM; }
+int tc_block_n() { return tc::BN; }
+
+cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                      const TcParams& p, int grid, cudaStream_t s) {
+  const bool f32 = p.out_type == ELEM_F32;
+  switch (epi) {
+    case EPI_RELU: return f32 ? tc::launch_one<EPI_RELU, 4>(a, b, o, p, grid, s)
+                              : tc::launch_one<EPI_RELU, 2>(a, b, o, p, grid, s);
+    case EPI_GATE: return f32 ? tc::launch_one<EPI_GATE, 4>(a, b, o, p, grid, s)
+                              : tc::launch_one<EPI_GATE, 2>(a, b, o, p, grid, s);
+    default: return f32 ? tc::launch_one<EPI_NONE, 4>(a, b, o, p, grid, s)
+                        : tc::launch_one<EPI_NONE, 2>(a, b, o, p, grid, s);
+  }
+}
+
+}  // namespace fgemm

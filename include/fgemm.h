@@ -1,0 +1,149 @@
+/*
+ * fgemm.h -- C ABI of the fused GEMM + epilogue library for NVIDIA GB300 (sm_103a).
+ *
+ * Two fused operations, each one kernel launch in which the fp32 accumulator never leaves the chip
+ * (tensor memory) between the end of the K reduction and the single store:
+ *
+ *   fgemm_bias_relu   out[i,j] = max(0, sum_k A[i,k] B[k,j] + bias[j])
+ *       "Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", the defining equation: the bias is
+ *       per column, broadcast over rows, added once after the K loop; "Epilogue concept", "Where
+ *       the accumulator is finally correct": bias and activation run on the complete sum.
+ *
+ *   fgemm_addmm_gate  X = A @ B + bias;  out = X + X * Y
+ *       "Optimizing GEMM + Activation on CDNA4 with TLX", "The GLU Block" (the projection, then
+ *       the elementwise gate with a second tensor Y of the output's shape), evaluated as
+ *       fma(X, Y, X) as in that page's "Version 4: Making the Epilogue Nearly Free".
+ *
+ * Rounding: products are accumulated in fp32; the epilogue runs in fp32; the result is rounded
+ * once (round to nearest even) to the output type at the store ("I3. Fuse a GEMM epilogue and
+ * change tile scheduling", opening paragraph and "Why the baseline uses FP32").
+ *
+ * K = 0 is valid: the zero accumulator still passes through the epilogue, so bias+ReLU gives
+ * ReLU(bias) on every row ("I3 ...", "Implement in stages", stage 2); the gate gives
+ * bias + bias * Y.  A and B may then be NULL.
+ *
+ * Conventions shared by every entry point
+ *   Layout     dense row-major, no leading-dimension arguments: A is M x K, B is K x N, Y and out
+ *              are M x N, bias has N elements.
+ *   Pointers   device pointers owned by the caller.  The library allocates nothing per call.
+ *   Stream     `stream` is a cudaStream_t (NULL = legacy default stream).  Calls return after
+ *              enqueueing the work; in-kernel failures are read with fgemm_device_status().
+ *   Aliasing   out must not overlap A, B, bias or Y (undefined behaviour).
+ *   Sizes      M, N, K >= 0 and each below 2^31; M == 0 or N == 0 returns FGEMM_OK without a launch.
+ *   Alignment  every pointer must be aligned to its element size (else FGEMM_ERR_MISALIGNED).
+ *              The tensor-core path additionally needs 16-byte aligned base pointers and row
+ *              strides (K and N multiples of 8); other shapes run on the generic CUDA-core path,
+ *              which is not an error.
+ *   Threading  no global mutable state apart from the per-device error word.
+ */
+#ifndef FGEMM_H
+#define FGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FGEMM_OK = 0,
+  FGEMM_ERR_INVALID_VALUE = 1,     /* negative size, NULL pointer where data is needed, bad option */
+  FGEMM_ERR_UNSUPPORTED_DTYPE = 2, /* unknown dtype word */
+  FGEMM_ERR_MISALIGNED = 3,        /* a pointer not aligned to its element size */
+  FGEMM_ERR_NO_DEVICE = 4,         /* no current CUDA device, or not compute capability 10.x */
+  FGEMM_ERR_LAUNCH = 5,            /* a CUDA call or kernel launch failed */
+  FGEMM_ERR_TIMEOUT = 6,           /* a device-side wait exceeded its bound (see fgemm_opts) */
+  FGEMM_ERR_WORKSPACE = 7          /* workspace NULL or smaller than required */
+} fgemm_status;
+
+/* dtype word = operand type | bias type | output type.  Y has the operand type. */
+#define FGEMM_F16 0x1        /* A, B (and Y) are IEEE binary16 */
+#define FGEMM_BF16 0x2       /* A, B (and Y) are bfloat16 */
+#define FGEMM_BIAS_SAME 0x00 /* bias has the operand type */
+#define FGEMM_BIAS_F32 0x10  /* bias is fp32 */
+#define FGEMM_OUT_SAME 0x000 /* out has the operand type */
+#define FGEMM_OUT_F32 0x100  /* out is fp32 */
+
+/* Kernel paths (fgemm_opts.path, and *path_taken of the _ex entries). */
+#define FGEMM_PATH_AUTO 0    /* library choice */
+#define FGEMM_PATH_TC 1      /* persistent TMA + tcgen05 kernel, grouped-M tile order */
+#define FGEMM_PATH_SKINNY 2  /* swap-AB split-K kernel for small M (bias+ReLU only) */
+#define FGEMM_PATH_GENERIC 3 /* CUDA-core tiled kernel: any shape and alignment */
+#define FGEMM_PATH_KZERO 4   /* K == 0: epilogue over the zero accumulator, no MMA */
+#define FGEMM_PATH_NONE 5    /* M == 0 or N == 0: nothing launched */
+
+/* Per-call options of the _ex entry points.  Zero-initialised fields mean "default". */
+typedef struct {
+  int group_m;    /* M-tiles per band of the grouped tile order (default 8; 1 = row-major) */
+  int path;       /* FGEMM_PATH_*; forcing a path the shape cannot take -> INVALID_VALUE */
+  int split_k;    /* skinny path: K splits (1..8, one CTA each in a cluster); 0 = automatic */
+  int max_ctas;   /* persistent grid cap (default: one CTA per SM) */
+  int timeout_ms; /* bound on every device-side barrier wait (default 1000 ms) */
+  int b_desc_swap; /* diagnostic: exchange the two byte offsets of B's shared-memory descriptor */
+  int reserved[2];
+} fgemm_opts;
+
+/*
+ * out = ReLU(A @ B + bias).  dtype: FGEMM_F16|FGEMM_BF16, optionally | FGEMM_BIAS_F32 and/or
+ * | FGEMM_OUT_F32.  Returns an fgemm_status.
+ */
+int fgemm_bias_relu(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                    int64_t N, int64_t K, int dtype, void* stream);
+
+/* X = A @ B + bias; out = X + X * Y (Y: M x N, operand type).  Returns an fgemm_status. */
+int fgemm_addmm_gate(const void* A, const void* B, const void* bias, const void* Y, void* out,
+                     int64_t M, int64_t N, int64_t K, int dtype, void* stream);
+
+/* As above, with options (may be NULL) and the path that ran (may be NULL). */
+int fgemm_bias_relu_ex(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                       int64_t N, int64_t K, int dtype, void* stream, const fgemm_opts* opts,
+                       int* path_taken);
+int fgemm_addmm_gate_ex(const void* A, const void* B, const void* bias, const void* Y, void* out,
+                        int64_t M, int64_t N, int64_t K, int dtype, void* stream,
+                        const fgemm_opts* opts, int* path_taken);
+
+/*
+ * Unfused comparison chain (for measuring the traffic that fusion removes; not a fast path).
+ * "Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "The HBM traffic - the whole point":
+ * the GEMM writes an intermediate I, a bias kernel reads and rewrites I, a ReLU kernel reads I
+ * and writes out (three launches).  "Optimizing GEMM + Activation on CDNA4 with TLX", "The GLU
+ * Block": the GEMM writes I, one gate kernel reads I and Y and writes out (two launches).
+ * I lives in the caller's `workspace` (device memory of at least
+ * fgemm_unfused_workspace_bytes() bytes, 256-byte aligned).  inter_f32 = 1 keeps I in fp32, else
+ * I has the output type.
+ */
+size_t fgemm_unfused_workspace_bytes(int64_t M, int64_t N, int dtype, int inter_f32);
+int fgemm_unfused_bias_relu(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                            int64_t N, int64_t K, int dtype, void* workspace,
+                            size_t workspace_bytes, int inter_f32, void* stream);
+int fgemm_unfused_addmm_gate(const void* A, const void* B, const void* bias, const void* Y,
+                             void* out, int64_t M, int64_t N, int64_t K, int dtype,
+                             void* workspace, size_t workspace_bytes, int inter_f32,
+                             void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's error word.  *code receives 0
+ * or the first in-kernel failure since the last call (an fgemm_status in the low byte, the
+ * failing wait's site in the next byte).  Returns FGEMM_OK, or FGEMM_ERR_LAUNCH if the stream
+ * reported a CUDA error.
+ */
+int fgemm_device_status(void* stream, int* code);
+
+/* Human-readable name of an fgemm_status. */
+const char* fgemm_status_string(int status);
+
+/*
+ * The persistent kernels' tile order, exposed for host-side tests: linear tile t of a
+ * tiles_m x tiles_n grid with `group` M-tiles per band ("I3. Fuse a GEMM epilogue and change tile
+ * scheduling", "Tiles and grouped ownership").  Returns FGEMM_ERR_INVALID_VALUE when t is out of
+ * range or a count is not positive.
+ */
+int fgemm_tile_of(int64_t t, int64_t tiles_m, int64_t tiles_n, int group, int64_t* m_tile,
+                  int64_t* n_tile);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FGEMM_H */

@@ -1,0 +1,97 @@
+"""Helpers for the GPU parity tests: uploads, tolerance checks against the oracle."""
+import math
+
+import numpy as np
+
+import oracle
+
+F16, BF16, F32 = 1, 2, 3
+
+
+def torch_dtype(t):
+    import torch
+    return {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}[t]
+
+
+def up(a, t, dev="cuda"):
+    """numpy bits (uint16) or float32 -> device tensor of type t."""
+    import torch
+    if a is None:
+        return None
+    if t == F32:
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch_dtype(t)).to(dev)
+
+
+def down(x, t):
+    """device tensor -> numpy bits (uint16) or float32."""
+    import torch
+    x = x.detach().cpu().contiguous()
+    if t == F32:
+        return x.numpy().astype(np.float32)
+    return x.view(torch.int16).numpy().view(np.uint16)
+
+
+def dtype_word(ab, bias, out):
+    import gemm_epilogue_gb300.binding as fg
+    w = fg.F16 if ab == F16 else fg.BF16
+    if bias == F32:
+        w |= fg.BIAS_F32
+    elif bias != ab:
+        raise ValueError("bias type must be the operand type or f32")
+    if out == F32:
+        w |= fg.OUT_F32
+    elif out != ab:
+        raise ValueError("out type must be the operand type or f32")
+    return w
+
+
+def ulp(x, t):
+    """Spacing of type t at |x| (the gap to the next representable magnitude)."""
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    p, emin = {F16: (11, -14), BF16: (8, -126), F32: (24, -126)}[t]
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** emin)))
+    return np.exp2(np.maximum(e, emin) - (p - 1))
+
+
+def tolerance(K, ref_vals, out_type):
+    """Stated tolerance: max|err| <= 2e-2 sqrt(K/4096) max|ref| + 1e-3 (16-bit outputs),
+    1e-4 relative for fp32 outputs."""
+    m = float(np.abs(ref_vals).max()) if ref_vals.size else 0.0
+    if out_type == F32:
+        return 1e-4 * m
+    return 2e-2 * math.sqrt(K / 4096.0) * m + 1e-3
+
+
+def check_close(got_bits, res, K, out_type, Y64=None, bias64=None, what=""):
+    """Stated tolerance plus the per-element forward-error bound.
+
+    Secondary bound per element: |gpu - oracle| <= 1 ulp(out) + K * 2^-22 * (sum|a b| + |bias|)
+    * (1 + |y|): an fp32 recursive sum of K products (with a margin for the tensor core's
+    accumulation) and one rounding of each result to the output type.
+    """
+    got = oracle.decode(got_bits, out_type)
+    ref = oracle.decode(res.out, out_type)
+    err = np.abs(got - ref)
+    tol = tolerance(K, ref, out_type)
+    worst = float(err.max()) if err.size else 0.0
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert worst <= tol, f"{what}: max|err| {worst:.4g} > tolerance {tol:.4g}"
+    scale = res.absdot + (np.abs(bias64)[None, :] if bias64 is not None else 0.0)
+    if Y64 is not None:
+        scale = scale * (1.0 + np.abs(Y64))
+    bound = ulp(np.maximum(np.abs(ref), np.abs(got)), out_type) + K * 2.0 ** -22 * scale + 1e-30
+    bad = err > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements exceed the forward-error bound " \
+                          f"(first at {np.argwhere(bad)[0]}, err {err[bad][0]:.3g}, bound {bound[bad][0]:.3g})"
+    return worst, tol
+
+
+def sample_rows(M, BM=128, n_random=64, seed=0):
+    """Rows for full-size parity: first and last rows, every row of the last (ragged) M tile,
+    and a seeded random sample."""
+    rng = np.random.default_rng(seed)
+    rows = {0, M - 1}
+    rows.update(range(max(0, (M - 1) // BM * BM), M))
+    rows.update(int(r) for r in rng.integers(0, M, min(n_random, M)))
+    return np.array(sorted(rows), dtype=np.int64)

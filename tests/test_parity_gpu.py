@@ -1,0 +1,249 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded inputs."""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import parse_matrix, read_golden
+from gemm_epilogue_gb300 import inputs as gen
+from gpu_util import (BF16, F16, F32, check_close, down, dtype_word, sample_rows, up)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import gemm_epilogue_gb300.binding as fg  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gemm_epilogue_gb300 import build
+    build.build()
+    oracle.build()
+    fg.lib()
+    yield
+    assert fg.fgemm_device_status() == 0
+
+
+def run_fused(p, M, N, K, ab, bt, ot, gate=False, opts=None, out=None):
+    A, B = up(p.A, ab), up(p.B, ab)
+    bias = up(p.bias, bt)
+    Y = up(p.Y, ab) if gate else None
+    if out is None:
+        out = torch.empty(M, N, dtype={F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}[ot],
+                          device="cuda")
+    w = dtype_word(ab, bt, ot)
+    if gate:
+        path = fg.fgemm_addmm_gate_ex(A, B, bias, Y, out, M, N, K, w, opts=opts)
+    else:
+        path = fg.fgemm_bias_relu_ex(A, B, bias, out, M, N, K, w, opts=opts)
+    torch.cuda.synchronize()
+    return out, path
+
+
+def oracle_run(p, M, N, K, ab, bt, ot, gate=False, rows=None):
+    if gate:
+        return oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, ab, bt, ot, rows=rows)
+    return oracle.bias_relu(p.A, p.B, p.bias, M, N, K, ab, bt, ot, rows=rows)
+
+
+# ------------------------------------------------------------ exact small cases --
+
+@pytest.mark.parametrize("ab,bt,ot", [(F16, F16, F16), (BF16, BF16, BF16), (F16, F32, F32)])
+def test_worked_example(ab, bt, ot):
+    g = read_golden("worked_example_2x2.txt")
+    A = oracle.encode(np.array(parse_matrix(g["A"])), ab)
+    B = oracle.encode(np.array(parse_matrix(g["B"])), ab)
+    bias = oracle.encode(np.array(parse_matrix(g["bias"])[0]), bt)
+    p = gen.Inputs(A, B, bias, None)
+    out, path = run_fused(p, 2, 2, 2, ab, bt, ot)
+    assert path == fg.PATH_GENERIC
+    assert np.array_equal(oracle.decode(down(out, ot), ot), np.array(parse_matrix(g["relu"])))
+
+
+@pytest.mark.parametrize("gate", [False, True])
+@pytest.mark.parametrize("ab,bt,ot", [(F16, F32, F16), (BF16, BF16, BF16), (BF16, BF16, F32)])
+def test_k_zero(gate, ab, bt, ot):
+    M, N = 37, 70
+    p = gen.random_problem(M, N, 0, ab, bt, seed=1, gate=gate)
+    out, path = run_fused(gen.Inputs(None, None, p.bias, p.Y), M, N, 0, ab, bt, ot, gate=gate)
+    assert path == fg.PATH_KZERO
+    ref = oracle_run(gen.Inputs(None, None, p.bias, p.Y), M, N, 0, ab, bt, ot, gate=gate)
+    assert np.array_equal(down(out, ot), ref.out)
+
+
+@pytest.mark.parametrize("K", [1, 3])
+def test_k1_k3_fused_matches_oracle_and_unfused_chain(K):
+    # "Epilogue concept", "Things that break": same shape at K = 1 and K = 3.
+    M, N = 37, 45
+    p = gen.integer_problem(M, N, K, F16, F16, seed=K)
+    out, _ = run_fused(p, M, N, K, F16, F16, F16)
+    ref = oracle_run(p, M, N, K, F16, F16, F16)
+    assert np.array_equal(down(out, F16), ref.out)
+    ws_bytes = fg.fgemm_unfused_workspace_bytes(M, N, fg.F16, 1)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out2 = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    fg.fgemm_unfused_bias_relu(up(p.A, F16), up(p.B, F16), up(p.bias, F16), out2, M, N, K, fg.F16,
+                               ws, ws_bytes, 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(down(out2, F16), ref.out)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 2), (7, 9, 40), (17, 33, 13), (40, 40, 39),
+                                   (65, 3, 31), (2, 129, 17)])
+def test_brute_force_ragged_generic_bit_exact(M, N, K):
+    for ab, bt, ot in ((F16, F16, F16), (BF16, F32, BF16)):
+        p = gen.integer_problem(M, N, K, ab, bt, seed=M + N + K)
+        out, path = run_fused(p, M, N, K, ab, bt, ot)
+        assert path == fg.PATH_GENERIC
+        assert np.array_equal(down(out, ot), oracle_run(p, M, N, K, ab, bt, ot).out)
+        g = gen.integer_problem(M, N, K, ab, bt, seed=M * N + K, gate=True)
+        out, _ = run_fused(g, M, N, K, ab, bt, ot, gate=True)
+        assert np.array_equal(down(out, ot), oracle_run(g, M, N, K, ab, bt, ot, gate=True).out)
+
+
+# ------------------------------------------------------ tensor-core path, exact --
+
+TC_SHAPES = [(1, 8, 8), (128, 256, 64), (200, 136, 72), (129, 264, 136), (300, 520, 200),
+             (77, 1032, 24), (513, 264, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", TC_SHAPES)
+@pytest.mark.parametrize("ab", [F16, BF16])
+def test_tc_integer_bit_exact(M, N, K, ab):
+    # Small integers: every partial sum is exact in fp32, so the only rounding is the final one
+    # and the tensor-core result must equal the oracle bit for bit.  Shapes are ragged against the
+    # 128 x 256 x 64 tile in M, N and K.
+    p = gen.integer_problem(M, N, K, ab, ab, seed=M * 7 + N + K)
+    out, path = run_fused(p, M, N, K, ab, ab, ab)
+    assert path == fg.PATH_TC
+    ref = oracle_run(p, M, N, K, ab, ab, ab)
+    got = down(out, ab)
+    if not np.array_equal(got, ref.out):
+        bad = np.argwhere(got != ref.out)
+        pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 136, 72), (300, 520, 200)])
+def test_tc_gate_integer_bit_exact(M, N, K):
+    for ab, ot in ((F16, F16), (BF16, F32)):
+        p = gen.integer_problem(M, N, K, ab, ab, seed=K, gate=True)
+        out, path = run_fused(p, M, N, K, ab, ab, ot, gate=True)
+        assert path == fg.PATH_TC
+        assert np.array_equal(down(out, ot), oracle_run(p, M, N, K, ab, ab, ot, gate=True).out)
+
+
+@pytest.mark.parametrize("bt,ot", [(F32, F32), (F32, F16), (F16, F32)])
+def test_tc_bias_and_output_types(bt, ot):
+    M, N, K = 150, 392, 96
+    p = gen.integer_problem(M, N, K, F16, bt, seed=5)
+    out, path = run_fused(p, M, N, K, F16, bt, ot)
+    assert path == fg.PATH_TC
+    assert np.array_equal(down(out, ot), oracle_run(p, M, N, K, F16, bt, ot).out)
+
+
+# ----------------------------------------------------------- float tolerance --
+
+def test_small_ragged_workload_tc_and_generic():
+    w = gen.WORKLOADS["ragged_200x136x72"]
+    x = gen.make(w)
+    ref = oracle_run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type)
+    b64 = oracle.decode(x.bias, w.bias_type)
+    for path in (fg.PATH_TC, fg.PATH_GENERIC):
+        out, taken = run_fused(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, opts={"path": path})
+        assert taken == path
+        check_close(down(out, w.out_type), ref, w.K, w.out_type, bias64=b64, what=f"path {path}")
+
+
+@pytest.mark.parametrize("gate", [False, True])
+def test_random_tc_unit_scale(gate):
+    # unit-scale inputs: the GEMM term dominates the bias, so the tolerance is sensitive to it
+    M, N, K = 333, 776, 1024
+    p = gen.random_problem(M, N, K, BF16, BF16, seed=9, scale=K ** -0.25, gate=gate)
+    out, path = run_fused(p, M, N, K, BF16, BF16, BF16, gate=gate)
+    assert path == fg.PATH_TC
+    ref = oracle_run(p, M, N, K, BF16, BF16, BF16, gate=gate)
+    check_close(down(out, BF16), ref, K, BF16, Y64=oracle.decode(p.Y, BF16) if gate else None,
+                bias64=oracle.decode(p.bias, BF16), what="unit-scale")
+
+
+# ----------------------------------------------------- coverage and ordering --
+
+@pytest.mark.parametrize("M,N,K", [(200, 136, 72), (513, 776, 64)])
+def test_tile_coverage_sentinel_and_guards(M, N, K):
+    # every output element written once, nothing written outside out ("I3 ...": every tile exactly
+    # once; "Triton: ReLU ...", "Mask discipline": the store mask protects memory past the end)
+    p = gen.random_problem(M, N, K, F16, F16, seed=2)
+    guard = 4096
+    buf = torch.full((guard + M * N + guard,), float("nan"), dtype=torch.float16, device="cuda")
+    out = buf[guard:guard + M * N].view(M, N)
+    _, path = run_fused(p, M, N, K, F16, F16, F16, out=out)
+    assert path == fg.PATH_TC
+    b = buf.cpu()
+    assert torch.isnan(b[:guard]).all() and torch.isnan(b[guard + M * N:]).all()
+    assert not torch.isnan(b[guard:guard + M * N]).any()
+
+
+def test_grouping_and_grid_do_not_change_results():
+    M, N, K = 700, 1800, 128
+    p = gen.random_problem(M, N, K, BF16, BF16, seed=4)
+    base, _ = run_fused(p, M, N, K, BF16, BF16, BF16)
+    for opts in ({"group_m": 1}, {"group_m": 4}, {"group_m": 3, "max_ctas": 7}, {"max_ctas": 1}):
+        out, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts=opts)
+        assert torch.equal(out, base), opts
+
+
+# -------------------------------------------------------------- unfused chain --
+
+@pytest.mark.parametrize("inter_f32", [0, 1])
+@pytest.mark.parametrize("gate", [False, True])
+def test_unfused_chain_matches_oracle(inter_f32, gate):
+    M, N, K = 257, 520, 192
+    p = gen.random_problem(M, N, K, F16, F16, seed=8, gate=gate)
+    ref = oracle_run(p, M, N, K, F16, F16, F16, gate=gate)
+    ws_bytes = fg.fgemm_unfused_workspace_bytes(M, N, fg.F16, inter_f32)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    args = (up(p.A, F16), up(p.B, F16), up(p.bias, F16))
+    if gate:
+        fg.fgemm_unfused_addmm_gate(*args, up(p.Y, F16), out, M, N, K, fg.F16, ws, ws_bytes, inter_f32)
+    else:
+        fg.fgemm_unfused_bias_relu(*args, out, M, N, K, fg.F16, ws, ws_bytes, inter_f32)
+    torch.cuda.synchronize()
+    got = oracle.decode(down(out, F16), F16)
+    want = oracle.decode(ref.out, F16)
+    from gpu_util import tolerance
+    assert float(np.abs(got - want).max()) <= tolerance(K, want, F16)
+
+
+# ------------------------------------------------------------ full-size sampled --
+
+FULL = ["square_4096", "glu_gate_1024x21568x4096", "ffn_up_8192x14336x4096", "skinny_M1_8192",
+        "skinny_M16_8192", "skinny_M64_8192", "skinny_M128_8192"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_sampled_rows(name):
+    w = gen.WORKLOADS[name]
+    x = gen.make(w)
+    gate = w.epilogue == "gate"
+    out, path = run_fused(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, gate=gate)
+    rows = sample_rows(w.M)
+    ref = oracle_run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, gate=gate, rows=rows)
+    got = down(out, w.out_type)[rows]
+    Y64 = oracle.decode(x.Y[rows], w.ab_type) if gate else None
+    b64 = oracle.decode(x.bias, w.bias_type)
+    check_close(got, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what=name)
+    # negative control: an output that left out the GEMM term must fail the per-element bound
+    fake = oracle.gemm_epilogue(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type,
+                                w.out_type, oracle.EPI_GATE if gate else oracle.EPI_RELU,
+                                Y=x.Y, rows=rows, mutant=oracle.MUT_DROP_GEMM)
+    with pytest.raises(AssertionError):
+        check_close(fake.out, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what="bias-only control")
+
+
+def test_device_error_word_clear():
+    assert fg.fgemm_device_status() == 0
