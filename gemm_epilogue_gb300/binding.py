@@ -58,6 +58,8 @@ _SIGS = {
                                        _int, _vp]),
     "fgemm_unfused_addmm_gate": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp,
                                         _sz, _int, _vp]),
+    "fgemm_unfused_bias_relu_noalloc": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int,
+                                               _vp]),
     "fgemm_device_status": (_int, [_vp, ctypes.POINTER(_int)]),
     "fgemm_status_string": (ctypes.c_char_p, [_int]),
     "fgemm_tile_of": (_int, [_i64, _i64, _i64, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
@@ -165,6 +167,19 @@ def fgemm_unfused_addmm_gate(A, B, bias, Y, out, M, N, K, dtype, workspace, work
                                           K, dtype, _ptr(workspace), workspace_bytes,
                                           int(inter_f32), _stream(stream)),
            "fgemm_unfused_addmm_gate")
+
+
+# Size of the library's own intermediate array used by fgemm_unfused_bias_relu_noalloc.
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def fgemm_unfused_bias_relu_noalloc(A, B, bias, out, M, N, K, dtype, inter_f32=0,
+                                    stream=None) -> None:
+    """Unfused bias + ReLU chain whose intermediate lives in the library's fixed device array
+    (for callers that cannot allocate device memory); see include/fgemm.h."""
+    _check(lib().fgemm_unfused_bias_relu_noalloc(_ptr(A), _ptr(B), _ptr(bias), _ptr(out), M, N,
+                                                 K, dtype, int(inter_f32), _stream(stream)),
+           "fgemm_unfused_bias_relu_noalloc")
 
 
 def fgemm_device_status(stream=None) -> int:

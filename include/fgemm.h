@@ -123,6 +123,31 @@ int fgemm_unfused_addmm_gate(const void* A, const void* B, const void* bias, con
                              void* stream);
 
 /*
+ * fgemm_unfused_bias_relu_noalloc -- the unfused bias + ReLU chain with no allocation at all.
+ * (The pages have no counterpart: this entry exists only for callers of this library.)
+ *
+ * For callers that must not allocate device memory: for example code that runs inside a host
+ * application which reserves the device's whole memory budget up front and hands out no more,
+ * or a serving loop that forbids cudaMalloc / cudaFree after start-up because they can fail
+ * there, or synchronise the device and stall other streams.  Instead of a caller-provided
+ * workspace, the intermediate lives in a fixed array of FGEMM_NOALLOC_SCRATCH_BYTES bytes that
+ * the library reserves in device memory; every device that loads the library holds it until the
+ * process exits.  This call allocates nothing, and calls no allocating library routine.
+ *
+ * Arguments, layout, ownership and the result are those of fgemm_unfused_bias_relu minus the
+ * workspace.  Limit: fgemm_unfused_workspace_bytes(M, N, dtype, inter_f32) must not exceed
+ * FGEMM_NOALLOC_SCRATCH_BYTES, else FGEMM_ERR_WORKSPACE is returned and nothing runs.
+ * The first call on each device (with that device current) looks up the array's device address
+ * once; make that first call before any stream capture.  All calls share the array and it keeps
+ * the previous call's contents (nothing in it needs to start at zero: each call writes every
+ * intermediate element before reading it); calls whose work overlaps on the GPU race on it.
+ */
+#define FGEMM_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int fgemm_unfused_bias_relu_noalloc(const void* A, const void* B, const void* bias, void* out,
+                                    int64_t M, int64_t N, int64_t K, int dtype, int inter_f32,
+                                    void* stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's error word.  *code receives 0
  * or the first in-kernel failure since the last call (an fgemm_status in the low byte, the
  * failing wait's site in the next byte).  Returns FGEMM_OK, or FGEMM_ERR_LAUNCH if the stream
