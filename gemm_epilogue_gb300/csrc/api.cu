@@ -202,6 +202,43 @@ int run_tc(const Call& c, DeviceInfo* d) {
   return status_of(launch_tc(c.epi, tmA, tmB, tmO, p, grid, c.stream));
 }
 
+int run_skinny(const Call& c, DeviceInfo* d) {
+  const int BN = skinny_block_n();
+  const int mpad = static_cast<int>((c.M + 15) / 16 * 16);
+  CUtensorMap tmB, tmA;
+  if (!encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
+      !encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, static_cast<uint32_t>(mpad), 64))
+    return FGEMM_ERR_LAUNCH;
+  SkParams p{};
+  p.M = static_cast<int>(c.M);
+  p.N = static_cast<int>(c.N);
+  p.K = static_cast<int>(c.K);
+  p.mpad = mpad;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < mpad) p.tmem_cols *= 2;
+  const int tiles_n = static_cast<int>((c.N + BN - 1) / BN);
+  const int kb = static_cast<int>((c.K + 63) / 64);
+  int split = (c.opts && c.opts->split_k > 0) ? c.opts->split_k : 0;
+  if (split == 0) {  // enough clusters to cover the SMs, each split at least 4 K blocks
+    split = d->num_sms / (tiles_n > 0 ? tiles_n : 1);
+    if (split > kb / 4) split = kb / 4;
+    if (split > 8) split = 8;
+    if (split < 1) split = 1;
+  }
+  p.split = split;
+  p.ab_type = c.t.ab;
+  p.bias_type = c.t.bias;
+  p.out_type = c.t.out;
+  p.bias = c.bias;
+  p.Y = c.Y;
+  p.out = c.out;
+  p.idesc = idesc_f16_f32acc(c.t.ab == ELEM_BF16, BN, mpad, /*a_mn=*/true, /*b_mn=*/false);
+  const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
+  p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
+  p.err = d->err;
+  return status_of(launch_skinny(c.epi, tmB, tmA, p, tiles_n, c.stream));
+}
+
 SimtParams simt_params(const Call& c) {
   SimtParams p{};
   p.A = c.A;
@@ -225,17 +262,21 @@ int dispatch(const Call& c, DeviceInfo* d, int* path_taken) {
   if (forced == FGEMM_PATH_AUTO) {
     if (c.K == 0)
       path = (c.epi == EPI_NONE) ? FGEMM_PATH_GENERIC : FGEMM_PATH_KZERO;
+    else if (!tc_eligible(c))
+      path = FGEMM_PATH_GENERIC;
     else
-      path = tc_eligible(c) ? FGEMM_PATH_TC : FGEMM_PATH_GENERIC;
+      path = (c.M <= skinny_max_m()) ? FGEMM_PATH_SKINNY : FGEMM_PATH_TC;
   } else {
     path = forced;
     if (path == FGEMM_PATH_TC && (c.K == 0 || !tc_eligible(c))) return FGEMM_ERR_INVALID_VALUE;
+    if (path == FGEMM_PATH_SKINNY && (c.K == 0 || !tc_eligible(c) || c.M > skinny_max_m()))
+      return FGEMM_ERR_INVALID_VALUE;
     if (path == FGEMM_PATH_KZERO && (c.K != 0 || c.epi == EPI_NONE)) return FGEMM_ERR_INVALID_VALUE;
-    if (path == FGEMM_PATH_SKINNY) return FGEMM_ERR_INVALID_VALUE;  // not available for this call
   }
   if (path_taken) *path_taken = path;
   switch (path) {
     case FGEMM_PATH_TC: return run_tc(c, d);
+    case FGEMM_PATH_SKINNY: return run_skinny(c, d);
     case FGEMM_PATH_KZERO: return status_of(launch_kzero(c.epi, simt_params(c), d->num_sms, c.stream));
     default: return status_of(launch_generic(c.epi, simt_params(c), c.stream));
   }

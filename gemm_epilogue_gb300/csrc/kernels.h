@@ -46,6 +46,25 @@ size_t tc_smem_bytes();
 int tc_block_m();
 int tc_block_n();
 
+// Small-M kernel (swap-AB, split-K over a cluster, reduction through distributed shared memory).
+struct SkParams {
+  int M, N, K;
+  int mpad;       // M rounded up to a multiple of 16 (the MMA's N), <= 128
+  int tmem_cols;  // power of two >= 32 and >= mpad
+  int split;      // CTAs per cluster splitting K (1..8)
+  int ab_type, bias_type, out_type;  // Elem
+  const void* bias;
+  const void* Y;
+  void* out;
+  uint32_t idesc;
+  uint64_t timeout_ns;
+  int* err;
+};
+cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA,
+                          const SkParams& p, int tiles_n, cudaStream_t s);
+int skinny_block_n();
+int skinny_max_m();
+
 cudaError_t launch_generic(int epi, const SimtParams& p, cudaStream_t s);
 
 // K == 0: out[i,j] = epilogue(0 + bias[j], Y[i,j])

@@ -1,0 +1,279 @@
+// skinny.cu -- fused GEMM + epilogue for small M (decode-like: a few to 128 rows), sm_103a.
+//
+// With M <= 128 the square-tile kernel has too few tiles to keep the GPU busy and the time is
+// the stream of B (K x N) from HBM.  This kernel therefore
+//   * swaps the operands: out^T (N x M) = B^T A^T, so the 128-row MMA dimension runs over N (128
+//     output columns per tile) and the MMA's N is M rounded up to 16 (rows >= M are zero-filled
+//     by TMA); B is read N-major exactly as it lies in memory, A K-major;
+//   * splits K over the S CTAs of a thread-block cluster (one N tile per cluster), each CTA
+//     streaming its K range of B through a 6-stage TMA ring into tcgen05.mma (fp32 in TMEM);
+//   * reduces the S partial accumulators through distributed shared memory: each CTA copies its
+//     partial from TMEM to its own shared memory, the cluster synchronises, and CTA r sums rows
+//     [r*128/S, (r+1)*128/S) of the tile over all S CTAs;
+//   * applies the epilogue once, on the complete sum ("Epilogue concept", "Why it cannot move
+//     earlier": ReLU of a partial sum is not ReLU of the sum, and a bias added per partial would be
+//     added S times): x = sum + bias[n], then ReLU or the gate, one rounding, coalesced store.
+// No workspace in global memory: the reduction stays on chip.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace fgemm {
+namespace sk {
+
+constexpr int BN = 128;  // output columns per tile (MMA M)
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t B_BOX_BYTES = 64 * 64 * 2;        // 64 K-rows x 64 N-columns
+constexpr uint32_t B_STAGE_BYTES = 2 * B_BOX_BYTES;  // 64 x 128
+constexpr int MAX_MPAD = 128;
+constexpr uint32_t BAR_BYTES = 256;
+
+enum { SITE_PROD_EMPTY = 16, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN };
+
+__host__ __device__ inline uint32_t stage_bytes(int mpad) {
+  return B_STAGE_BYTES + static_cast<uint32_t>(mpad) * 128u;
+}
+__host__ inline uint32_t smem_bytes(int mpad) {
+  return STAGES * stage_bytes(mpad) + BAR_BYTES + 1024;
+}
+
+__device__ __forceinline__ float ld_any(const void* p, int64_t i, int type) {
+  switch (type) {
+    case ELEM_F16: return __half2float(static_cast<const __half*>(p)[i]);
+    case ELEM_BF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+    default: return static_cast<const float*>(p)[i];
+  }
+}
+__device__ __forceinline__ void st_any(void* p, int64_t i, int type, float v) {
+  switch (type) {
+    case ELEM_F16: static_cast<__half*>(p)[i] = __float2half_rn(v); break;
+    case ELEM_BF16: static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v); break;
+    default: static_cast<float*>(p)[i] = v; break;
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
+                  const SkParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sbytes = stage_bytes(p.mpad);
+  const uint32_t bar0 = sbase + STAGES * sbytes;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  // barriers: full[0..5], empty[6..11], acc_full 12, mma_done 13
+  constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_ACC_FULL = 2 * STAGES,
+                BAR_MMA_DONE = 2 * STAGES + 1;
+  uint8_t* bar_area = smem + STAGES * sbytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 136);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t S = static_cast<uint32_t>(p.split);
+  const uint32_t rank = (S > 1) ? cluster_ctarank() : 0u;
+  const int tile = static_cast<int>(blockIdx.x / S);
+  const int n0 = tile * BN;
+  const int KB = (p.K + BK - 1) / BK;
+  const int kb0 = static_cast<int>(static_cast<int64_t>(KB) * rank / S);
+  const int kb1 = static_cast<int>(static_cast<int64_t>(KB) * (rank + 1) / S);
+  const int nkb = kb1 - kb0;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(BAR_FULL + s), 1);
+      mbar_init(bar(BAR_EMPTY + s), 1);
+    }
+    mbar_init(bar(BAR_ACC_FULL), 1);
+    mbar_init(bar(BAR_MMA_DONE), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmA);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_b = policy_evict_first();   // B is streamed once
+      const uint64_t pol_a = policy_evict_last();    // A is re-read by every N tile
+      uint32_t stage = 0, phase = 0, issued = 0, issued_parity = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err, SITE_PROD_EMPTY))
+          break;
+        const uint32_t fb = bar(BAR_FULL + stage);
+        mbar_arrive_expect_tx(fb, sbytes);
+        const uint32_t dst = sbase + stage * sbytes;
+        tma_load_2d(dst, &tmB, fb, n0, kb * BK, pol_b);
+        tma_load_2d(dst + B_BOX_BYTES, &tmB, fb, n0 + 64, kb * BK, pol_b);
+        tma_load_2d(dst + B_STAGE_BYTES, &tmA, fb, kb * BK, 0, pol_a);
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      volatile int never = 0;
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          mbar_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, &never, tmo, p.err, SITE_DRAIN);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(bar(BAR_FULL + stage), phase, abort_flag, tmo, p.err, SITE_MMA_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t b_addr = sbase + stage * sbytes;       // MMA operand A: B^T, N-major
+        const uint32_t a_addr = b_addr + B_STAGE_BYTES;       // MMA operand B: A^T, K-major
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t da = sdesc_sw128(b_addr + 2048u * k, B_BOX_BYTES, 1024u);
+          const uint64_t db = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
+          umma_f16(tmem_base, da, db, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+        }
+        umma_commit(bar(BAR_EMPTY + stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok && nkb > 0) umma_commit(bar(BAR_ACC_FULL));
+      umma_commit(bar(BAR_MMA_DONE));
+      volatile int never = 0;
+      mbar_wait(bar(BAR_MMA_DONE), 0, &never, tmo, p.err, SITE_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------ partial: TMEM -> shared
+    // partial[n][m], row stride mpad + 1 floats, overlays the (now idle) stage buffers
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    float* partial = reinterpret_cast<float*>(smem);
+    const int stride = p.mpad + 1;
+    bool have = nkb > 0;
+    if (have) {
+      have = mbar_wait(bar(BAR_ACC_FULL), 0, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL);
+      tc_fence_after();
+    }
+    if (have) {
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+      for (int c = 0; c < p.mpad / 16; ++c) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld16(taddr + 16u * c, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) partial[row * stride + 16 * c + j] = __uint_as_float(v[j]);
+      }
+    } else {
+      for (int m = 0; m < p.mpad; ++m) partial[row * stride + m] = 0.f;
+    }
+    tc_fence_before();
+  }
+
+  // ------------------------------------------------------------ reduction across the cluster
+  __syncwarp();
+  if (S > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+
+  if (warp >= 2) {
+    const int t = threadIdx.x - 64;
+    const int r0 = static_cast<int>(BN * rank / S), r1 = static_cast<int>(BN * (rank + 1) / S);
+    const int nrows = r1 - r0;
+    const int stride = p.mpad + 1;
+    const uint32_t part_base = sbase;  // partial[] starts at the aligned smem base
+    for (int idx = t; idx < nrows * p.M; idx += 32 * EPI_WARPS) {
+      const int nl = r0 + idx % nrows;
+      const int m = idx / nrows;
+      const int n = n0 + nl;
+      const uint32_t off = part_base + 4u * static_cast<uint32_t>(nl * stride + m);
+      float sum = 0.f;
+      for (uint32_t src = 0; src < S; ++src) {
+        if (S > 1)
+          sum += ld_shared_cluster_f32(map_shared_rank(off, src));
+        else
+          sum += reinterpret_cast<const float*>(smem)[nl * stride + m];
+      }
+      if (n < p.N) {
+        const int64_t o = static_cast<int64_t>(m) * p.N + n;
+        float v = sum;
+        if constexpr (EPI != EPI_NONE) v += ld_any(p.bias, n, p.bias_type);  // once, on the full sum
+        if constexpr (EPI == EPI_RELU) v = fmaxf(v, 0.0f);
+        if constexpr (EPI == EPI_GATE) v = fmaf(v, ld_any(p.Y, o, p.ab_type), v);
+        st_any(p.out, o, p.out_type, v);
+      }
+    }
+  }
+
+  // No CTA may leave (or release TMEM) while a peer still reads its shared memory.
+  __syncwarp();
+  if (S > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+  }
+}
+
+template <int EPI>
+cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkParams& p, int tiles_n,
+                       cudaStream_t s) {
+  auto k = skinny_kernel<EPI>;
+  const uint32_t smem = smem_bytes(p.mpad);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles_n * p.split));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, tb, ta, p);
+}
+
+}  // namespace sk
+
+int skinny_block_n() { return sk::BN; }
+int skinny_max_m() { return sk::MAX_MPAD; }
+
+cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA, const SkParams& p,
+                          int tiles_n, cudaStream_t s) {
+  switch (epi) {
+    case EPI_RELU: return sk::launch_one<EPI_RELU>(tmB, tmA, p, tiles_n, s);
+    case EPI_GATE: return sk::launch_one<EPI_GATE>(tmB, tmA, p, tiles_n, s);
+    default: return sk::launch_one<EPI_NONE>(tmB, tmA, p, tiles_n, s);
+  }
+}
+
+}  // namespace fgemm

@@ -118,7 +118,7 @@ def test_tc_integer_bit_exact(M, N, K, ab):
     # and the tensor-core result must equal the oracle bit for bit.  Shapes are ragged against the
     # 128 x 256 x 64 tile in M, N and K.
     p = gen.integer_problem(M, N, K, ab, ab, seed=M * 7 + N + K)
-    out, path = run_fused(p, M, N, K, ab, ab, ab)
+    out, path = run_fused(p, M, N, K, ab, ab, ab, opts={"path": fg.PATH_TC})
     assert path == fg.PATH_TC
     ref = oracle_run(p, M, N, K, ab, ab, ab)
     got = down(out, ab)
@@ -143,6 +143,51 @@ def test_tc_bias_and_output_types(bt, ot):
     out, path = run_fused(p, M, N, K, F16, bt, ot)
     assert path == fg.PATH_TC
     assert np.array_equal(down(out, ot), oracle_run(p, M, N, K, F16, bt, ot).out)
+
+
+# ------------------------------------------------------------ skinny-M path --
+
+SKINNY_SHAPES = [(1, 8, 8, 1), (1, 136, 72, 2), (5, 264, 520, 3), (16, 1032, 2048, 4),
+                 (33, 392, 256, 2), (64, 136, 8, 4), (100, 520, 1024, 8), (128, 1032, 512, 2)]
+
+
+@pytest.mark.parametrize("M,N,K,split", SKINNY_SHAPES)
+@pytest.mark.parametrize("gate", [False, True])
+def test_skinny_integer_bit_exact(M, N, K, split, gate):
+    # split K over a cluster; (64, 136, 8, 4) leaves some CTAs of the cluster with no K block
+    for ab, bt, ot in ((BF16, BF16, BF16), (F16, F32, F32)):
+        p = gen.integer_problem(M, N, K, ab, bt, seed=M + N + K + split, gate=gate)
+        out, path = run_fused(p, M, N, K, ab, bt, ot, gate=gate, opts={"split_k": split})
+        assert path == fg.PATH_SKINNY
+        ref = oracle_run(p, M, N, K, ab, bt, ot, gate=gate)
+        got = down(out, ot)
+        if not np.array_equal(got, ref.out):
+            bad = np.argwhere(got != ref.out)
+            pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
+
+
+def test_skinny_auto_split_and_coverage():
+    M, N, K = 16, 2056, 4096
+    p = gen.random_problem(M, N, K, BF16, BF16, seed=12)
+    guard = 4096
+    buf = torch.full((guard + M * N + guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + M * N].view(M, N)
+    _, path = run_fused(p, M, N, K, BF16, BF16, BF16, out=out)
+    assert path == fg.PATH_SKINNY
+    b = buf.cpu()
+    assert torch.isnan(b[:guard]).all() and torch.isnan(b[guard + M * N:]).all()
+    ref = oracle_run(p, M, N, K, BF16, BF16, BF16)
+    check_close(down(out, BF16), ref, K, BF16, bias64=oracle.decode(p.bias, BF16), what="skinny")
+
+
+def test_skinny_matches_square_tile_path():
+    M, N, K = 128, 1024, 1024
+    p = gen.random_problem(M, N, K, F16, F16, seed=13)
+    a, _ = run_fused(p, M, N, K, F16, F16, F16, opts={"path": fg.PATH_SKINNY})
+    b, _ = run_fused(p, M, N, K, F16, F16, F16, opts={"path": fg.PATH_TC})
+    ref = oracle_run(p, M, N, K, F16, F16, F16)
+    for x in (a, b):
+        check_close(down(x, F16), ref, K, F16, bias64=oracle.decode(p.bias, F16), what="skinny/tc")
 
 
 # ----------------------------------------------------------- float tolerance --
