@@ -411,14 +411,19 @@ def run_sweep(args):
         unf = w.name in ("square_4096", "glu_gate_1024x21568x4096")
         prob = Problem(w, dev, l2, with_unfused=unf)
         steps = max(5, min(200, int(2e-1 / max(w.flops / 1.2e15, 1e-6))))
-        groups = [1, 4, 8] if w.name.startswith("ffn") else [None]
-        for g in groups:
-            opts = {"group_m": g} if g else None
+        if w.name.startswith("ffn"):
+            variants = [{"group_m": g} for g in (1, 4, 8)]
+        elif w.name.startswith("skinny"):
+            variants = [None] + [{"split_k": s} for s in (1, 2, 3, 4, 8)]
+        else:
+            variants = [None]
+        for opts in variants:
+            g = (opts or {}).get("group_m")
             ms, path = time_steps(prob, steps, 5, stream, opts=opts)
             t = w.flops / (ms * 1e-3) / 1e12
             gbs = w.unavoidable_bytes() / (ms * 1e-3) / 1e9
             t_roof = max(w.flops / (pk["bf16_tflops"] * 1e12), w.unavoidable_bytes() / (pk["hbm_gbs"] * 1e9))
-            r = {"workload": name, "group_m": g or 8, "path": fg.PATH_NAMES.get(path), "us": ms * 1e3,
+            r = {"workload": name, "opts": opts or "auto", "path": fg.PATH_NAMES.get(path), "us": ms * 1e3,
                  "tflops": t, "gbs": gbs, "roofline_frac": t_roof / (ms * 1e-3),
                  "pct_bf16_peak": 100 * t / pk["bf16_tflops"], "pct_hbm": 100 * gbs / pk["hbm_gbs"]}
             results.append(r)

@@ -7,9 +7,10 @@
 //     by TMA); B is read N-major exactly as it lies in memory, A K-major;
 //   * splits K over the S CTAs of a thread-block cluster (one N tile per cluster), each CTA
 //     streaming its K range of B through a 6-stage TMA ring into tcgen05.mma (fp32 in TMEM);
-//   * reduces the S partial accumulators through distributed shared memory: each CTA copies its
-//     partial from TMEM to its own shared memory, the cluster synchronises, and CTA r sums rows
-//     [r*128/S, (r+1)*128/S) of the tile over all S CTAs;
+//   * reduces the S partial accumulators through distributed shared memory: rows
+//     [r*128/S, (r+1)*128/S) of the tile belong to CTA r; every CTA pushes its partial rows from
+//     TMEM straight into the owner's shared memory (remote vector stores), and after a cluster
+//     barrier each owner sums its rows locally;
 //   * applies the epilogue once, on the complete sum ("Epilogue concept", "Why it cannot move
 //     earlier": ReLU of a partial sum is not ReLU of the sum, and a bias added per partial would be
 //     added S times): x = sum + bias[n], then ReLU or the gate, one rounding, coalesced store.
@@ -163,63 +164,90 @@ __global__ void __launch_bounds__(THREADS, 1)
       volatile int never = 0;
       mbar_wait(bar(BAR_MMA_DONE), 0, &never, tmo, p.err, SITE_DRAIN);
     }
-  } else {
-    // ------------------------------------------------------------ partial: TMEM -> shared
-    // partial[n][m], row stride mpad + 1 floats, overlays the (now idle) stage buffers
-    const int q = warp & 3;
-    const int row = 32 * q + lane;
-    float* partial = reinterpret_cast<float*>(smem);
-    const int stride = p.mpad + 1;
-    bool have = nkb > 0;
-    if (have) {
-      have = mbar_wait(bar(BAR_ACC_FULL), 0, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL);
-      tc_fence_after();
-    }
-    if (have) {
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
-      for (int c = 0; c < p.mpad / 16; ++c) {
-        uint32_t v[16];
-        __syncwarp();
-        tmem_ld16(taddr + 16u * c, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) partial[row * stride + 16 * c + j] = __uint_as_float(v[j]);
-      }
-    } else {
-      for (int m = 0; m < p.mpad; ++m) partial[row * stride + m] = 0.f;
-    }
-    tc_fence_before();
   }
 
   // ------------------------------------------------------------ reduction across the cluster
+  // Row n of the tile is owned by CTA owner(n), the r with 128r/S <= n < 128(r+1)/S.  Each CTA
+  // pushes its partial row n into the owner's receive area recv[src][n - first_row(owner)][m]
+  // (row stride mpad + 4 floats), which overlays the owner's stage buffers; so the first cluster
+  // barrier makes sure every CTA has finished its main loop before any push, and the second one
+  // that every push has landed before the owners read.
   __syncwarp();
   if (S > 1)
     cluster_sync();
   else
     __syncthreads();
 
+  const int maxslice = (BN + static_cast<int>(S) - 1) / static_cast<int>(S);
+  const int stride = p.mpad + 4;
+  auto first_row = [&](uint32_t r) { return static_cast<int>(BN * r / S); };
+  if (warp >= 2) {
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    uint32_t owner = (static_cast<uint32_t>(row) * S) / BN;
+    while (owner + 1 < S && first_row(owner + 1) <= row) ++owner;
+    while (owner > 0 && first_row(owner) > row) --owner;
+    const uint32_t slot = sbase + 4u * static_cast<uint32_t>(
+                                          (static_cast<int>(rank) * maxslice + row - first_row(owner)) * stride);
+    const uint32_t dst = (S > 1) ? map_shared_rank(slot, owner) : slot;
+    const bool have = (nkb > 0) && mbar_wait(bar(BAR_ACC_FULL), 0, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL);
+    tc_fence_after();
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
+    for (int c = 0; c < p.mpad / 16; ++c) {
+      uint32_t v[16];
+      if (have) {
+        __syncwarp();
+        tmem_ld16(taddr + 16u * c, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) {
+        const uint32_t a = dst + 4u * static_cast<uint32_t>(16 * c + j);
+        if (S > 1)
+          st_shared_cluster_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+        else
+          st_shared_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                       __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncwarp();
+  if (S > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+
+  // ------------------------------------------------------------ epilogue on the full sums
   if (warp >= 2) {
     const int t = threadIdx.x - 64;
-    const int r0 = static_cast<int>(BN * rank / S), r1 = static_cast<int>(BN * (rank + 1) / S);
-    const int nrows = r1 - r0;
-    const int stride = p.mpad + 1;
-    const uint32_t part_base = sbase;  // partial[] starts at the aligned smem base
-    for (int idx = t; idx < nrows * p.M; idx += 32 * EPI_WARPS) {
-      const int nl = r0 + idx % nrows;
-      const int m = idx / nrows;
-      const int n = n0 + nl;
-      const uint32_t off = part_base + 4u * static_cast<uint32_t>(nl * stride + m);
-      float sum = 0.f;
+    const int r0 = first_row(rank), nrows = first_row(rank + 1) - r0;
+    const int m4 = (p.M + 3) / 4;
+    const float* recv = reinterpret_cast<const float*>(smem);
+    for (int idx = t; idx < nrows * m4; idx += 32 * EPI_WARPS) {
+      const int nl = idx % nrows;
+      const int m = 4 * (idx / nrows);
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
       for (uint32_t src = 0; src < S; ++src) {
-        if (S > 1)
-          sum += ld_shared_cluster_f32(map_shared_rank(off, src));
-        else
-          sum += reinterpret_cast<const float*>(smem)[nl * stride + m];
+        const float4 v = *reinterpret_cast<const float4*>(
+            recv + (static_cast<int>(src) * maxslice + nl) * stride + m);
+        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
       }
-      if (n < p.N) {
-        const int64_t o = static_cast<int64_t>(m) * p.N + n;
-        float v = sum;
-        if constexpr (EPI != EPI_NONE) v += ld_any(p.bias, n, p.bias_type);  // once, on the full sum
+      const int n = n0 + r0 + nl;
+      if (n >= p.N) continue;
+      float b = 0.f;
+      if constexpr (EPI != EPI_NONE) b = ld_any(p.bias, n, p.bias_type);  // once, on the full sum
+      const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (m + e >= p.M) break;
+        const int64_t o = static_cast<int64_t>(m + e) * p.N + n;
+        float v = s4[e] + b;
         if constexpr (EPI == EPI_RELU) v = fmaxf(v, 0.0f);
         if constexpr (EPI == EPI_GATE) v = fmaf(v, ld_any(p.Y, o, p.ab_type), v);
         st_any(p.out, o, p.out_type, v);
@@ -227,12 +255,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
-  // No CTA may leave (or release TMEM) while a peer still reads its shared memory.
-  __syncwarp();
-  if (S > 1)
-    cluster_sync();
-  else
-    __syncthreads();
+  __syncthreads();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
