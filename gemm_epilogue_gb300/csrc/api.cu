@@ -154,7 +154,7 @@ int validate(const Call& c, bool* nothing) {
   if (c.opts) {
     const fgemm_opts& o = *c.opts;
     if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
-        o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0)
+        o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -167,7 +167,10 @@ bool tc_eligible(const Call& c) {
 }
 
 int run_tc(const Call& c, DeviceInfo* d) {
+  const int mode = c.opts ? c.opts->cta_pair : 0;
+  const bool pair = (mode == 2) || (mode == 0 && c.M > 128 && d->num_sms >= 2);
   const int BM = tc_block_m(), BN = tc_block_n();
+  const int TILE_M = pair ? 2 * BM : BM;
   CUtensorMap tmA, tmB, tmO;
   const uint32_t out_box_cols = (c.t.out == ELEM_F32) ? 32 : 64;
   if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, 64) ||
@@ -178,7 +181,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.M = static_cast<int>(c.M);
   p.N = static_cast<int>(c.N);
   p.K = static_cast<int>(c.K);
-  p.tiles_m = static_cast<int>((c.M + BM - 1) / BM);
+  p.tiles_m = static_cast<int>((c.M + TILE_M - 1) / TILE_M);
   p.tiles_n = static_cast<int>((c.N + BN - 1) / BN);
   const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffLL) return FGEMM_ERR_INVALID_VALUE;
@@ -189,17 +192,21 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.out_type = c.t.out;
   p.bias = c.bias;
   p.Y = c.Y;
-  p.idesc = idesc_f16_f32acc(p.ab_bf16 != 0, BM, BN, /*a_mn=*/false, /*b_mn=*/true);
+  p.idesc = idesc_f16_f32acc(p.ab_bf16 != 0, TILE_M, BN, /*a_mn=*/false, /*b_mn=*/true);
   const bool swap = c.opts && c.opts->b_desc_swap;
   p.b_lbo = swap ? 1024u : 64u * 64u * 2u;  // distance between 64-column boxes of B
   p.b_sbo = swap ? 64u * 64u * 2u : 1024u;  // distance between 8-row groups along K
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  int grid = d->num_sms;
-  if (c.opts && c.opts->max_ctas > 0 && c.opts->max_ctas < grid) grid = c.opts->max_ctas;
-  if (grid > p.num_tiles) grid = p.num_tiles;
-  return status_of(launch_tc(c.epi, tmA, tmB, tmO, p, grid, c.stream));
+  // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than the tiles
+  const int per_unit = pair ? 2 : 1;
+  int units = d->num_sms / per_unit;
+  if (c.opts && c.opts->max_ctas > 0 && c.opts->max_ctas / per_unit < units)
+    units = c.opts->max_ctas / per_unit;
+  if (units < 1) units = 1;
+  if (units > p.num_tiles) units = p.num_tiles;
+  return status_of(launch_tc(c.epi, tmA, tmB, tmO, p, units * per_unit, pair, c.stream));
 }
 
 int run_skinny(const Call& c, DeviceInfo* d) {

@@ -40,9 +40,10 @@ struct SimtParams {
   int out_type;   // Elem
 };
 
+// pair = true: 2-CTA clusters (grid even), 256 x 256 tiles, tiles_m counted in 256-row tiles.
 cudaError_t launch_tc(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                      const CUtensorMap& tmOut, const TcParams& p, int grid, cudaStream_t s);
-size_t tc_smem_bytes();
+                      const CUtensorMap& tmOut, const TcParams& p, int grid, bool pair,
+                      cudaStream_t s);
 int tc_block_m();
 int tc_block_n();
 

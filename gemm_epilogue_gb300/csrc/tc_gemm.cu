@@ -1,6 +1,10 @@
 // tc_gemm.cu -- persistent, warp-specialised TMA + tcgen05 GEMM with a fused epilogue (sm_103a).
 //
-// One CTA per SM walks output tiles of BM x BN = 128 x 256 in grouped-M order (tile_order.h).
+// One CTA per SM walks output tiles of BM x BN = 128 x 256 in grouped-M order (tile_order.h), or,
+// in the CTA-pair form (PAIR), one 2-CTA cluster per SM pair walks 256 x 256 tiles: each CTA
+// stages its own 128 rows of A and half (128 columns) of B, the even CTA issues
+// tcgen05.mma.cta_group::2 (M = 256) for both, and each CTA's TMEM receives its 128 rows.  The pair
+// halves the B bytes each SM fetches per MMA and lets each SM keep 6 stages in flight.
 //   warp 0      TMA producer: A tile 128 x 64 (K-major) and B tile 64 x 256 (N-major, four
 //               64-column boxes) per stage into a STAGES-deep shared-memory ring, completion
 //               counted in bytes on full[s]; out-of-range rows / columns / K are zero-filled by
@@ -27,32 +31,39 @@
 namespace fgemm {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;  // per-CTA rows, tile columns, K per stage
 constexpr int EPI_WARPS = 4;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;    // 8 KB: 64 K-rows x 64 N-columns
-constexpr uint32_t B_STAGE_BYTES = BK * BN * 2;  // 32 KB
-constexpr uint32_t STAGE_TX = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr uint32_t EPI_BUF_BYTES = 32 * 128;     // 32 rows x 128 bytes
-constexpr uint32_t SMEM_A = 0;
-constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
-constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
-constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
-constexpr uint32_t SMEM_USED = SMEM_BAR + 256;
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
 constexpr uint32_t TMEM_COLS = 512;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+template <bool PAIR>
+struct Cfg {
+  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int B_BOXES = PAIR ? 2 : 4;                 // 64-column B boxes per CTA
+  static constexpr uint32_t B_STAGE_BYTES = B_BOXES * B_BOX_BYTES;
+  static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr uint32_t STAGE_TX = (PAIR ? 2 : 1) * STAGE_BYTES;  // bytes per full barrier
+  static constexpr int TILE_M = PAIR ? 2 * BM : BM;
+  static constexpr uint32_t SMEM_A = 0;
+  static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
+  static constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
+  static constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
+  static constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + barriers + 1024-B alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
 
 // barrier slots (uint64 each) inside the SMEM_BAR area
+constexpr int MAX_STAGES = 6;
 constexpr int BAR_FULL = 0;
-constexpr int BAR_EMPTY = STAGES;
-constexpr int BAR_ACC_FULL = 2 * STAGES;
-constexpr int BAR_ACC_EMPTY = 2 * STAGES + 2;
-constexpr int BAR_MMA_DONE = 2 * STAGES + 4;
-constexpr uint32_t OFF_TMEM_SLOT = 128;
-constexpr uint32_t OFF_ABORT = 136;
+constexpr int BAR_EMPTY = MAX_STAGES;
+constexpr int BAR_ACC_FULL = 2 * MAX_STAGES;
+constexpr int BAR_ACC_EMPTY = 2 * MAX_STAGES + 2;
+constexpr int BAR_MMA_DONE = 2 * MAX_STAGES + 4;
+constexpr uint32_t OFF_TMEM_SLOT = 192;  // after the 17 barriers
+constexpr uint32_t OFF_ABORT = 200;
 
 // wait sites recorded with a timeout
 enum { SITE_PROD_EMPTY = 1, SITE_MMA_ACC_EMPTY, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN };
@@ -98,7 +109,7 @@ __device__ __forceinline__ void load_bias_granule(const TcParams& p, int col, fl
   }
 }
 
-template <int EPI, int OUT_BYTES>
+template <int EPI, int OUT_BYTES, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, const TcParams p) {
@@ -106,6 +117,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int NCH = BN / CH;         // chunks per tile
   constexpr int G = 16 / OUT_BYTES;    // columns per 16-byte granule
   constexpr int NG = CH / G;           // granules per chunk (8)
+  using C = Cfg<PAIR>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int CG = PAIR ? 2 : 1;
+  constexpr uint32_t SMEM_A = C::SMEM_A, SMEM_B = C::SMEM_B, SMEM_EPI = C::SMEM_EPI,
+                     SMEM_BAR = C::SMEM_BAR;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -118,6 +134,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;     // 0 = the MMA-issuing CTA
+  const bool leader = rank == 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x / 2) : static_cast<int>(blockIdx.x);
+  const int units = PAIR ? static_cast<int>(gridDim.x / 2) : static_cast<int>(gridDim.x);
+  // barriers of the even CTA as seen from anywhere in the cluster
+  auto lead_bar = [&](int i) { return PAIR ? map_shared_rank(bar(i), 0) : bar(i); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -126,7 +148,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(BAR_ACC_FULL + b), 1);
-      mbar_init(bar(BAR_ACC_EMPTY + b), EPI_WARPS);
+      mbar_init(bar(BAR_ACC_EMPTY + b), (PAIR ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(bar(BAR_MMA_DONE), 1);
     *abort_flag = 0;
@@ -138,11 +160,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish_cg<CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer signals the even CTA's barriers: both must be initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -156,10 +179,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = unit; ok && t < p.num_tiles; t += units) {
         int tm, tn;
         tile_of(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
-        const int m0 = tm * BM, n0 = tn * BN;
+        const int m0 = tm * C::TILE_M + static_cast<int>(rank) * BM;
+        const int nb0 = tn * BN + static_cast<int>(rank) * (BN / 2) * (PAIR ? 1 : 0);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err,
                          SITE_PROD_EMPTY)) {
@@ -167,13 +191,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const uint32_t fb = bar(BAR_FULL + stage);
-          mbar_arrive_expect_tx(fb, STAGE_TX);
+          // the even CTA's full barrier counts both CTAs' bytes of the stage
+          if (leader) mbar_arrive_expect_tx(fb, C::STAGE_TX);
           const uint32_t a_dst = sbase + SMEM_A + stage * A_STAGE_BYTES;
-          const uint32_t b_dst = sbase + SMEM_B + stage * B_STAGE_BYTES;
-          tma_load_2d(a_dst, &tmA, fb, kb * BK, m0, pol);
+          const uint32_t b_dst = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
+          if constexpr (PAIR) {
+            const uint32_t lfb = lead_bar(BAR_FULL + stage);
+            tma_load_2d_pair(a_dst, &tmA, lfb, kb * BK, m0, pol);
 #pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            tma_load_2d(b_dst + c * B_BOX_BYTES, &tmB, fb, n0 + 64 * c, kb * BK, pol);
+            for (int c = 0; c < C::B_BOXES; ++c)
+              tma_load_2d_pair(b_dst + c * B_BOX_BYTES, &tmB, lfb, nb0 + 64 * c, kb * BK, pol);
+          } else {
+            tma_load_2d(a_dst, &tmA, fb, kb * BK, m0, pol);
+#pragma unroll
+            for (int c = 0; c < C::B_BOXES; ++c)
+              tma_load_2d(b_dst + c * B_BOX_BYTES, &tmB, fb, nb0 + 64 * c, kb * BK, pol);
+          }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -182,17 +215,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // Every load issued must land before the CTA may exit (also after an abort).
-      for (int s = 0; s < STAGES; ++s)
-        if ((issued >> s) & 1u) drain_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, tmo, p.err);
+      // Every load issued must land before the CTA may exit (also after an abort).  In a pair the
+      // even CTA's full barriers count the peer's bytes too; the closing cluster barrier keeps the
+      // peer resident until then.
+      if (leader)
+        for (int s = 0; s < STAGES; ++s)
+          if ((issued >> s) & 1u) drain_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, tmo, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
+      constexpr uint16_t kPair = 0x3;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int it = 0;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
+      for (int t = unit; ok && t < p.num_tiles; t += units, ++it) {
         const int b = it & 1;
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
         if (!mbar_wait(bar(BAR_ACC_EMPTY + b), acc_phase ^ 1u, abort_flag, tmo, p.err,
@@ -207,24 +244,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a_addr = sbase + SMEM_A + stage * A_STAGE_BYTES;
-          const uint32_t b_addr = sbase + SMEM_B + stage * B_STAGE_BYTES;
+          const uint32_t b_addr = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
             const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, p.b_lbo, p.b_sbo);
-            umma_f16(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_f16_cg<CG>(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit(bar(BAR_EMPTY + stage));  // stage free once these MMAs have read it
+          umma_commit_cg<CG>(bar(BAR_EMPTY + stage), kPair);  // stage free (both CTAs) once read
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(bar(BAR_ACC_FULL + b));  // accumulator complete: hand it to the epilogue
+        umma_commit_cg<CG>(bar(BAR_ACC_FULL + b), kPair);  // accumulator complete (both CTAs)
       }
       // All MMAs issued by this thread must finish before TMEM is released.
-      umma_commit(bar(BAR_MMA_DONE));
+      umma_commit_cg<CG>(bar(BAR_MMA_DONE), 0x1);
       drain_wait(bar(BAR_MMA_DONE), 0, tmo, p.err);
     }
   } else {
@@ -237,10 +274,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint64_t pol_out = policy_evict_first();
     uint32_t nstore = 0;
     int it = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
+    for (int t = unit; t < p.num_tiles; t += units, ++it) {
       int tm, tn;
       tile_of(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
-      const int m0 = tm * BM, n0 = tn * BN;
+      const int m0 = tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = tn * BN;
       const int b = it & 1;
       const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
       const int row0 = m0 + 32 * q;
@@ -345,7 +382,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       // This warp has finished reading accumulator b: release it to the MMA warp.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + b));
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(lead_bar(BAR_ACC_EMPTY + b));  // the even CTA's MMA waits on it
+        else
+          mbar_arrive(bar(BAR_ACC_EMPTY + b));
+      }
     }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
@@ -354,39 +396,72 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the even CTA's MMAs and both epilogues are done with TMEM
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_cg<CG>(tmem_base, TMEM_COLS);
   }
 }
 
-template <int EPI, int OUT_BYTES>
+template <int EPI, int OUT_BYTES, bool PAIR>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                        const TcParams& p, int grid, cudaStream_t s) {
-  auto k = tc_gemm_kernel<EPI, OUT_BYTES>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR>;
+  constexpr uint32_t smem = Cfg<PAIR>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, THREADS, SMEM_BYTES, s>>>(a, b, o, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (PAIR) {
+    // A persistent grid must be co-resident: clusters of two need two free SMs in one GPC, so the
+    // number of pairs that fit at once can be below SMs / 2.
+    static int max_pairs = 0;  // per process; the library targets one GPU type
+    if (max_pairs == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = grid / 2;
+      }
+      max_pairs = n;
+    }
+    if (grid / 2 > max_pairs) cfg.gridDim = dim3(static_cast<unsigned>(2 * max_pairs));
+  }
+  return cudaLaunchKernelEx(&cfg, k, a, b, o, p);
+}
+
+template <int EPI, int OUT_BYTES>
+cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
+                               const TcParams& p, int grid, bool pair, cudaStream_t s) {
+  return pair ? launch_one<EPI, OUT_BYTES, true>(a, b, o, p, grid, s)
+              : launch_one<EPI, OUT_BYTES, false>(a, b, o, p, grid, s);
 }
 
 }  // namespace tc
 
-size_t tc_smem_bytes() { return tc::SMEM_BYTES; }
 int tc_block_m() { return tc::BM; }
 int tc_block_n() { return tc::BN; }
 
 cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                      const TcParams& p, int grid, cudaStream_t s) {
+                      const TcParams& p, int grid, bool pair, cudaStream_t s) {
   const bool f32 = p.out_type == ELEM_F32;
   switch (epi) {
-    case EPI_RELU: return f32 ? tc::launch_one<EPI_RELU, 4>(a, b, o, p, grid, s)
-                              : tc::launch_one<EPI_RELU, 2>(a, b, o, p, grid, s);
-    case EPI_GATE: return f32 ? tc::launch_one<EPI_GATE, 4>(a, b, o, p, grid, s)
-                              : tc::launch_one<EPI_GATE, 2>(a, b, o, p, grid, s);
-    default: return f32 ? tc::launch_one<EPI_NONE, 4>(a, b, o, p, grid, s)
-                        : tc::launch_one<EPI_NONE, 2>(a, b, o, p, grid, s);
+    case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, p, grid, pair, s)
+                              : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, p, grid, pair, s);
+    case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4>(a, b, o, p, grid, pair, s)
+                              : tc::launch_pair_or_not<EPI_GATE, 2>(a, b, o, p, grid, pair, s);
+    default: return f32 ? tc::launch_pair_or_not<EPI_NONE, 4>(a, b, o, p, grid, pair, s)
+                        : tc::launch_pair_or_not<EPI_NONE, 2>(a, b, o, p, grid, pair, s);
   }
 }
 

@@ -51,7 +51,7 @@ typedef enum {
   FGEMM_ERR_INVALID_VALUE = 1,     /* negative size, NULL pointer where data is needed, bad option */
   FGEMM_ERR_UNSUPPORTED_DTYPE = 2, /* unknown dtype word */
   FGEMM_ERR_MISALIGNED = 3,        /* a pointer not aligned to its element size */
-  FGEMM_ERR_NO_DEVICE = 4,         /* no current CUDA device, or not compute capability 10.x */
+  FGEMM_ERR_NO_DEVICE = 4,         /* no current CUDA device, or not compute capability 10.3 */
   FGEMM_ERR_LAUNCH = 5,            /* a CUDA call or kernel launch failed */
   FGEMM_ERR_TIMEOUT = 6,           /* a device-side wait exceeded its bound (see fgemm_opts) */
   FGEMM_ERR_WORKSPACE = 7          /* workspace NULL or smaller than required */
@@ -68,7 +68,7 @@ typedef enum {
 /* Kernel paths (fgemm_opts.path, and *path_taken of the _ex entries). */
 #define FGEMM_PATH_AUTO 0    /* library choice */
 #define FGEMM_PATH_TC 1      /* persistent TMA + tcgen05 kernel, grouped-M tile order */
-#define FGEMM_PATH_SKINNY 2  /* swap-AB split-K kernel for small M (bias+ReLU only) */
+#define FGEMM_PATH_SKINNY 2  /* M <= 128: swap-AB kernel, K split over a cluster, DSMEM reduction */
 #define FGEMM_PATH_GENERIC 3 /* CUDA-core tiled kernel: any shape and alignment */
 #define FGEMM_PATH_KZERO 4   /* K == 0: epilogue over the zero accumulator, no MMA */
 #define FGEMM_PATH_NONE 5    /* M == 0 or N == 0: nothing launched */
@@ -81,7 +81,9 @@ typedef struct {
   int max_ctas;   /* persistent grid cap (default: one CTA per SM) */
   int timeout_ms; /* bound on every device-side barrier wait (default 1000 ms) */
   int b_desc_swap; /* diagnostic: exchange the two byte offsets of B's shared-memory descriptor */
-  int reserved[2];
+  int cta_pair;   /* tensor-core path: 0 = automatic, 1 = one CTA per 128 x 256 tile,
+                     2 = CTA pairs (2-SM clusters, tcgen05 cta_group::2) on 256 x 256 tiles */
+  int reserved;
 } fgemm_opts;
 
 /*

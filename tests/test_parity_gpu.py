@@ -113,12 +113,13 @@ TC_SHAPES = [(1, 8, 8), (128, 256, 64), (200, 136, 72), (129, 264, 136), (300, 5
 
 @pytest.mark.parametrize("M,N,K", TC_SHAPES)
 @pytest.mark.parametrize("ab", [F16, BF16])
-def test_tc_integer_bit_exact(M, N, K, ab):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_tc_integer_bit_exact(M, N, K, ab, pair):
     # Small integers: every partial sum is exact in fp32, so the only rounding is the final one
     # and the tensor-core result must equal the oracle bit for bit.  Shapes are ragged against the
-    # 128 x 256 x 64 tile in M, N and K.
+    # 128 x 256 x 64 tile (single CTA) and the 256 x 256 tile (CTA pair) in M, N and K.
     p = gen.integer_problem(M, N, K, ab, ab, seed=M * 7 + N + K)
-    out, path = run_fused(p, M, N, K, ab, ab, ab, opts={"path": fg.PATH_TC})
+    out, path = run_fused(p, M, N, K, ab, ab, ab, opts={"path": fg.PATH_TC, "cta_pair": pair})
     assert path == fg.PATH_TC
     ref = oracle_run(p, M, N, K, ab, ab, ab)
     got = down(out, ab)
@@ -127,11 +128,12 @@ def test_tc_integer_bit_exact(M, N, K, ab):
         pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
 
 
-@pytest.mark.parametrize("M,N,K", [(200, 136, 72), (300, 520, 200)])
-def test_tc_gate_integer_bit_exact(M, N, K):
+@pytest.mark.parametrize("M,N,K", [(200, 136, 72), (300, 520, 200), (777, 1288, 328)])
+@pytest.mark.parametrize("pair", [1, 2])
+def test_tc_gate_integer_bit_exact(M, N, K, pair):
     for ab, ot in ((F16, F16), (BF16, F32)):
         p = gen.integer_problem(M, N, K, ab, ab, seed=K, gate=True)
-        out, path = run_fused(p, M, N, K, ab, ab, ot, gate=True)
+        out, path = run_fused(p, M, N, K, ab, ab, ot, gate=True, opts={"cta_pair": pair})
         assert path == fg.PATH_TC
         assert np.array_equal(down(out, ot), oracle_run(p, M, N, K, ab, ab, ot, gate=True).out)
 
@@ -232,13 +234,24 @@ def test_tile_coverage_sentinel_and_guards(M, N, K):
     assert not torch.isnan(b[guard:guard + M * N]).any()
 
 
-def test_grouping_and_grid_do_not_change_results():
+@pytest.mark.parametrize("pair", [1, 2])
+def test_grouping_and_grid_do_not_change_results(pair):
     M, N, K = 700, 1800, 128
     p = gen.random_problem(M, N, K, BF16, BF16, seed=4)
-    base, _ = run_fused(p, M, N, K, BF16, BF16, BF16)
-    for opts in ({"group_m": 1}, {"group_m": 4}, {"group_m": 3, "max_ctas": 7}, {"max_ctas": 1}):
-        out, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts=opts)
+    base, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts={"cta_pair": pair})
+    for opts in ({"group_m": 1}, {"group_m": 4}, {"group_m": 3, "max_ctas": 7}, {"max_ctas": 2}):
+        out, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts=dict(opts, cta_pair=pair))
         assert torch.equal(out, base), opts
+
+
+def test_pair_and_single_cta_agree():
+    M, N, K = 1000, 2056, 512
+    p = gen.random_problem(M, N, K, F16, F16, seed=14)
+    a, _ = run_fused(p, M, N, K, F16, F16, F16, opts={"cta_pair": 1})
+    b, _ = run_fused(p, M, N, K, F16, F16, F16, opts={"cta_pair": 2})
+    ref = oracle_run(p, M, N, K, F16, F16, F16)
+    for x in (a, b):
+        check_close(down(x, F16), ref, K, F16, bias64=oracle.decode(p.bias, F16), what="pair/single")
 
 
 # -------------------------------------------------------------- unfused chain --
