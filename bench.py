@@ -292,12 +292,13 @@ def run_ours(args):
     w = gen.WORKLOADS[args.workload]
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_DEFAULT
-    prob = Problem(w, dev, l2)
+    prob = Problem(w, dev, l2, with_unfused=args.variant == "unfused")
     stream = torch.cuda.Stream(device=dev)
     barrier = (lambda: dist.barrier()) if dist else None
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    ms, path = time_steps(prob, args.steps, args.warmup, stream, barrier=barrier)
+    unfused = args.variant == "unfused"
+    ms, path = time_steps(prob, args.steps, args.warmup, stream, barrier=barrier, unfused=unfused)
     clocks = sampler.stop() if sampler else None
     if dist:
         t = torch.tensor([ms], device=dev)
@@ -334,7 +335,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": gen.TYPE_NAMES[w.ab_type],
         "data": "synthetic (seeded normal inputs, shapes of the workload)",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "epilogue": w.epilogue,
+        "config": {"workload": w.name, "variant": args.variant, "M": w.M, "N": w.N, "K": w.K,
+                   "epilogue": w.epilogue,
                    "out": gen.TYPE_NAMES[w.out_type], "bias": gen.TYPE_NAMES[w.bias_type],
                    "path": fg.PATH_NAMES.get(path, str(path)), "parallelism": f"replicas{world}",
                    "l2": f"inputs rotate over {len(prob.sets)} sets of {prob.set_bytes / 1e6:.1f} MB "
@@ -343,7 +345,7 @@ def run_ours(args):
         "roofline": roof,
         "e2e": {"value": w.flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * ((3 if w.epilogue != "gate" else 2) if unfused else 1),
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -450,6 +452,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="square_4096")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
+                    help="unfused: time the GEMM -> elementwise chain instead (traffic comparison)")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-workloads", default="")
     args = ap.parse_args()
