@@ -154,7 +154,8 @@ int validate(const Call& c, bool* nothing) {
   if (c.opts) {
     const fgemm_opts& o = *c.opts;
     if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
-        o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2)
+        o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
+        o.tail_split < 0 || o.tail_split > 1)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -199,13 +200,30 @@ int run_tc(const Call& c, DeviceInfo* d) {
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  // persistent grid: one CTA (or CTA pair) per SM (pair of SMs), never more than the tiles
+  // persistent grid: one CTA (or CTA pair) per SM (pair of SMs) that can be resident at once,
+  // never more than the tiles
   const int per_unit = pair ? 2 : 1;
   int units = d->num_sms / per_unit;
+  if (pair) {
+    const int resident = tc_max_active_pairs(c.epi, c.t.out);
+    if (resident > 0 && resident < units) units = resident;
+  }
   if (c.opts && c.opts->max_ctas > 0 && c.opts->max_ctas / per_unit < units)
     units = c.opts->max_ctas / per_unit;
   if (units < 1) units = 1;
   if (units > p.num_tiles) units = p.num_tiles;
+  // Tail: the tiles of the last, partial round are cut along N into pieces so that the round's
+  // pieces still fit on the grid (pairs need >= 64 columns per CTA: at most 2 pieces).
+  const int rem = p.num_tiles % units;
+  int split = 1;
+  const bool allow = !(c.opts && c.opts->tail_split == 1);
+  if (allow && rem > 0 && p.num_tiles > units) {
+    const int max_split = pair ? 2 : 4;
+    while (split * 2 <= max_split && rem * split * 2 <= units) split *= 2;
+  }
+  p.tail_split = split;
+  p.full_tiles = p.num_tiles - (split > 1 ? rem : 0);
+  p.num_items = p.full_tiles + (p.num_tiles - p.full_tiles) * split;
   return status_of(launch_tc(c.epi, tmA, tmB, tmO, p, units * per_unit, pair, c.stream));
 }
 

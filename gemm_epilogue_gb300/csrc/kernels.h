@@ -16,6 +16,10 @@ inline int elem_bytes(int e) { return e == ELEM_F32 ? 4 : 2; }
 struct TcParams {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles, group;
+  // Work items: items 0 .. full_tiles-1 are whole tiles; the remaining num_tiles - full_tiles tiles
+  // (the last, partial round of the persistent grid) are each cut into `tail_split` pieces along N
+  // (256 / tail_split columns each) so that the last round takes a fraction of a tile's time.
+  int full_tiles, tail_split, num_items;
   int ab_bf16;     // operand (and Y) type: 0 = f16, 1 = bf16
   int bias_type;   // Elem of the bias
   int out_type;    // Elem of out
@@ -44,6 +48,9 @@ struct SimtParams {
 cudaError_t launch_tc(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                       const CUtensorMap& tmOut, const TcParams& p, int grid, bool pair,
                       cudaStream_t s);
+// How many CTA pairs of the pair-mode kernel can be resident at once (clusters need two free SMs
+// in one GPC); cached per process.
+int tc_max_active_pairs(int epi, int out_type);
 int tc_block_m();
 int tc_block_n();
 

@@ -75,6 +75,27 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
   return mbar_wait(bar, parity, &never, timeout_ns, err, SITE_DRAIN);
 }
 
+// One unit of work of the persistent loop: a whole 256-column tile, or a piece of a tail tile.
+struct Work {
+  int tm, tn;   // tile coordinates
+  int col0;     // first output column of the piece
+  int width;    // columns in the piece (256, 128 or 64)
+};
+__device__ __forceinline__ Work work_of(const TcParams& p, int item) {
+  Work w;
+  int tile = item, piece = 0, split = 1;
+  if (item >= p.full_tiles) {
+    const int j = item - p.full_tiles;
+    split = p.tail_split;
+    tile = p.full_tiles + j / split;
+    piece = j % split;
+  }
+  tile_of(tile, p.tiles_m, p.tiles_n, p.group, w.tm, w.tn);
+  w.width = BN / split;
+  w.col0 = w.tn * BN + piece * w.width;
+  return w;
+}
+
 template <int OUT_BYTES>
 __device__ __forceinline__ void load_bias_granule(const TcParams& p, int col, float (&b)[16 / OUT_BYTES]) {
   constexpr int G = 16 / OUT_BYTES;
@@ -114,7 +135,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, const TcParams p) {
   constexpr int CH = 128 / OUT_BYTES;  // output columns per 128-byte staging row
-  constexpr int NCH = BN / CH;         // chunks per tile
   constexpr int G = 16 / OUT_BYTES;    // columns per 16-byte granule
   constexpr int NG = CH / G;           // granules per chunk (8)
   using C = Cfg<PAIR>;
@@ -179,11 +199,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       bool ok = true;
-      for (int t = unit; ok && t < p.num_tiles; t += units) {
-        int tm, tn;
-        tile_of(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
-        const int m0 = tm * C::TILE_M + static_cast<int>(rank) * BM;
-        const int nb0 = tn * BN + static_cast<int>(rank) * (BN / 2) * (PAIR ? 1 : 0);
+      for (int t = unit; ok && t < p.num_items; t += units) {
+        const Work wk = work_of(p, t);
+        const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM;
+        // each CTA of a pair stages half of the piece's columns
+        const int cols = PAIR ? wk.width / 2 : wk.width;
+        const int nb0 = wk.col0 + static_cast<int>(rank) * cols;
+        const int boxes = cols / 64;
+        const uint32_t tx = (PAIR ? 2u : 1u) * (A_STAGE_BYTES + static_cast<uint32_t>(boxes) * B_BOX_BYTES);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err,
                          SITE_PROD_EMPTY)) {
@@ -192,19 +215,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t fb = bar(BAR_FULL + stage);
           // the even CTA's full barrier counts both CTAs' bytes of the stage
-          if (leader) mbar_arrive_expect_tx(fb, C::STAGE_TX);
+          if (leader) mbar_arrive_expect_tx(fb, tx);
           const uint32_t a_dst = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_dst = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
           if constexpr (PAIR) {
             const uint32_t lfb = lead_bar(BAR_FULL + stage);
             tma_load_2d_pair(a_dst, &tmA, lfb, kb * BK, m0, pol);
-#pragma unroll
-            for (int c = 0; c < C::B_BOXES; ++c)
+            for (int c = 0; c < boxes; ++c)
               tma_load_2d_pair(b_dst + c * B_BOX_BYTES, &tmB, lfb, nb0 + 64 * c, kb * BK, pol);
           } else {
             tma_load_2d(a_dst, &tmA, fb, kb * BK, m0, pol);
-#pragma unroll
-            for (int c = 0; c < C::B_BOXES; ++c)
+            for (int c = 0; c < boxes; ++c)
               tma_load_2d(b_dst + c * B_BOX_BYTES, &tmB, fb, nb0 + 64 * c, kb * BK, pol);
           }
           issued |= 1u << stage;
@@ -229,7 +250,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int it = 0;
-      for (int t = unit; ok && t < p.num_tiles; t += units, ++it) {
+      for (int t = unit; ok && t < p.num_items; t += units, ++it) {
+        // MMA N = the piece's width (all tiles but the tail pieces: 256)
+        const int width = work_of(p, t).width;
+        const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(width >> 3) << 17);
         const int b = it & 1;
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
         if (!mbar_wait(bar(BAR_ACC_EMPTY + b), acc_phase ^ 1u, abort_flag, tmo, p.err,
@@ -249,7 +273,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
             const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, p.b_lbo, p.b_sbo);
-            umma_f16_cg<CG>(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_f16_cg<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit_cg<CG>(bar(BAR_EMPTY + stage), kPair);  // stage free (both CTAs) once read
           if (++stage == STAGES) {
@@ -274,10 +298,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint64_t pol_out = policy_evict_first();
     uint32_t nstore = 0;
     int it = 0;
-    for (int t = unit; t < p.num_tiles; t += units, ++it) {
-      int tm, tn;
-      tile_of(t, p.tiles_m, p.tiles_n, p.group, tm, tn);
-      const int m0 = tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = tn * BN;
+    for (int t = unit; t < p.num_items; t += units, ++it) {
+      const Work wk = work_of(p, t);
+      const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = wk.col0;
+      const int nch = wk.width / CH;
       const int b = it & 1;
       const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
       const int row0 = m0 + 32 * q;
@@ -291,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
 
 #pragma unroll 1
-      for (int c = 0; c < NCH; ++c) {
+      for (int c = 0; c < nch; ++c) {
         const int col0 = n0 + c * CH;
         if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
 
@@ -423,21 +447,36 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (PAIR) {
-    // A persistent grid must be co-resident: clusters of two need two free SMs in one GPC, so the
-    // number of pairs that fit at once can be below SMs / 2.
-    static int max_pairs = 0;  // per process; the library targets one GPU type
-    if (max_pairs == 0) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        n = grid / 2;
-      }
-      max_pairs = n;
-    }
-    if (grid / 2 > max_pairs) cfg.gridDim = dim3(static_cast<unsigned>(2 * max_pairs));
-  }
   return cudaLaunchKernelEx(&cfg, k, a, b, o, p);
+}
+
+// A persistent grid must be co-resident: clusters of two need two free SMs in one GPC, so the
+// number of pairs that fit at once can be below SMs / 2.
+template <int EPI, int OUT_BYTES>
+int max_pairs() {
+  static int cached = 0;  // per process; the library targets one GPU type
+  if (cached == 0) {
+    auto k = tc_gemm_kernel<EPI, OUT_BYTES, true>;
+    constexpr uint32_t smem = Cfg<true>::SMEM_BYTES;
+    int n = 0;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+      cudaLaunchConfig_t cfg{};
+      cfg.gridDim = dim3(2);
+      cfg.blockDim = dim3(THREADS);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cached = n > 0 ? n : -1;
+  }
+  return cached;
 }
 
 template <int EPI, int OUT_BYTES>
@@ -448,6 +487,15 @@ cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const
 }
 
 }  // namespace tc
+
+int tc_max_active_pairs(int epi, int out_type) {
+  const bool f32 = out_type == ELEM_F32;
+  switch (epi) {
+    case EPI_RELU: return f32 ? tc::max_pairs<EPI_RELU, 4>() : tc::max_pairs<EPI_RELU, 2>();
+    case EPI_GATE: return f32 ? tc::max_pairs<EPI_GATE, 4>() : tc::max_pairs<EPI_GATE, 2>();
+    default: return f32 ? tc::max_pairs<EPI_NONE, 4>() : tc::max_pairs<EPI_NONE, 2>();
+  }
+}
 
 int tc_block_m() { return tc::BM; }
 int tc_block_n() { return tc::BN; }

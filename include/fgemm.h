@@ -83,7 +83,8 @@ typedef struct {
   int b_desc_swap; /* diagnostic: exchange the two byte offsets of B's shared-memory descriptor */
   int cta_pair;   /* tensor-core path: 0 = automatic, 1 = one CTA per 128 x 256 tile,
                      2 = CTA pairs (2-SM clusters, tcgen05 cta_group::2) on 256 x 256 tiles */
-  int reserved;
+  int tail_split; /* tensor-core path: 0 = cut the tiles of the last partial round of the
+                     persistent grid into 128- or 64-column pieces, 1 = keep whole tiles */
 } fgemm_opts;
 
 /*

@@ -244,6 +244,23 @@ def test_grouping_and_grid_do_not_change_results(pair):
         assert torch.equal(out, base), opts
 
 
+@pytest.mark.parametrize("pair,max_ctas", [(1, 20), (1, 35), (1, 44), (2, 12), (2, 20), (2, 40)])
+def test_tail_round_pieces_integer_bit_exact(pair, max_ctas):
+    # The last partial round of the persistent grid is cut into 128- or 64-column pieces; a grid
+    # cap chosen per case makes 2 or 4 pieces per tail tile, on ragged M, N and K.
+    M, N, K = 700, 1800, 200
+    for gate in (False, True):
+        p = gen.integer_problem(M, N, K, BF16, BF16, seed=max_ctas, gate=gate)
+        out, path = run_fused(p, M, N, K, BF16, BF16, BF16, gate=gate,
+                              opts={"cta_pair": pair, "max_ctas": max_ctas})
+        assert path == fg.PATH_TC
+        ref = oracle_run(p, M, N, K, BF16, BF16, BF16, gate=gate)
+        assert np.array_equal(down(out, BF16), ref.out)
+        whole, _ = run_fused(p, M, N, K, BF16, BF16, BF16, gate=gate,
+                             opts={"cta_pair": pair, "max_ctas": max_ctas, "tail_split": 1})
+        assert torch.equal(whole, out)
+
+
 def test_pair_and_single_cta_agree():
     M, N, K = 1000, 2056, 512
     p = gen.random_problem(M, N, K, F16, F16, seed=14)
