@@ -168,6 +168,12 @@ class Problem:
             self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
             self.ws_bytes = nb
 
+    def plan(self, opts=None):
+        a, b, bias, y, out = self.sets[0]
+        w = self.w
+        return self.fg.fgemm_plan(a, b, bias, y, out, w.M, w.N, w.K, self.word,
+                                  gate=y is not None, opts=opts)
+
     def call(self, i, stream, opts=None, unfused=False):
         a, b, bias, y, out = self.sets[i % len(self.sets)]
         w, fg = self.w, self.fg
@@ -338,7 +344,8 @@ def run_ours(args):
         "config": {"workload": w.name, "variant": args.variant, "M": w.M, "N": w.N, "K": w.K,
                    "epilogue": w.epilogue,
                    "out": gen.TYPE_NAMES[w.out_type], "bias": gen.TYPE_NAMES[w.bias_type],
-                   "path": fg.PATH_NAMES.get(path, str(path)), "parallelism": f"replicas{world}",
+                   "path": fg.PATH_NAMES.get(path, str(path)), "plan": prob.plan(),
+                   "parallelism": f"replicas{world}",
                    "l2": f"inputs rotate over {len(prob.sets)} sets of {prob.set_bytes / 1e6:.1f} MB "
                          f"(> 2 x L2 {l2 / 1e6:.0f} MB)"},
         "pct_of_peak": 100.0 * tflops / pk["bf16_tflops"],
@@ -418,14 +425,15 @@ def run_sweep(args):
         elif w.name.startswith("skinny"):
             variants = [None] + [{"split_k": s} for s in (1, 2, 3, 4, 8)]
         else:
-            variants = [None]
+            variants = [None, {"tail_split": 1}, {"cta_pair": 1}, {"cta_pair": 1, "tail_split": 1}]
         for opts in variants:
             g = (opts or {}).get("group_m")
             ms, path = time_steps(prob, steps, 5, stream, opts=opts)
             t = w.flops / (ms * 1e-3) / 1e12
             gbs = w.unavoidable_bytes() / (ms * 1e-3) / 1e9
             t_roof = max(w.flops / (pk["bf16_tflops"] * 1e12), w.unavoidable_bytes() / (pk["hbm_gbs"] * 1e9))
-            r = {"workload": name, "opts": opts or "auto", "path": fg.PATH_NAMES.get(path), "us": ms * 1e3,
+            r = {"workload": name, "opts": opts or "auto", "plan": prob.plan(opts),
+                 "path": fg.PATH_NAMES.get(path), "us": ms * 1e3,
                  "tflops": t, "gbs": gbs, "roofline_frac": t_roof / (ms * 1e-3),
                  "pct_bf16_peak": 100 * t / pk["bf16_tflops"], "pct_hbm": 100 * gbs / pk["hbm_gbs"]}
             results.append(r)

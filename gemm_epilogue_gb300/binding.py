@@ -43,6 +43,13 @@ class Opts(ctypes.Structure):
                 ("b_desc_swap", ctypes.c_int), ("cta_pair", ctypes.c_int), ("tail_split", ctypes.c_int)]
 
 
+class PlanInfo(ctypes.Structure):
+    """fgemm_plan_info."""
+    _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("tiles", ctypes.c_int), ("work_items", ctypes.c_int), ("tail_split", ctypes.c_int),
+                ("resident_pairs", ctypes.c_int), ("reserved", ctypes.c_int)]
+
+
 _lock = threading.Lock()
 _lib = None
 _vp, _i64, _int, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
@@ -62,6 +69,8 @@ _SIGS = {
                                                _vp]),
     "fgemm_device_status": (_int, [_vp, ctypes.POINTER(_int)]),
     "fgemm_status_string": (ctypes.c_char_p, [_int]),
+    "fgemm_plan": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int,
+                          ctypes.POINTER(Opts), ctypes.POINTER(PlanInfo)]),
     "fgemm_tile_of": (_int, [_i64, _i64, _i64, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
 }
 
@@ -187,6 +196,16 @@ def fgemm_device_status(stream=None) -> int:
     code = ctypes.c_int(0)
     _check(lib().fgemm_device_status(_stream(stream), ctypes.byref(code)), "fgemm_device_status")
     return code.value
+
+
+def fgemm_plan(A, B, bias, Y, out, M, N, K, dtype, gate=False, opts=None) -> dict:
+    """Launch plan of a fused call (nothing is launched)."""
+    info = PlanInfo()
+    o = _opts(opts)
+    _check(lib().fgemm_plan(_ptr(A), _ptr(B), _ptr(bias), _ptr(Y), _ptr(out), M, N, K, dtype,
+                            int(bool(gate)), ctypes.byref(o) if o else None, ctypes.byref(info)),
+           "fgemm_plan")
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if name != "reserved"}
 
 
 def fgemm_tile_of(t, tiles_m, tiles_n, group) -> tuple[int, int]:

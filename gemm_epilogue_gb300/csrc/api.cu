@@ -167,11 +167,80 @@ bool tc_eligible(const Call& c) {
          (c.bias == nullptr || aligned(c.bias, 16)) && (c.Y == nullptr || aligned(c.Y, 16));
 }
 
-int run_tc(const Call& c, DeviceInfo* d) {
+// ---------------------------------------------------------------- launch plans
+struct TcPlan {
+  bool pair;
+  int tiles_m, tiles_n, num_tiles;
+  int units;       // persistent CTAs (or CTA pairs)
+  int resident;    // pairs that can be resident at once (pair mode), else 0
+  int tail_split, full_tiles, num_items;
+};
+
+TcPlan plan_tc(const Call& c, DeviceInfo* d) {
+  TcPlan t{};
   const int mode = c.opts ? c.opts->cta_pair : 0;
-  const bool pair = (mode == 2) || (mode == 0 && c.M > 128 && d->num_sms >= 2);
+  t.pair = (mode == 2) || (mode == 0 && c.M > 128 && d->num_sms >= 2);
+  const int TILE_M = t.pair ? 2 * tc_block_m() : tc_block_m(), BN = tc_block_n();
+  t.tiles_m = static_cast<int>((c.M + TILE_M - 1) / TILE_M);
+  t.tiles_n = static_cast<int>((c.N + BN - 1) / BN);
+  const int64_t tiles = static_cast<int64_t>(t.tiles_m) * t.tiles_n;
+  t.num_tiles = tiles > 0x7fffffffLL ? -1 : static_cast<int>(tiles);
+  if (t.num_tiles < 0) return t;
+  // persistent grid: one CTA (or CTA pair) per SM (pair of SMs) that can be resident at once,
+  // never more than the tiles
+  const int per_unit = t.pair ? 2 : 1;
+  int units = d->num_sms / per_unit;
+  if (t.pair) {
+    t.resident = tc_max_active_pairs(c.epi, c.t.out);
+    if (t.resident > 0 && t.resident < units) units = t.resident;
+  }
+  if (c.opts && c.opts->max_ctas > 0 && c.opts->max_ctas / per_unit < units)
+    units = c.opts->max_ctas / per_unit;
+  if (units < 1) units = 1;
+  if (units > t.num_tiles) units = t.num_tiles;
+  t.units = units;
+  // Tail: the tiles of the last, partial round are cut along N into pieces so that the round's
+  // pieces still fit on the grid (pairs need >= 64 columns per CTA: at most 2 pieces).
+  const int rem = t.num_tiles % units;
+  int split = 1;
+  const bool allow = !(c.opts && c.opts->tail_split == 1);
+  if (allow && rem > 0 && t.num_tiles > units) {
+    const int max_split = t.pair ? 2 : 4;
+    while (split * 2 <= max_split && rem * split * 2 <= units) split *= 2;
+  }
+  t.tail_split = split;
+  t.full_tiles = t.num_tiles - (split > 1 ? rem : 0);
+  t.num_items = t.full_tiles + (t.num_tiles - t.full_tiles) * split;
+  return t;
+}
+
+struct SkPlan {
+  int mpad, tmem_cols, tiles_n, split;
+};
+
+SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
+  SkPlan s{};
+  s.mpad = static_cast<int>((c.M + 15) / 16 * 16);
+  s.tmem_cols = 32;
+  while (s.tmem_cols < s.mpad) s.tmem_cols *= 2;
+  s.tiles_n = static_cast<int>((c.N + skinny_block_n() - 1) / skinny_block_n());
+  const int kb = static_cast<int>((c.K + 63) / 64);
+  int split = (c.opts && c.opts->split_k > 0) ? c.opts->split_k : 0;
+  if (split == 0) {  // enough clusters to cover the SMs, each split at least 4 K blocks
+    split = d->num_sms / (s.tiles_n > 0 ? s.tiles_n : 1);
+    if (split > kb / 4) split = kb / 4;
+    if (split > 8) split = 8;
+    if (split < 1) split = 1;
+  }
+  s.split = split;
+  return s;
+}
+
+int run_tc(const Call& c, DeviceInfo* d) {
+  const TcPlan t = plan_tc(c, d);
+  if (t.num_tiles < 0) return FGEMM_ERR_INVALID_VALUE;
   const int BM = tc_block_m(), BN = tc_block_n();
-  const int TILE_M = pair ? 2 * BM : BM;
+  const int TILE_M = t.pair ? 2 * BM : BM;
   CUtensorMap tmA, tmB, tmO;
   const uint32_t out_box_cols = (c.t.out == ELEM_F32) ? 32 : 64;
   if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, 64) ||
@@ -182,11 +251,12 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.M = static_cast<int>(c.M);
   p.N = static_cast<int>(c.N);
   p.K = static_cast<int>(c.K);
-  p.tiles_m = static_cast<int>((c.M + TILE_M - 1) / TILE_M);
-  p.tiles_n = static_cast<int>((c.N + BN - 1) / BN);
-  const int64_t tiles = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-  if (tiles > 0x7fffffffLL) return FGEMM_ERR_INVALID_VALUE;
-  p.num_tiles = static_cast<int>(tiles);
+  p.tiles_m = t.tiles_m;
+  p.tiles_n = t.tiles_n;
+  p.num_tiles = t.num_tiles;
+  p.full_tiles = t.full_tiles;
+  p.tail_split = t.tail_split;
+  p.num_items = t.num_items;
   p.group = (c.opts && c.opts->group_m > 0) ? c.opts->group_m : 8;
   p.ab_bf16 = c.t.ab == ELEM_BF16;
   p.bias_type = c.t.bias;
@@ -200,68 +270,34 @@ int run_tc(const Call& c, DeviceInfo* d) {
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  // persistent grid: one CTA (or CTA pair) per SM (pair of SMs) that can be resident at once,
-  // never more than the tiles
-  const int per_unit = pair ? 2 : 1;
-  int units = d->num_sms / per_unit;
-  if (pair) {
-    const int resident = tc_max_active_pairs(c.epi, c.t.out);
-    if (resident > 0 && resident < units) units = resident;
-  }
-  if (c.opts && c.opts->max_ctas > 0 && c.opts->max_ctas / per_unit < units)
-    units = c.opts->max_ctas / per_unit;
-  if (units < 1) units = 1;
-  if (units > p.num_tiles) units = p.num_tiles;
-  // Tail: the tiles of the last, partial round are cut along N into pieces so that the round's
-  // pieces still fit on the grid (pairs need >= 64 columns per CTA: at most 2 pieces).
-  const int rem = p.num_tiles % units;
-  int split = 1;
-  const bool allow = !(c.opts && c.opts->tail_split == 1);
-  if (allow && rem > 0 && p.num_tiles > units) {
-    const int max_split = pair ? 2 : 4;
-    while (split * 2 <= max_split && rem * split * 2 <= units) split *= 2;
-  }
-  p.tail_split = split;
-  p.full_tiles = p.num_tiles - (split > 1 ? rem : 0);
-  p.num_items = p.full_tiles + (p.num_tiles - p.full_tiles) * split;
-  return status_of(launch_tc(c.epi, tmA, tmB, tmO, p, units * per_unit, pair, c.stream));
+  return status_of(launch_tc(c.epi, tmA, tmB, tmO, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
 }
 
 int run_skinny(const Call& c, DeviceInfo* d) {
-  const int BN = skinny_block_n();
-  const int mpad = static_cast<int>((c.M + 15) / 16 * 16);
+  const SkPlan s = plan_skinny(c, d);
   CUtensorMap tmB, tmA;
   if (!encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
-      !encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, static_cast<uint32_t>(mpad), 64))
+      !encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, static_cast<uint32_t>(s.mpad), 64))
     return FGEMM_ERR_LAUNCH;
   SkParams p{};
   p.M = static_cast<int>(c.M);
   p.N = static_cast<int>(c.N);
   p.K = static_cast<int>(c.K);
-  p.mpad = mpad;
-  p.tmem_cols = 32;
-  while (p.tmem_cols < mpad) p.tmem_cols *= 2;
-  const int tiles_n = static_cast<int>((c.N + BN - 1) / BN);
-  const int kb = static_cast<int>((c.K + 63) / 64);
-  int split = (c.opts && c.opts->split_k > 0) ? c.opts->split_k : 0;
-  if (split == 0) {  // enough clusters to cover the SMs, each split at least 4 K blocks
-    split = d->num_sms / (tiles_n > 0 ? tiles_n : 1);
-    if (split > kb / 4) split = kb / 4;
-    if (split > 8) split = 8;
-    if (split < 1) split = 1;
-  }
-  p.split = split;
+  p.mpad = s.mpad;
+  p.tmem_cols = s.tmem_cols;
+  p.split = s.split;
   p.ab_type = c.t.ab;
   p.bias_type = c.t.bias;
   p.out_type = c.t.out;
   p.bias = c.bias;
   p.Y = c.Y;
   p.out = c.out;
-  p.idesc = idesc_f16_f32acc(c.t.ab == ELEM_BF16, BN, mpad, /*a_mn=*/true, /*b_mn=*/false);
+  p.idesc = idesc_f16_f32acc(c.t.ab == ELEM_BF16, skinny_block_n(), s.mpad, /*a_mn=*/true,
+                             /*b_mn=*/false);
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  return status_of(launch_skinny(c.epi, tmB, tmA, p, tiles_n, c.stream));
+  return status_of(launch_skinny(c.epi, tmB, tmA, p, s.tiles_n, c.stream));
 }
 
 SimtParams simt_params(const Call& c) {
@@ -280,8 +316,8 @@ SimtParams simt_params(const Call& c) {
   return p;
 }
 
-// Choose and run a path for a validated, non-empty call.
-int dispatch(const Call& c, DeviceInfo* d, int* path_taken) {
+// Choose the path for a validated, non-empty call.
+int choose_path(const Call& c, int* out_path) {
   const int forced = c.opts ? c.opts->path : FGEMM_PATH_AUTO;
   int path;
   if (forced == FGEMM_PATH_AUTO) {
@@ -298,6 +334,15 @@ int dispatch(const Call& c, DeviceInfo* d, int* path_taken) {
       return FGEMM_ERR_INVALID_VALUE;
     if (path == FGEMM_PATH_KZERO && (c.K != 0 || c.epi == EPI_NONE)) return FGEMM_ERR_INVALID_VALUE;
   }
+  *out_path = path;
+  return FGEMM_OK;
+}
+
+// Choose and run a path for a validated, non-empty call.
+int dispatch(const Call& c, DeviceInfo* d, int* path_taken) {
+  int path = 0;
+  const int st = choose_path(c, &path);
+  if (st != FGEMM_OK) return st;
   if (path_taken) *path_taken = path;
   switch (path) {
     case FGEMM_PATH_TC: return run_tc(c, d);
@@ -443,6 +488,46 @@ const char* fgemm_status_string(int s) {
     case FGEMM_ERR_WORKSPACE: return "FGEMM_ERR_WORKSPACE";
     default: return "FGEMM_ERR_UNKNOWN";
   }
+}
+
+int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
+               int64_t M, int64_t N, int64_t K, int dtype, int gate, const fgemm_opts* opts,
+               fgemm_plan_info* info) {
+  if (!info) return FGEMM_ERR_INVALID_VALUE;
+  *info = fgemm_plan_info{};
+  info->path = FGEMM_PATH_NONE;
+  Call c{A, B, bias, gate ? Y : nullptr, const_cast<void*>(out), M, N, K, {},
+         gate ? EPI_GATE : EPI_RELU, nullptr, opts};
+  int st = parse_dtype(dtype, &c.t);
+  if (st != FGEMM_OK) return st;
+  bool nothing = false;
+  st = validate(c, &nothing);
+  if (st != FGEMM_OK || nothing) return st;
+  DeviceInfo* d = current_device();
+  if (!d) return FGEMM_ERR_NO_DEVICE;
+  int path = 0;
+  st = choose_path(c, &path);
+  if (st != FGEMM_OK) return st;
+  info->path = path;
+  info->cluster = 1;
+  info->tail_split = 1;
+  if (path == FGEMM_PATH_TC) {
+    const TcPlan t = plan_tc(c, d);
+    if (t.num_tiles < 0) return FGEMM_ERR_INVALID_VALUE;
+    info->cluster = t.pair ? 2 : 1;
+    info->grid = t.units * info->cluster;
+    info->tiles = t.num_tiles;
+    info->work_items = t.num_items;
+    info->tail_split = t.tail_split;
+    info->resident_pairs = t.resident;
+  } else if (path == FGEMM_PATH_SKINNY) {
+    const SkPlan s = plan_skinny(c, d);
+    info->cluster = s.split;
+    info->grid = s.tiles_n * s.split;
+    info->tiles = s.tiles_n;
+    info->work_items = s.tiles_n * s.split;
+  }
+  return FGEMM_OK;
 }
 
 int fgemm_tile_of(int64_t t, int64_t tiles_m, int64_t tiles_n, int group, int64_t* m_tile,

@@ -162,6 +162,26 @@ int fgemm_device_status(void* stream, int* code);
 const char* fgemm_status_string(int status);
 
 /*
+ * Launch plan of a fused call, computed without launching anything: the path, grid and cluster
+ * shape, the tile count and how the persistent grid's last round is cut.  Same arguments and
+ * validation as fgemm_bias_relu_ex (gate = 0) or fgemm_addmm_gate_ex (gate = 1); the buffers are
+ * inspected for alignment only.
+ */
+typedef struct {
+  int path;           /* FGEMM_PATH_* that would run */
+  int grid;           /* CTAs launched */
+  int cluster;        /* CTAs per cluster: 2 for CTA pairs, the K split on the skinny path */
+  int tiles;          /* output tiles (tensor-core and skinny paths) */
+  int work_items;     /* persistent work items, after cutting the last round into pieces */
+  int tail_split;     /* pieces per tile of the last round (1 = whole tiles) */
+  int resident_pairs; /* CTA pairs resident at once (pair mode; 0 otherwise) */
+  int reserved;
+} fgemm_plan_info;
+int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
+               int64_t M, int64_t N, int64_t K, int dtype, int gate, const fgemm_opts* opts,
+               fgemm_plan_info* info);
+
+/*
  * The persistent kernels' tile order, exposed for host-side tests: linear tile t of a
  * tiles_m x tiles_n grid with `group` M-tiles per band ("I3. Fuse a GEMM epilogue and change tile
  * scheduling", "Tiles and grouped ownership").  Returns FGEMM_ERR_INVALID_VALUE when t is out of

@@ -320,5 +320,33 @@ def test_full_size_workloads_sampled_rows(name):
         check_close(fake.out, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what="bias-only control")
 
 
+def test_plan_matches_the_path_that_runs():
+    cases = [(4096, 4096, 512, False, None), (1024, 21568, 256, True, None), (16, 8192, 1024, False, None),
+             (700, 1800, 200, False, {"cta_pair": 1, "max_ctas": 44}), (3, 5, 7, False, None)]
+    for M, N, K, gate, opts in cases:
+        p = gen.random_problem(M, N, K, F16, F16, seed=1, gate=gate)
+        A, B, bias, Y = up(p.A, F16), up(p.B, F16), up(p.bias, F16), up(p.Y, F16) if gate else None
+        out = torch.empty(M, N, dtype=torch.float16, device="cuda")
+        plan = fg.fgemm_plan(A, B, bias, Y, out, M, N, K, fg.F16, gate=gate, opts=opts)
+        if gate:
+            path = fg.fgemm_addmm_gate_ex(A, B, bias, Y, out, M, N, K, fg.F16, opts=opts)
+        else:
+            path = fg.fgemm_bias_relu_ex(A, B, bias, out, M, N, K, fg.F16, opts=opts)
+        torch.cuda.synchronize()
+        assert plan["path"] == path
+        if path == fg.PATH_TC:
+            assert plan["grid"] % plan["cluster"] == 0 and plan["grid"] > 0
+            units = plan["grid"] // plan["cluster"]
+            rem = plan["tiles"] % units
+            assert plan["work_items"] == plan["tiles"] + rem * (plan["tail_split"] - 1) or \
+                plan["tail_split"] == 1
+    # the split of the 44-CTA single-CTA case: 48 tiles on 44 CTAs -> 4 tail tiles in 4 pieces
+    p = gen.random_problem(700, 1800, 200, F16, F16, seed=1)
+    plan = fg.fgemm_plan(up(p.A, F16), up(p.B, F16), up(p.bias, F16), None,
+                         torch.empty(700, 1800, dtype=torch.float16, device="cuda"), 700, 1800, 200,
+                         fg.F16, opts={"cta_pair": 1, "max_ctas": 44})
+    assert (plan["tiles"], plan["grid"], plan["tail_split"], plan["work_items"]) == (48, 44, 4, 60)
+
+
 def test_device_error_word_clear():
     assert fg.fgemm_device_status() == 0
