@@ -423,7 +423,7 @@ def run_sweep(args):
         if w.name.startswith("ffn"):
             variants = [{"group_m": g} for g in (1, 4, 8)]
         elif w.name.startswith("skinny"):
-            variants = [None] + [{"split_k": s} for s in (1, 2, 3, 4, 8)]
+            variants = [None] + [{"split_k": s, "skinny_tiles": t} for t in (1, 2) for s in (2, 3, 4)]
         else:
             variants = [None, {"tail_split": 1}, {"cta_pair": 1}, {"cta_pair": 1, "tail_split": 1}]
         for opts in variants:

@@ -155,7 +155,7 @@ int validate(const Call& c, bool* nothing) {
     const fgemm_opts& o = *c.opts;
     if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
         o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
-        o.tail_split < 0 || o.tail_split > 1)
+        o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -215,24 +215,32 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
 }
 
 struct SkPlan {
-  int mpad, tmem_cols, tiles_n, split;
+  int mpad, nt, tmem_cols, tiles_n, groups, split;
 };
 
 SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
   SkPlan s{};
   s.mpad = static_cast<int>((c.M + 15) / 16 * 16);
-  s.tmem_cols = 32;
-  while (s.tmem_cols < s.mpad) s.tmem_cols *= 2;
   s.tiles_n = static_cast<int>((c.N + skinny_block_n() - 1) / skinny_block_n());
   const int kb = static_cast<int>((c.K + 63) / 64);
-  int split = (c.opts && c.opts->split_k > 0) ? c.opts->split_k : 0;
-  if (split == 0) {  // enough clusters to cover the SMs, each split at least 4 K blocks
-    split = d->num_sms / (s.tiles_n > 0 ? s.tiles_n : 1);
-    if (split > kb / 4) split = kb / 4;
-    if (split > 8) split = 8;
-    if (split < 1) split = 1;
+  // Two 128-column tiles per CTA halve the re-reads of A, which matter once A is wide (M >= 64).
+  int nt = (c.opts && c.opts->skinny_tiles > 0) ? c.opts->skinny_tiles
+                                                : ((s.mpad >= 64 && s.tiles_n >= 2) ? 2 : 1);
+  for (;; --nt) {
+    s.nt = nt;
+    s.groups = (s.tiles_n + nt - 1) / nt;
+    int split = (c.opts && c.opts->split_k > 0) ? c.opts->split_k : 0;
+    if (split == 0) {  // enough clusters to cover the SMs, each split at least 4 K blocks
+      split = d->num_sms / (s.groups > 0 ? s.groups : 1);
+      if (split > kb / 4) split = kb / 4;
+      if (split > 8) split = 8;
+      if (split < 1) split = 1;
+    }
+    s.split = split;
+    if (nt == 1 || skinny_fits(s.mpad, nt, split)) break;
   }
-  s.split = split;
+  s.tmem_cols = 32;
+  while (s.tmem_cols < s.nt * s.mpad) s.tmem_cols *= 2;
   return s;
 }
 
@@ -284,6 +292,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   p.N = static_cast<int>(c.N);
   p.K = static_cast<int>(c.K);
   p.mpad = s.mpad;
+  p.nt = s.nt;
   p.tmem_cols = s.tmem_cols;
   p.split = s.split;
   p.ab_type = c.t.ab;
@@ -297,7 +306,8 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  return status_of(launch_skinny(c.epi, tmB, tmA, p, s.tiles_n, c.stream));
+  if (!skinny_fits(s.mpad, s.nt, s.split)) return FGEMM_ERR_INVALID_VALUE;
+  return status_of(launch_skinny(c.epi, tmB, tmA, p, s.groups * s.split, c.stream));
 }
 
 SimtParams simt_params(const Call& c) {
@@ -523,9 +533,10 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
   } else if (path == FGEMM_PATH_SKINNY) {
     const SkPlan s = plan_skinny(c, d);
     info->cluster = s.split;
-    info->grid = s.tiles_n * s.split;
+    info->grid = s.groups * s.split;
     info->tiles = s.tiles_n;
-    info->work_items = s.tiles_n * s.split;
+    info->work_items = s.groups * s.split;
+    info->tail_split = s.nt;  // reused: 128-column tiles per CTA on the skinny path
   }
   return FGEMM_OK;
 }

@@ -58,7 +58,8 @@ int tc_block_n();
 struct SkParams {
   int M, N, K;
   int mpad;       // M rounded up to a multiple of 16 (the MMA's N), <= 128
-  int tmem_cols;  // power of two >= 32 and >= mpad
+  int nt;         // 128-column tiles per CTA (1 or 2), sharing each staged block of A
+  int tmem_cols;  // power of two >= 32 and >= nt * mpad
   int split;      // CTAs per cluster splitting K (1..8)
   int ab_type, bias_type, out_type;  // Elem
   const void* bias;
@@ -69,9 +70,11 @@ struct SkParams {
   int* err;
 };
 cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA,
-                          const SkParams& p, int tiles_n, cudaStream_t s);
+                          const SkParams& p, int ctas, cudaStream_t s);
 int skinny_block_n();
 int skinny_max_m();
+// Whether the stage ring and the cluster-reduction buffer fit in shared memory.
+bool skinny_fits(int mpad, int nt, int split);
 
 cudaError_t launch_generic(int epi, const SimtParams& p, cudaStream_t s);
 

@@ -3,14 +3,16 @@
 // With M <= 128 the square-tile kernel has too few tiles to keep the GPU busy and the time is
 // the stream of B (K x N) from HBM.  This kernel therefore
 //   * swaps the operands: out^T (N x M) = B^T A^T, so the 128-row MMA dimension runs over N (128
-//     output columns per tile) and the MMA's N is M rounded up to 16 (rows >= M are zero-filled
+//     output columns per MMA) and the MMA's N is M rounded up to 16 (rows >= M are zero-filled
 //     by TMA); B is read N-major exactly as it lies in memory, A K-major;
-//   * splits K over the S CTAs of a thread-block cluster (one N tile per cluster), each CTA
-//     streaming its K range of B through a 6-stage TMA ring into tcgen05.mma (fp32 in TMEM);
+//   * gives each CTA `nt` adjacent 128-column tiles (one TMEM accumulator each) that share every
+//     staged A block, so A is re-read from L2 once per 128 * nt columns instead of once per 128;
+//   * splits K over the S CTAs of a thread-block cluster, each CTA streaming its K range of B
+//     through a TMA ring into tcgen05.mma (fp32 in TMEM);
 //   * reduces the S partial accumulators through distributed shared memory: rows
-//     [r*128/S, (r+1)*128/S) of the tile belong to CTA r; every CTA pushes its partial rows from
-//     TMEM straight into the owner's shared memory (remote vector stores), and after a cluster
-//     barrier each owner sums its rows locally;
+//     [r*W/S, (r+1)*W/S) of the CTA's W = 128 * nt columns belong to CTA r; every CTA pushes its
+//     partial rows from TMEM straight into the owner's shared memory (remote vector stores), and
+//     after a cluster barrier each owner sums its rows locally;
 //   * applies the epilogue once, on the complete sum ("Epilogue concept", "Why it cannot move
 //     earlier": ReLU of a partial sum is not ReLU of the sum, and a bias added per partial would be
 //     added S times): x = sum + bias[n], then ReLU or the gate, one rounding, coalesced store.
@@ -21,23 +23,34 @@
 namespace fgemm {
 namespace sk {
 
-constexpr int BN = 128;  // output columns per tile (MMA M)
+constexpr int BN = 128;  // output columns per MMA (MMA M)
 constexpr int BK = 64;
-constexpr int STAGES = 6;
+constexpr int MAX_STAGES = 8;
 constexpr int EPI_WARPS = 4;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr uint32_t B_BOX_BYTES = 64 * 64 * 2;        // 64 K-rows x 64 N-columns
-constexpr uint32_t B_STAGE_BYTES = 2 * B_BOX_BYTES;  // 64 x 128
+constexpr uint32_t B_BOX_BYTES = 64 * 64 * 2;         // 64 K-rows x 64 N-columns
+constexpr uint32_t B_TILE_BYTES = 2 * B_BOX_BYTES;    // 64 x 128: one MMA's worth of B
 constexpr int MAX_MPAD = 128;
 constexpr uint32_t BAR_BYTES = 256;
+constexpr uint32_t STAGE_AREA_MAX = 196608;           // bytes of stage ring at most
 
 enum { SITE_PROD_EMPTY = 16, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN };
 
-__host__ __device__ inline uint32_t stage_bytes(int mpad) {
-  return B_STAGE_BYTES + static_cast<uint32_t>(mpad) * 128u;
+__host__ __device__ inline uint32_t stage_bytes(int mpad, int nt) {
+  return static_cast<uint32_t>(nt) * B_TILE_BYTES + static_cast<uint32_t>(mpad) * 128u;
 }
-__host__ inline uint32_t smem_bytes(int mpad) {
-  return STAGES * stage_bytes(mpad) + BAR_BYTES + 1024;
+__host__ __device__ inline int num_stages(int mpad, int nt) {
+  int s = static_cast<int>(STAGE_AREA_MAX / stage_bytes(mpad, nt));
+  return s > MAX_STAGES ? MAX_STAGES : s;
+}
+__host__ inline uint32_t smem_bytes(int mpad, int nt) {
+  return static_cast<uint32_t>(num_stages(mpad, nt)) * stage_bytes(mpad, nt) + BAR_BYTES + 1024;
+}
+// Receive area of the cluster reduction, overlaid on the stage ring.
+__host__ __device__ inline uint32_t recv_bytes(int mpad, int nt, int split) {
+  const int rows = BN * nt;
+  const int maxslice = (rows + split - 1) / split;
+  return static_cast<uint32_t>(split * maxslice * (mpad + 4)) * 4u;
 }
 
 __device__ __forceinline__ float ld_any(const void* p, int64_t i, int type) {
@@ -63,21 +76,23 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sbytes = stage_bytes(p.mpad);
-  const uint32_t bar0 = sbase + STAGES * sbytes;
+  const int nt = p.nt;
+  const int stages = num_stages(p.mpad, nt);
+  const uint32_t sbytes = stage_bytes(p.mpad, nt);
+  const uint32_t bar0 = sbase + static_cast<uint32_t>(stages) * sbytes;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-  // barriers: full[0..5], empty[6..11], acc_full 12, mma_done 13
-  constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_ACC_FULL = 2 * STAGES,
-                BAR_MMA_DONE = 2 * STAGES + 1;
-  uint8_t* bar_area = smem + STAGES * sbytes;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 128);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 136);
+  // barriers: full[0..7], empty[8..15], acc_full 16, mma_done 17
+  constexpr int BAR_FULL = 0, BAR_EMPTY = MAX_STAGES, BAR_ACC_FULL = 2 * MAX_STAGES,
+                BAR_MMA_DONE = 2 * MAX_STAGES + 1;
+  uint8_t* bar_area = smem + static_cast<uint32_t>(stages) * sbytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 200);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t S = static_cast<uint32_t>(p.split);
   const uint32_t rank = (S > 1) ? cluster_ctarank() : 0u;
-  const int tile = static_cast<int>(blockIdx.x / S);
-  const int n0 = tile * BN;
+  const int W = BN * nt;  // output columns of this CTA
+  const int n0 = static_cast<int>(blockIdx.x / S) * W;
   const int KB = (p.K + BK - 1) / BK;
   const int kb0 = static_cast<int>(static_cast<int64_t>(KB) * rank / S);
   const int kb1 = static_cast<int>(static_cast<int64_t>(KB) * (rank + 1) / S);
@@ -85,7 +100,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint64_t tmo = p.timeout_ns;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(bar(BAR_FULL + s), 1);
       mbar_init(bar(BAR_EMPTY + s), 1);
     }
@@ -111,7 +126,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_b = policy_evict_first();   // B is streamed once
-      const uint64_t pol_a = policy_evict_last();    // A is re-read by every N tile
+      const uint64_t pol_a = policy_evict_last();    // A is re-read by every group of N tiles
       uint32_t stage = 0, phase = 0, issued = 0, issued_parity = 0;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err, SITE_PROD_EMPTY))
@@ -119,18 +134,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t fb = bar(BAR_FULL + stage);
         mbar_arrive_expect_tx(fb, sbytes);
         const uint32_t dst = sbase + stage * sbytes;
-        tma_load_2d(dst, &tmB, fb, n0, kb * BK, pol_b);
-        tma_load_2d(dst + B_BOX_BYTES, &tmB, fb, n0 + 64, kb * BK, pol_b);
-        tma_load_2d(dst + B_STAGE_BYTES, &tmA, fb, kb * BK, 0, pol_a);
+        for (int c = 0; c < 2 * nt; ++c)
+          tma_load_2d(dst + c * B_BOX_BYTES, &tmB, fb, n0 + 64 * c, kb * BK, pol_b);
+        tma_load_2d(dst + static_cast<uint32_t>(nt) * B_TILE_BYTES, &tmA, fb, kb * BK, 0, pol_a);
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
+        if (++stage == static_cast<uint32_t>(stages)) {
           stage = 0;
           phase ^= 1u;
         }
       }
       volatile int never = 0;
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < stages; ++s)
         if ((issued >> s) & 1u)
           mbar_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, &never, tmo, p.err, SITE_DRAIN);
     }
@@ -145,16 +160,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t b_addr = sbase + stage * sbytes;       // MMA operand A: B^T, N-major
-        const uint32_t a_addr = b_addr + B_STAGE_BYTES;       // MMA operand B: A^T, K-major
+        const uint32_t b_addr = sbase + stage * sbytes;                            // B^T, N-major
+        const uint32_t a_addr = b_addr + static_cast<uint32_t>(nt) * B_TILE_BYTES;  // A^T, K-major
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t da = sdesc_sw128(b_addr + 2048u * k, B_BOX_BYTES, 1024u);
           const uint64_t db = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
-          umma_f16(tmem_base, da, db, p.idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          for (int t = 0; t < nt; ++t) {
+            const uint64_t da =
+                sdesc_sw128(b_addr + t * B_TILE_BYTES + 2048u * k, B_BOX_BYTES, 1024u);
+            umma_f16(tmem_base + static_cast<uint32_t>(t * p.mpad), da, db, p.idesc,
+                     (kb > kb0 || k > 0) ? 1u : 0u);
+          }
         }
         umma_commit(bar(BAR_EMPTY + stage));
-        if (++stage == STAGES) {
+        if (++stage == static_cast<uint32_t>(stages)) {
           stage = 0;
           phase ^= 1u;
         }
@@ -167,51 +186,56 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ------------------------------------------------------------ reduction across the cluster
-  // Row n of the tile is owned by CTA owner(n), the r with 128r/S <= n < 128(r+1)/S.  Each CTA
-  // pushes its partial row n into the owner's receive area recv[src][n - first_row(owner)][m]
-  // (row stride mpad + 4 floats), which overlays the owner's stage buffers; so the first cluster
-  // barrier makes sure every CTA has finished its main loop before any push, and the second one
-  // that every push has landed before the owners read.
+  // Row n (0 <= n < W) of the CTA's columns is owned by CTA owner(n), the r with
+  // W r / S <= n < W (r + 1) / S.  Each CTA pushes its partial row n into the owner's receive area
+  // recv[src][n - first_row(owner)][m] (row stride mpad + 4 floats), which overlays the owner's
+  // stage ring; so the first cluster barrier makes sure every CTA has finished its main loop
+  // before any push, and the second one that every push has landed before the owners read.
   __syncwarp();
   if (S > 1)
     cluster_sync();
   else
     __syncthreads();
 
-  const int maxslice = (BN + static_cast<int>(S) - 1) / static_cast<int>(S);
+  const int maxslice = (W + static_cast<int>(S) - 1) / static_cast<int>(S);
   const int stride = p.mpad + 4;
-  auto first_row = [&](uint32_t r) { return static_cast<int>(BN * r / S); };
+  auto first_row = [&](uint32_t r) { return static_cast<int>(static_cast<uint32_t>(W) * r / S); };
   if (warp >= 2) {
     const int q = warp & 3;
-    const int row = 32 * q + lane;
-    uint32_t owner = (static_cast<uint32_t>(row) * S) / BN;
-    while (owner + 1 < S && first_row(owner + 1) <= row) ++owner;
-    while (owner > 0 && first_row(owner) > row) --owner;
-    const uint32_t slot = sbase + 4u * static_cast<uint32_t>(
-                                          (static_cast<int>(rank) * maxslice + row - first_row(owner)) * stride);
-    const uint32_t dst = (S > 1) ? map_shared_rank(slot, owner) : slot;
-    const bool have = (nkb > 0) && mbar_wait(bar(BAR_ACC_FULL), 0, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL);
+    const bool have = (nkb > 0) && mbar_wait(bar(BAR_ACC_FULL), 0, abort_flag, tmo, p.err,
+                                             SITE_EPI_ACC_FULL);
     tc_fence_after();
-    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16);
-    for (int c = 0; c < p.mpad / 16; ++c) {
-      uint32_t v[16];
-      if (have) {
-        __syncwarp();
-        tmem_ld16(taddr + 16u * c, v);
-        tmem_ld_wait();
-      } else {
+    for (int t = 0; t < nt; ++t) {
+      const int row = t * BN + 32 * q + lane;
+      uint32_t owner = (static_cast<uint32_t>(row) * S) / static_cast<uint32_t>(W);
+      while (owner + 1 < S && first_row(owner + 1) <= row) ++owner;
+      while (owner > 0 && first_row(owner) > row) --owner;
+      const uint32_t slot =
+          sbase + 4u * static_cast<uint32_t>(
+                           (static_cast<int>(rank) * maxslice + row - first_row(owner)) * stride);
+      const uint32_t dst = (S > 1) ? map_shared_rank(slot, owner) : slot;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                             static_cast<uint32_t>(t * p.mpad);
+      for (int c = 0; c < p.mpad / 16; ++c) {
+        uint32_t v[16];
+        if (have) {
+          __syncwarp();
+          tmem_ld16(taddr + 16u * c, v);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0u;
-      }
+          for (int j = 0; j < 16; ++j) v[j] = 0u;
+        }
 #pragma unroll
-      for (int j = 0; j < 16; j += 4) {
-        const uint32_t a = dst + 4u * static_cast<uint32_t>(16 * c + j);
-        if (S > 1)
-          st_shared_cluster_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-        else
-          st_shared_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                       __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+        for (int j = 0; j < 16; j += 4) {
+          const uint32_t a = dst + 4u * static_cast<uint32_t>(16 * c + j);
+          if (S > 1)
+            st_shared_cluster_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                 __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+          else
+            st_shared_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                         __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+        }
       }
     }
     tc_fence_before();
@@ -264,14 +288,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int EPI>
-cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkParams& p, int tiles_n,
+cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkParams& p, int ctas,
                        cudaStream_t s) {
   auto k = skinny_kernel<EPI>;
-  const uint32_t smem = smem_bytes(p.mpad);
+  const uint32_t smem = smem_bytes(p.mpad, p.nt);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(tiles_n * p.split));
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -289,13 +313,18 @@ cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkPar
 
 int skinny_block_n() { return sk::BN; }
 int skinny_max_m() { return sk::MAX_MPAD; }
+bool skinny_fits(int mpad, int nt, int split) {
+  return sk::num_stages(mpad, nt) >= 2 &&
+         sk::recv_bytes(mpad, nt, split) <=
+             static_cast<uint32_t>(sk::num_stages(mpad, nt)) * sk::stage_bytes(mpad, nt);
+}
 
 cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA, const SkParams& p,
-                          int tiles_n, cudaStream_t s) {
+                          int ctas, cudaStream_t s) {
   switch (epi) {
-    case EPI_RELU: return sk::launch_one<EPI_RELU>(tmB, tmA, p, tiles_n, s);
-    case EPI_GATE: return sk::launch_one<EPI_GATE>(tmB, tmA, p, tiles_n, s);
-    default: return sk::launch_one<EPI_NONE>(tmB, tmA, p, tiles_n, s);
+    case EPI_RELU: return sk::launch_one<EPI_RELU>(tmB, tmA, p, ctas, s);
+    case EPI_GATE: return sk::launch_one<EPI_GATE>(tmB, tmA, p, ctas, s);
+    default: return sk::launch_one<EPI_NONE>(tmB, tmA, p, ctas, s);
   }
 }
 

@@ -85,6 +85,9 @@ typedef struct {
                      2 = CTA pairs (2-SM clusters, tcgen05 cta_group::2) on 256 x 256 tiles */
   int tail_split; /* tensor-core path: 0 = cut the tiles of the last partial round of the
                      persistent grid into 128- or 64-column pieces, 1 = keep whole tiles */
+  int skinny_tiles; /* skinny path: 128-column tiles per CTA sharing each A block (1 or 2);
+                       0 = automatic */
+  int reserved[3];
 } fgemm_opts;
 
 /*
@@ -173,7 +176,8 @@ typedef struct {
   int cluster;        /* CTAs per cluster: 2 for CTA pairs, the K split on the skinny path */
   int tiles;          /* output tiles (tensor-core and skinny paths) */
   int work_items;     /* persistent work items, after cutting the last round into pieces */
-  int tail_split;     /* pieces per tile of the last round (1 = whole tiles) */
+  int tail_split;     /* pieces per tile of the last round (1 = whole tiles); on the skinny
+                         path: 128-column tiles per CTA */
   int resident_pairs; /* CTA pairs resident at once (pair mode; 0 otherwise) */
   int reserved;
 } fgemm_plan_info;

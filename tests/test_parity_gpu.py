@@ -155,11 +155,14 @@ SKINNY_SHAPES = [(1, 8, 8, 1), (1, 136, 72, 2), (5, 264, 520, 3), (16, 1032, 204
 
 @pytest.mark.parametrize("M,N,K,split", SKINNY_SHAPES)
 @pytest.mark.parametrize("gate", [False, True])
-def test_skinny_integer_bit_exact(M, N, K, split, gate):
-    # split K over a cluster; (64, 136, 8, 4) leaves some CTAs of the cluster with no K block
+@pytest.mark.parametrize("tiles", [1, 2])
+def test_skinny_integer_bit_exact(M, N, K, split, gate, tiles):
+    # split K over a cluster; (64, 136, 8, 4) leaves some CTAs of the cluster with no K block;
+    # tiles = 2 gives each CTA two 128-column tiles sharing A (N = 136 leaves the second ragged)
     for ab, bt, ot in ((BF16, BF16, BF16), (F16, F32, F32)):
         p = gen.integer_problem(M, N, K, ab, bt, seed=M + N + K + split, gate=gate)
-        out, path = run_fused(p, M, N, K, ab, bt, ot, gate=gate, opts={"split_k": split})
+        out, path = run_fused(p, M, N, K, ab, bt, ot, gate=gate,
+                              opts={"split_k": split, "skinny_tiles": tiles})
         assert path == fg.PATH_SKINNY
         ref = oracle_run(p, M, N, K, ab, bt, ot, gate=gate)
         got = down(out, ot)
