@@ -210,6 +210,28 @@ def time_steps(prob, steps, warmup, stream, opts=None, unfused=False, barrier=No
     return start.elapsed_time(end) / steps, path
 
 
+def time_graph(prob, steps, warmup, stream, opts=None, reps=5):
+    """Device time per call with host launch overhead removed: `steps` calls captured once in a
+    CUDA graph, the graph replayed `reps` times between CUDA events."""
+    import torch
+    for i in range(warmup):
+        prob.call(i, stream.cuda_stream, opts)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(steps):
+            prob.call(i, stream.cuda_stream, opts)
+    g.replay()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(reps):
+        g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / (steps * reps)
+
+
 def e2e_steps(prob, steps, stream):
     """Host buffers in pinned memory; H2D of A, B, bias (and Y), the call, D2H of out."""
     import torch
@@ -428,12 +450,13 @@ def run_sweep(args):
             variants = [None, {"tail_split": 1}, {"cta_pair": 1}, {"cta_pair": 1, "tail_split": 1}]
         for opts in variants:
             g = (opts or {}).get("group_m")
-            ms, path = time_steps(prob, steps, 5, stream, opts=opts)
+            ms_stream, path = time_steps(prob, steps, 5, stream, opts=opts)
+            ms = time_graph(prob, min(steps, 50), 3, stream, opts=opts)
             t = w.flops / (ms * 1e-3) / 1e12
             gbs = w.unavoidable_bytes() / (ms * 1e-3) / 1e9
             t_roof = max(w.flops / (pk["bf16_tflops"] * 1e12), w.unavoidable_bytes() / (pk["hbm_gbs"] * 1e9))
             r = {"workload": name, "opts": opts or "auto", "plan": prob.plan(opts),
-                 "path": fg.PATH_NAMES.get(path), "us": ms * 1e3,
+                 "path": fg.PATH_NAMES.get(path), "us": ms * 1e3, "us_stream_loop": ms_stream * 1e3,
                  "tflops": t, "gbs": gbs, "roofline_frac": t_roof / (ms * 1e-3),
                  "pct_bf16_peak": 100 * t / pk["bf16_tflops"], "pct_hbm": 100 * gbs / pk["hbm_gbs"]}
             results.append(r)

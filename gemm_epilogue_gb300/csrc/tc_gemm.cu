@@ -433,8 +433,14 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
                        const TcParams& p, int grid, cudaStream_t s) {
   auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR>;
   constexpr uint32_t smem = Cfg<PAIR>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!opted_in[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    opted_in[dev] = true;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(THREADS);
@@ -454,7 +460,10 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
 // number of pairs that fit at once can be below SMs / 2.
 template <int EPI, int OUT_BYTES>
 int max_pairs() {
-  static int cached = 0;  // per process; the library targets one GPU type
+  static int cached_dev[64] = {};  // per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  int& cached = cached_dev[dev];
   if (cached == 0) {
     auto k = tc_gemm_kernel<EPI, OUT_BYTES, true>;
     constexpr uint32_t smem = Cfg<true>::SMEM_BYTES;
