@@ -224,10 +224,11 @@ def time_graph(prob, steps, warmup, stream, opts=None, reps=5):
     g.replay()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(reps):
-        g.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / (steps * reps)
 
@@ -445,7 +446,8 @@ def run_sweep(args):
         if w.name.startswith("ffn"):
             variants = [{"group_m": g} for g in (1, 4, 8)]
         elif w.name.startswith("skinny"):
-            variants = [None] + [{"split_k": s, "skinny_tiles": t} for t in (1, 2) for s in (2, 3, 4)]
+            variants = [None] + [{"split_k": s, "skinny_tiles": t, "stages": g}
+                                 for t in (1, 2) for s in (2, 4) for g in (2, 3, 4, 6, 8)]
         else:
             variants = [None, {"tail_split": 1}, {"cta_pair": 1}, {"cta_pair": 1, "tail_split": 1}]
         for opts in variants:

@@ -41,7 +41,8 @@ class Opts(ctypes.Structure):
     _fields_ = [("group_m", ctypes.c_int), ("path", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("timeout_ms", ctypes.c_int),
                 ("b_desc_swap", ctypes.c_int), ("cta_pair", ctypes.c_int), ("tail_split", ctypes.c_int),
-                ("skinny_tiles", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("skinny_tiles", ctypes.c_int), ("stages", ctypes.c_int),
+                ("reserved", ctypes.c_int * 2)]
 
 
 class PlanInfo(ctypes.Structure):

@@ -155,7 +155,7 @@ int validate(const Call& c, bool* nothing) {
     const fgemm_opts& o = *c.opts;
     if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
         o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
-        o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2)
+        o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -215,11 +215,12 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
 }
 
 struct SkPlan {
-  int mpad, nt, tmem_cols, tiles_n, groups, split;
+  int mpad, nt, tmem_cols, tiles_n, groups, split, stages;
 };
 
 SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
   SkPlan s{};
+  s.stages = c.opts ? c.opts->stages : 0;
   s.mpad = static_cast<int>((c.M + 15) / 16 * 16);
   s.tiles_n = static_cast<int>((c.N + skinny_block_n() - 1) / skinny_block_n());
   const int kb = static_cast<int>((c.K + 63) / 64);
@@ -237,7 +238,7 @@ SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
       if (split < 1) split = 1;
     }
     s.split = split;
-    if (nt == 1 || skinny_fits(s.mpad, nt, split)) break;
+    if (nt == 1 || skinny_fits(s.mpad, nt, split, s.stages)) break;
   }
   s.tmem_cols = 32;
   while (s.tmem_cols < s.nt * s.mpad) s.tmem_cols *= 2;
@@ -295,6 +296,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   p.nt = s.nt;
   p.tmem_cols = s.tmem_cols;
   p.split = s.split;
+  p.stages = s.stages;
   p.ab_type = c.t.ab;
   p.bias_type = c.t.bias;
   p.out_type = c.t.out;
@@ -306,7 +308,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  if (!skinny_fits(s.mpad, s.nt, s.split)) return FGEMM_ERR_INVALID_VALUE;
+  if (!skinny_fits(s.mpad, s.nt, s.split, s.stages)) return FGEMM_ERR_INVALID_VALUE;
   return status_of(launch_skinny(c.epi, tmB, tmA, p, s.groups * s.split, c.stream));
 }
 

@@ -61,6 +61,7 @@ struct SkParams {
   int nt;         // 128-column tiles per CTA (1 or 2), sharing each staged block of A
   int tmem_cols;  // power of two >= 32 and >= nt * mpad
   int split;      // CTAs per cluster splitting K (1..8)
+  int stages;     // ring depth requested (0 = default)
   int ab_type, bias_type, out_type;  // Elem
   const void* bias;
   const void* Y;
@@ -74,7 +75,7 @@ cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tm
 int skinny_block_n();
 int skinny_max_m();
 // Whether the stage ring and the cluster-reduction buffer fit in shared memory.
-bool skinny_fits(int mpad, int nt, int split);
+bool skinny_fits(int mpad, int nt, int split, int stages);
 
 cudaError_t launch_generic(int epi, const SimtParams& p, cudaStream_t s);
 

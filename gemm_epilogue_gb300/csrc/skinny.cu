@@ -39,12 +39,16 @@ enum { SITE_PROD_EMPTY = 16, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN };
 __host__ __device__ inline uint32_t stage_bytes(int mpad, int nt) {
   return static_cast<uint32_t>(nt) * B_TILE_BYTES + static_cast<uint32_t>(mpad) * 128u;
 }
-__host__ __device__ inline int num_stages(int mpad, int nt) {
+// Ring depth: `want` stages (0 = as many as fit, at most 6), capped by the stage area.
+__host__ __device__ inline int num_stages(int mpad, int nt, int want) {
   int s = static_cast<int>(STAGE_AREA_MAX / stage_bytes(mpad, nt));
-  return s > MAX_STAGES ? MAX_STAGES : s;
+  if (s > MAX_STAGES) s = MAX_STAGES;
+  const int cap = want > 0 ? want : 6;
+  return s > cap ? cap : s;
 }
-__host__ inline uint32_t smem_bytes(int mpad, int nt) {
-  return static_cast<uint32_t>(num_stages(mpad, nt)) * stage_bytes(mpad, nt) + BAR_BYTES + 1024;
+__host__ inline uint32_t smem_bytes(int mpad, int nt, int want) {
+  return static_cast<uint32_t>(num_stages(mpad, nt, want)) * stage_bytes(mpad, nt) + BAR_BYTES +
+         1024;
 }
 // Receive area of the cluster reduction, overlaid on the stage ring.
 __host__ __device__ inline uint32_t recv_bytes(int mpad, int nt, int split) {
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
   const int nt = p.nt;
-  const int stages = num_stages(p.mpad, nt);
+  const int stages = num_stages(p.mpad, nt, p.stages);
   const uint32_t sbytes = stage_bytes(p.mpad, nt);
   const uint32_t bar0 = sbase + static_cast<uint32_t>(stages) * sbytes;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -291,7 +295,7 @@ template <int EPI>
 cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkParams& p, int ctas,
                        cudaStream_t s) {
   auto k = skinny_kernel<EPI>;
-  const uint32_t smem = smem_bytes(p.mpad, p.nt);
+  const uint32_t smem = smem_bytes(p.mpad, p.nt, p.stages);
   static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -320,10 +324,9 @@ cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkPar
 
 int skinny_block_n() { return sk::BN; }
 int skinny_max_m() { return sk::MAX_MPAD; }
-bool skinny_fits(int mpad, int nt, int split) {
-  return sk::num_stages(mpad, nt) >= 2 &&
-         sk::recv_bytes(mpad, nt, split) <=
-             static_cast<uint32_t>(sk::num_stages(mpad, nt)) * sk::stage_bytes(mpad, nt);
+bool skinny_fits(int mpad, int nt, int split, int stages) {
+  const int s = sk::num_stages(mpad, nt, stages);
+  return s >= 2 && sk::recv_bytes(mpad, nt, split) <= static_cast<uint32_t>(s) * sk::stage_bytes(mpad, nt);
 }
 
 cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA, const SkParams& p,

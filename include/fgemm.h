@@ -87,7 +87,8 @@ typedef struct {
                      persistent grid into 128- or 64-column pieces, 1 = keep whole tiles */
   int skinny_tiles; /* skinny path: 128-column tiles per CTA sharing each A block (1 or 2);
                        0 = automatic */
-  int reserved[3];
+  int stages;     /* skinny path: TMA ring depth 2..8 (capped by shared memory); 0 = default */
+  int reserved[2];
 } fgemm_opts;
 
 /*
