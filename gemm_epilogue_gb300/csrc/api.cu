@@ -219,26 +219,35 @@ struct SkPlan {
 };
 
 SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
+  // Default shape of the grid: a streaming kernel wants every SM busy and plenty of bytes in
+  // flight, so aim for two resident CTAs per SM (ring depth chosen so that two fit) and split K
+  // until the clusters cover them; two 128-column tiles per CTA once A is wide (M >= 64), which
+  // halves A's re-reads from L2.
   SkPlan s{};
-  s.stages = c.opts ? c.opts->stages : 0;
   s.mpad = static_cast<int>((c.M + 15) / 16 * 16);
   s.tiles_n = static_cast<int>((c.N + skinny_block_n() - 1) / skinny_block_n());
   const int kb = static_cast<int>((c.K + 63) / 64);
-  // Two 128-column tiles per CTA halve the re-reads of A, which matter once A is wide (M >= 64).
+  const int want_stages = c.opts ? c.opts->stages : 0;
   int nt = (c.opts && c.opts->skinny_tiles > 0) ? c.opts->skinny_tiles
                                                 : ((s.mpad >= 64 && s.tiles_n >= 2) ? 2 : 1);
   for (;; --nt) {
     s.nt = nt;
     s.groups = (s.tiles_n + nt - 1) / nt;
     int split = (c.opts && c.opts->split_k > 0) ? c.opts->split_k : 0;
-    if (split == 0) {  // enough clusters to cover the SMs, each split at least 4 K blocks
-      split = d->num_sms / (s.groups > 0 ? s.groups : 1);
+    if (split == 0) {
+      split = (2 * d->num_sms) / (s.groups > 0 ? s.groups : 1);
       if (split > kb / 4) split = kb / 4;
       if (split > 8) split = 8;
       if (split < 1) split = 1;
     }
     s.split = split;
-    if (nt == 1 || skinny_fits(s.mpad, nt, split, s.stages)) break;
+    int stages = want_stages;
+    if (stages == 0) {  // deepest ring with which two CTAs still fit on one SM
+      stages = 6;
+      while (stages > 2 && skinny_smem_bytes(s.mpad, nt, split, stages) > 113 * 1024) --stages;
+    }
+    s.stages = stages;
+    if (nt == 1 || skinny_fits(s.mpad, nt, split, stages)) break;
   }
   s.tmem_cols = 32;
   while (s.tmem_cols < s.nt * s.mpad) s.tmem_cols *= 2;

@@ -76,6 +76,7 @@ int skinny_block_n();
 int skinny_max_m();
 // Whether the stage ring and the cluster-reduction buffer fit in shared memory.
 bool skinny_fits(int mpad, int nt, int split, int stages);
+uint32_t skinny_smem_bytes(int mpad, int nt, int split, int stages);
 
 cudaError_t launch_generic(int epi, const SimtParams& p, cudaStream_t s);
 

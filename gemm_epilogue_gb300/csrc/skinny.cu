@@ -46,15 +46,20 @@ __host__ __device__ inline int num_stages(int mpad, int nt, int want) {
   const int cap = want > 0 ? want : 6;
   return s > cap ? cap : s;
 }
-__host__ inline uint32_t smem_bytes(int mpad, int nt, int want) {
-  return static_cast<uint32_t>(num_stages(mpad, nt, want)) * stage_bytes(mpad, nt) + BAR_BYTES +
-         1024;
-}
 // Receive area of the cluster reduction, overlaid on the stage ring.
 __host__ __device__ inline uint32_t recv_bytes(int mpad, int nt, int split) {
   const int rows = BN * nt;
   const int maxslice = (rows + split - 1) / split;
   return static_cast<uint32_t>(split * maxslice * (mpad + 4)) * 4u;
+}
+// Shared memory before the barriers: the larger of the ring and the reduction's receive area.
+__host__ __device__ inline uint32_t data_bytes(int mpad, int nt, int split, int want) {
+  const uint32_t ring = static_cast<uint32_t>(num_stages(mpad, nt, want)) * stage_bytes(mpad, nt);
+  const uint32_t recv = recv_bytes(mpad, nt, split);
+  return ((ring > recv ? ring : recv) + 1023u) & ~1023u;
+}
+__host__ inline uint32_t smem_bytes(int mpad, int nt, int split, int want) {
+  return data_bytes(mpad, nt, split, want) + BAR_BYTES + 1024;
 }
 
 __device__ __forceinline__ float ld_any(const void* p, int64_t i, int type) {
@@ -83,12 +88,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int nt = p.nt;
   const int stages = num_stages(p.mpad, nt, p.stages);
   const uint32_t sbytes = stage_bytes(p.mpad, nt);
-  const uint32_t bar0 = sbase + static_cast<uint32_t>(stages) * sbytes;
+  const uint32_t dbytes = data_bytes(p.mpad, nt, p.split, p.stages);
+  const uint32_t bar0 = sbase + dbytes;
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   // barriers: full[0..7], empty[8..15], acc_full 16, mma_done 17
   constexpr int BAR_FULL = 0, BAR_EMPTY = MAX_STAGES, BAR_ACC_FULL = 2 * MAX_STAGES,
                 BAR_MMA_DONE = 2 * MAX_STAGES + 1;
-  uint8_t* bar_area = smem + static_cast<uint32_t>(stages) * sbytes;
+  uint8_t* bar_area = smem + dbytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 200);
 
@@ -193,7 +199,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   // Row n (0 <= n < W) of the CTA's columns is owned by CTA owner(n), the r with
   // W r / S <= n < W (r + 1) / S.  Each CTA pushes its partial row n into the owner's receive area
   // recv[src][n - first_row(owner)][m] (row stride mpad + 4 floats), which overlays the owner's
-  // stage ring; so the first cluster barrier makes sure every CTA has finished its main loop
+  // stage ring (or extends past it); so the first cluster barrier makes sure every CTA has
+  // finished its main loop
   // before any push, and the second one that every push has landed before the owners read.
   __syncwarp();
   if (S > 1)
@@ -295,7 +302,7 @@ template <int EPI>
 cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkParams& p, int ctas,
                        cudaStream_t s) {
   auto k = skinny_kernel<EPI>;
-  const uint32_t smem = smem_bytes(p.mpad, p.nt, p.stages);
+  const uint32_t smem = smem_bytes(p.mpad, p.nt, p.split, p.stages);
   static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -325,8 +332,10 @@ cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkPar
 int skinny_block_n() { return sk::BN; }
 int skinny_max_m() { return sk::MAX_MPAD; }
 bool skinny_fits(int mpad, int nt, int split, int stages) {
-  const int s = sk::num_stages(mpad, nt, stages);
-  return s >= 2 && sk::recv_bytes(mpad, nt, split) <= static_cast<uint32_t>(s) * sk::stage_bytes(mpad, nt);
+  return sk::num_stages(mpad, nt, stages) >= 2 && sk::smem_bytes(mpad, nt, split, stages) <= 232448;
+}
+uint32_t skinny_smem_bytes(int mpad, int nt, int split, int stages) {
+  return sk::smem_bytes(mpad, nt, split, stages);
 }
 
 cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA, const SkParams& p,
