@@ -219,17 +219,16 @@ struct SkPlan {
 };
 
 SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
-  // Default shape of the grid: a streaming kernel wants every SM busy and plenty of bytes in
-  // flight, so aim for two resident CTAs per SM (ring depth chosen so that two fit) and split K
-  // until the clusters cover them; two 128-column tiles per CTA once A is wide (M >= 64), which
-  // halves A's re-reads from L2.
+  // Default shape of the grid (measured on GB300 for N = K = 8192, M = 1 .. 128): every CTA must
+  // be resident at once, two per SM, so the ring is at most 4 stages and small enough that two
+  // CTAs fit on an SM, and K is split until the clusters cover 2 x SMs.  One 128-column tile per
+  // CTA: sharing A between two tiles halves A's L2 re-reads but measured slower.
   SkPlan s{};
   s.mpad = static_cast<int>((c.M + 15) / 16 * 16);
   s.tiles_n = static_cast<int>((c.N + skinny_block_n() - 1) / skinny_block_n());
   const int kb = static_cast<int>((c.K + 63) / 64);
   const int want_stages = c.opts ? c.opts->stages : 0;
-  int nt = (c.opts && c.opts->skinny_tiles > 0) ? c.opts->skinny_tiles
-                                                : ((s.mpad >= 64 && s.tiles_n >= 2) ? 2 : 1);
+  int nt = (c.opts && c.opts->skinny_tiles > 0) ? c.opts->skinny_tiles : 1;
   for (;; --nt) {
     s.nt = nt;
     s.groups = (s.tiles_n + nt - 1) / nt;
@@ -242,8 +241,8 @@ SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
     }
     s.split = split;
     int stages = want_stages;
-    if (stages == 0) {  // deepest ring with which two CTAs still fit on one SM
-      stages = 6;
+    if (stages == 0) {  // deepest ring (at most 4) with which two CTAs still fit on one SM
+      stages = 4;
       while (stages > 2 && skinny_smem_bytes(s.mpad, nt, split, stages) > 113 * 1024) --stages;
     }
     s.stages = stages;
