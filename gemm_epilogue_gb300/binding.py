@@ -42,7 +42,7 @@ class Opts(ctypes.Structure):
                 ("max_ctas", ctypes.c_int), ("timeout_ms", ctypes.c_int),
                 ("b_desc_swap", ctypes.c_int), ("cta_pair", ctypes.c_int), ("tail_split", ctypes.c_int),
                 ("skinny_tiles", ctypes.c_int), ("stages", ctypes.c_int),
-                ("reserved", ctypes.c_int * 2)]
+                ("inject_stall", ctypes.c_int), ("reserved", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):

@@ -29,6 +29,7 @@ struct TcParams {
   uint32_t b_lbo, b_sbo;  // B (MN-major) descriptor byte offsets
   uint64_t timeout_ns;
   int* err;        // device error word
+  int inject_stall;  // diagnostic: CTA 0 skips the loads of its first stage (see fgemm_opts)
 };
 
 // Generic CUDA-core kernel and elementwise kernels: plain pointers.
@@ -69,6 +70,7 @@ struct SkParams {
   uint32_t idesc;
   uint64_t timeout_ns;
   int* err;
+  int inject_stall;  // diagnostic: CTA 0 skips the loads of its first stage (see fgemm_opts)
 };
 cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           const SkParams& p, int ctas, cudaStream_t s);

@@ -144,6 +144,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t fb = bar(BAR_FULL + stage);
         mbar_arrive_expect_tx(fb, sbytes);
         const uint32_t dst = sbase + stage * sbytes;
+        // diagnostic stall: announce the stage's bytes but never load them
+        if (p.inject_stall && blockIdx.x == 0 && kb == kb0) {
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == static_cast<uint32_t>(stages)) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         for (int c = 0; c < 2 * nt; ++c)
           tma_load_2d(dst + c * B_BOX_BYTES, &tmB, fb, n0 + 64 * c, kb * BK, pol_b);
         tma_load_2d(dst + static_cast<uint32_t>(nt) * B_TILE_BYTES, &tmA, fb, kb * BK, 0, pol_a);

@@ -218,7 +218,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (leader) mbar_arrive_expect_tx(fb, tx);
           const uint32_t a_dst = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_dst = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
-          if constexpr (PAIR) {
+          // diagnostic stall: announce the stage's bytes but never load them
+          const bool stall = p.inject_stall && blockIdx.x == 0 && t == unit && kb == 0;
+          if (stall) {
+          } else if constexpr (PAIR) {
             const uint32_t lfb = lead_bar(BAR_FULL + stage);
             tma_load_2d_pair(a_dst, &tmA, lfb, kb * BK, m0, pol);
             for (int c = 0; c < boxes; ++c)

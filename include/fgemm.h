@@ -88,7 +88,12 @@ typedef struct {
   int skinny_tiles; /* skinny path: 128-column tiles per CTA sharing each A block (1 or 2);
                        0 = automatic */
   int stages;     /* skinny path: TMA ring depth 2..8 (capped by shared memory); 0 = default */
-  int reserved[2];
+  int inject_stall; /* diagnostic for testing the bounded waits: 1 = the first CTA's producer
+                       announces its first stage but issues none of its loads, so the MMA's wait
+                       on that stage can never complete; it expires after timeout_ms, the kernel
+                       drains and exits, and fgemm_device_status reports FGEMM_ERR_TIMEOUT.
+                       The output of that call is undefined.  Tensor-core and skinny paths. */
+  int reserved;
 } fgemm_opts;
 
 /*
