@@ -66,6 +66,12 @@ WORKLOADS = {
     "ffn_up_8192x14336x4096": Workload("ffn_up_8192x14336x4096", 8192, 14336, 4096,
                                        BF16, BF16, BF16, "bias_relu", 1.0 / 64.0, "uniform", 3),
 }
+# The GLU block at the K values of the page's own measurements ("Optimizing GEMM + Activation on
+# CDNA4 with TLX", "Configuration Details": M = 1024, N = 21568, fp16, K in {256, 512, 1024}).
+for _k in (256, 512, 1024):
+    WORKLOADS[f"glu_gate_1024x21568x{_k}"] = Workload(f"glu_gate_1024x21568x{_k}", 1024, 21568, _k,
+                                                      F16, F16, F16, "gate", 1.0 / 64.0, "normal",
+                                                      5)
 for _m in (1, 16, 64, 128):
     WORKLOADS[f"skinny_M{_m}_8192"] = Workload(f"skinny_M{_m}_8192", _m, 8192, 8192, BF16, BF16,
                                                BF16, "bias_relu", 1.0 / 90.0, "normal", 4)

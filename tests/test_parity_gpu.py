@@ -300,7 +300,8 @@ def test_unfused_chain_matches_oracle(inter_f32, gate):
 # ------------------------------------------------------------ full-size sampled --
 
 FULL = ["square_4096", "glu_gate_1024x21568x4096", "ffn_up_8192x14336x4096", "skinny_M1_8192",
-        "skinny_M16_8192", "skinny_M64_8192", "skinny_M128_8192"]
+        "skinny_M16_8192", "skinny_M64_8192", "skinny_M128_8192", "glu_gate_1024x21568x256",
+        "glu_gate_1024x21568x512", "glu_gate_1024x21568x1024"]
 
 
 @pytest.mark.parametrize("name", FULL)
