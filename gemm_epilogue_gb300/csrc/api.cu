@@ -259,12 +259,17 @@ int run_tc(const Call& c, DeviceInfo* d) {
   if (t.num_tiles < 0) return FGEMM_ERR_INVALID_VALUE;
   const int BM = tc_block_m(), BN = tc_block_n();
   const int TILE_M = t.pair ? 2 * BM : BM;
-  CUtensorMap tmA, tmB, tmO;
+  CUtensorMap tmA, tmB, tmO, tmY;
   const uint32_t out_box_cols = (c.t.out == ELEM_F32) ? 32 : 64;
   if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, 64) ||
       !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
       !encode_2d(&tmO, c.t.out, c.out, c.M, c.N, 32, out_box_cols))
     return FGEMM_ERR_LAUNCH;
+  if (c.epi == EPI_GATE && c.t.out != ELEM_F32) {
+    if (!encode_2d(&tmY, c.t.ab, c.Y, c.M, c.N, 32, 64)) return FGEMM_ERR_LAUNCH;
+  } else {
+    tmY = tmO;  // unused
+  }
   TcParams p{};
   p.M = static_cast<int>(c.M);
   p.N = static_cast<int>(c.N);
@@ -289,7 +294,8 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
   p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
-  return status_of(launch_tc(c.epi, tmA, tmB, tmO, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
+  return status_of(
+      launch_tc(c.epi, tmA, tmB, tmO, tmY, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
 }
 
 int run_skinny(const Call& c, DeviceInfo* d) {

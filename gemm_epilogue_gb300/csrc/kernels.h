@@ -46,9 +46,10 @@ struct SimtParams {
 };
 
 // pair = true: 2-CTA clusters (grid even), 256 x 256 tiles, tiles_m counted in 256-row tiles.
+// tmY: the gate's Y (M x N, operand type, 32 x 64 boxes, 128-byte swizzle); any map otherwise.
 cudaError_t launch_tc(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                      const CUtensorMap& tmOut, const TcParams& p, int grid, bool pair,
-                      cudaStream_t s);
+                      const CUtensorMap& tmOut, const CUtensorMap& tmY, const TcParams& p,
+                      int grid, bool pair, cudaStream_t s);
 // How many CTA pairs of the pair-mode kernel can be resident at once (clusters need two free SMs
 // in one GPC); cached per process.
 int tc_max_active_pairs(int epi, int out_type);

@@ -39,9 +39,11 @@ constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;    // 8 KB: 64 K-rows x 64 N-colum
 constexpr uint32_t EPI_BUF_BYTES = 32 * 128;     // 32 rows x 128 bytes
 constexpr uint32_t TMEM_COLS = 512;
 
-template <bool PAIR>
+// YS: the gate's Y is staged through shared memory by TMA (16-bit outputs), which costs one ring
+// stage of shared memory for a 64 KB Y / output block.
+template <bool PAIR, bool YS = false>
 struct Cfg {
-  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int STAGES = PAIR ? (YS ? 5 : 6) : (YS ? 3 : 4);
   static constexpr int B_BOXES = PAIR ? 2 : 4;                 // 64-column B boxes per CTA
   static constexpr uint32_t B_STAGE_BYTES = B_BOXES * B_BOX_BYTES;
   static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
@@ -50,7 +52,8 @@ struct Cfg {
   static constexpr uint32_t SMEM_A = 0;
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
   static constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
-  static constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * 2 * EPI_BUF_BYTES;
+  static constexpr uint32_t EPI_WARP_BYTES = YS ? 4 * EPI_BUF_BYTES : 2 * EPI_BUF_BYTES;
+  static constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * EPI_WARP_BYTES;
   static constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + barriers + 1024-B alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -62,11 +65,13 @@ constexpr int BAR_EMPTY = MAX_STAGES;
 constexpr int BAR_ACC_FULL = 2 * MAX_STAGES;
 constexpr int BAR_ACC_EMPTY = 2 * MAX_STAGES + 2;
 constexpr int BAR_MMA_DONE = 2 * MAX_STAGES + 4;
+constexpr int BAR_Y = 2 * MAX_STAGES + 5;  // one per epilogue warp (gate with staged Y)
 constexpr uint32_t OFF_TMEM_SLOT = 192;  // after the 17 barriers
 constexpr uint32_t OFF_ABORT = 200;
 
 // wait sites recorded with a timeout
-enum { SITE_PROD_EMPTY = 1, SITE_MMA_ACC_EMPTY, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN };
+enum { SITE_PROD_EMPTY = 1, SITE_MMA_ACC_EMPTY, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN,
+       SITE_EPI_Y };
 
 // Bounded wait that ignores the abort flag: used only to drain copies / MMAs already in flight.
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
@@ -133,11 +138,13 @@ __device__ __forceinline__ void load_bias_granule(const TcParams& p, int col, fl
 template <int EPI, int OUT_BYTES, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmOut, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmY,
+                   const TcParams p) {
   constexpr int CH = 128 / OUT_BYTES;  // output columns per 128-byte staging row
   constexpr int G = 16 / OUT_BYTES;    // columns per 16-byte granule
   constexpr int NG = CH / G;           // granules per chunk (8)
-  using C = Cfg<PAIR>;
+  constexpr bool YS = (EPI == EPI_GATE) && (OUT_BYTES == 2);
+  using C = Cfg<PAIR, YS>;
   constexpr int STAGES = C::STAGES;
   constexpr int CG = PAIR ? 2 : 1;
   constexpr uint32_t SMEM_A = C::SMEM_A, SMEM_B = C::SMEM_B, SMEM_EPI = C::SMEM_EPI,
@@ -171,6 +178,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar(BAR_ACC_EMPTY + b), (PAIR ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(bar(BAR_MMA_DONE), 1);
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(bar(BAR_Y + w), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -178,6 +186,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmOut);
+    if (YS) tma_prefetch_desc(&tmY);
   }
   if (warp == 1) {
     tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS);
@@ -295,12 +304,112 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ew = warp - 2;
-    const uint32_t ebuf = sbase + SMEM_EPI + static_cast<uint32_t>(ew) * 2u * EPI_BUF_BYTES;
+    const uint32_t ebuf = sbase + SMEM_EPI + static_cast<uint32_t>(ew) * C::EPI_WARP_BYTES;
     const bool out_bf = p.out_type == ELEM_BF16;
     const bool y_bf = p.ab_bf16 != 0;
     const uint64_t pol_out = policy_evict_first();
-    uint32_t nstore = 0;
     int it = 0;
+    if constexpr (YS) {
+      // Gate with Y staged by TMA: the warp's 32 x 256 block of Y lands in its 16 KB region (four
+      // 128-byte-swizzled 32 x 64 chunks) while the tile's main loop still runs; the epilogue reads
+      // y from there, writes the result over it, and stores each chunk with one TMA store.
+      const uint32_t ybar = bar(BAR_Y + ew);
+      uint32_t y_par = 0;
+      auto issue_y = [&](int t) -> bool {  // warp-uniform result
+        const Work w = work_of(p, t);
+        const int r0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + 32 * q;
+        if (r0 >= p.M) return false;
+        int nchunks = 0;
+        for (int c = 0; c < w.width / CH; ++c)
+          if (w.col0 + c * CH < p.N) ++nchunks;
+        if (lane == 0) {
+          bulk_wait_read<0>();  // the stores that last read this region are done with it
+          mbar_arrive_expect_tx(ybar, static_cast<uint32_t>(nchunks) * EPI_BUF_BYTES);
+          for (int c = 0; c < nchunks; ++c)
+            tma_load_2d(ebuf + c * EPI_BUF_BYTES, &tmY, ybar, w.col0 + c * CH, r0, pol_out);
+        }
+        return true;
+      };
+      bool y_issued = (unit < p.num_items) ? issue_y(unit) : false;
+      for (int t = unit; t < p.num_items; t += units, ++it) {
+        const Work wk = work_of(p, t);
+        const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = wk.col0;
+        const int nch = wk.width / CH;
+        const int b = it & 1;
+        const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
+        const int row0 = m0 + 32 * q;
+        const bool rows_live = row0 < p.M;  // warp-uniform
+
+        if (!mbar_wait(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
+          break;
+        tc_fence_after();
+        if (y_issued) {
+          if (!mbar_wait(ybar, y_par, abort_flag, tmo, p.err, SITE_EPI_Y)) break;
+          y_par ^= 1u;
+        }
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+          const int col0 = n0 + c * CH;
+          if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
+          uint32_t acc[CH];
+          __syncwarp();  // tcgen05.ld is warp-collective
+          {
+            uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[0]);
+            uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[32]);
+            tmem_ld32(taddr, a0, c * CH);
+            tmem_ld32(taddr, a1, c * CH + 32);
+            tmem_ld_wait();
+          }
+          const uint32_t sb = ebuf + static_cast<uint32_t>(c) * EPI_BUF_BYTES;
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            // 128-byte swizzle: granule g of row `lane` sits at slot g ^ (lane & 7)
+            const uint32_t addr = sb + static_cast<uint32_t>(lane) * 128u +
+                                  (static_cast<uint32_t>(g ^ (lane & 7)) << 4);
+            uint32_t y[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(y[0]), "=r"(y[1]), "=r"(y[2]), "=r"(y[3])
+                         : "r"(addr)
+                         : "memory");
+            float bv[G];
+            load_bias_granule<OUT_BYTES>(p, col0 + g * G, bv);
+            uint32_t packed[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 y2 = unpack2(y[e], y_bf);
+              float x0 = __uint_as_float(acc[g * G + 2 * e]) + bv[2 * e];  // bias once
+              float x1 = __uint_as_float(acc[g * G + 2 * e + 1]) + bv[2 * e + 1];
+              x0 = fmaf(x0, y2.x, x0);  // X + X * Y
+              x1 = fmaf(x1, y2.y, x1);
+              packed[e] = pack2(x0, x1, out_bf);
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[0]),
+                         "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&tmOut, sb, col0, row0, pol_out);
+        }
+        if (lane == 0) bulk_commit();
+        // This warp has finished reading accumulator b: release it to the MMA warp.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR)
+            mbar_arrive_cluster(lead_bar(BAR_ACC_EMPTY + b));
+          else
+            mbar_arrive(bar(BAR_ACC_EMPTY + b));
+        }
+        // Prefetch the Y block of this CTA's next work item (its main loop runs meanwhile).
+        y_issued = (t + units < p.num_items) ? issue_y(t + units) : false;
+      }
+      // After an abort a prefetched Y block may still be landing: wait for it (bounded).
+      if (y_issued) drain_wait(ybar, y_par, tmo, p.err);
+    } else {
+    uint32_t nstore = 0;
     for (int t = unit; t < p.num_items; t += units, ++it) {
       const Work wk = work_of(p, t);
       const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = wk.col0;
@@ -416,6 +525,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive(bar(BAR_ACC_EMPTY + b));
       }
     }
+    }
     if (lane == 0) bulk_wait<0>();
     __syncwarp();
   }
@@ -433,9 +543,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int EPI, int OUT_BYTES, bool PAIR>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                       const TcParams& p, int grid, cudaStream_t s) {
+                       const CUtensorMap& y, const TcParams& p, int grid, cudaStream_t s) {
   auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR>;
-  constexpr uint32_t smem = Cfg<PAIR>::SMEM_BYTES;
+  constexpr uint32_t smem = Cfg<PAIR, EPI == EPI_GATE && OUT_BYTES == 2>::SMEM_BYTES;
   static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -456,7 +566,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, o, p);
+  return cudaLaunchKernelEx(&cfg, k, a, b, o, y, p);
 }
 
 // A persistent grid must be co-resident: clusters of two need two free SMs in one GPC, so the
@@ -469,7 +579,7 @@ int max_pairs() {
   int& cached = cached_dev[dev];
   if (cached == 0) {
     auto k = tc_gemm_kernel<EPI, OUT_BYTES, true>;
-    constexpr uint32_t smem = Cfg<true>::SMEM_BYTES;
+    constexpr uint32_t smem = Cfg<true, EPI == EPI_GATE && OUT_BYTES == 2>::SMEM_BYTES;
     int n = 0;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
       cudaLaunchConfig_t cfg{};
@@ -493,9 +603,10 @@ int max_pairs() {
 
 template <int EPI, int OUT_BYTES>
 cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                               const TcParams& p, int grid, bool pair, cudaStream_t s) {
-  return pair ? launch_one<EPI, OUT_BYTES, true>(a, b, o, p, grid, s)
-              : launch_one<EPI, OUT_BYTES, false>(a, b, o, p, grid, s);
+                               const CUtensorMap& y, const TcParams& p, int grid, bool pair,
+                               cudaStream_t s) {
+  return pair ? launch_one<EPI, OUT_BYTES, true>(a, b, o, y, p, grid, s)
+              : launch_one<EPI, OUT_BYTES, false>(a, b, o, y, p, grid, s);
 }
 
 }  // namespace tc
@@ -513,15 +624,16 @@ int tc_block_m() { return tc::BM; }
 int tc_block_n() { return tc::BN; }
 
 cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                      const TcParams& p, int grid, bool pair, cudaStream_t s) {
+                      const CUtensorMap& y, const TcParams& p, int grid, bool pair,
+                      cudaStream_t s) {
   const bool f32 = p.out_type == ELEM_F32;
   switch (epi) {
-    case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, p, grid, pair, s)
-                              : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, p, grid, pair, s);
-    case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4>(a, b, o, p, grid, pair, s)
-                              : tc::launch_pair_or_not<EPI_GATE, 2>(a, b, o, p, grid, pair, s);
-    default: return f32 ? tc::launch_pair_or_not<EPI_NONE, 4>(a, b, o, p, grid, pair, s)
-                        : tc::launch_pair_or_not<EPI_NONE, 2>(a, b, o, p, grid, pair, s);
+    case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, y, p, grid, pair, s)
+                              : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, y, p, grid, pair, s);
+    case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4>(a, b, o, y, p, grid, pair, s)
+                              : tc::launch_pair_or_not<EPI_GATE, 2>(a, b, o, y, p, grid, pair, s);
+    default: return f32 ? tc::launch_pair_or_not<EPI_NONE, 4>(a, b, o, y, p, grid, pair, s)
+                        : tc::launch_pair_or_not<EPI_NONE, 2>(a, b, o, y, p, grid, pair, s);
   }
 }
 
