@@ -32,7 +32,7 @@ namespace fgemm {
 namespace tc {
 
 constexpr int BM = 128, BN = 256, BK = 64;  // per-CTA rows, tile columns, K per stage
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;  // two warpgroups: each owns half (128) of a tile's columns
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
 constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;    // 8 KB: 64 K-rows x 64 N-columns
@@ -52,7 +52,8 @@ struct Cfg {
   static constexpr uint32_t SMEM_A = 0;
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
   static constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
-  static constexpr uint32_t EPI_WARP_BYTES = YS ? 4 * EPI_BUF_BYTES : 2 * EPI_BUF_BYTES;
+  // per epilogue warp: its 32 x 128 block of Y and results (YS), or one 32-row staging buffer
+  static constexpr uint32_t EPI_WARP_BYTES = YS ? 2 * EPI_BUF_BYTES : EPI_BUF_BYTES;
   static constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * EPI_WARP_BYTES;
   static constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + barriers + 1024-B alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -66,8 +67,8 @@ constexpr int BAR_ACC_FULL = 2 * MAX_STAGES;
 constexpr int BAR_ACC_EMPTY = 2 * MAX_STAGES + 2;
 constexpr int BAR_MMA_DONE = 2 * MAX_STAGES + 4;
 constexpr int BAR_Y = 2 * MAX_STAGES + 5;  // one per epilogue warp (gate with staged Y)
-constexpr uint32_t OFF_TMEM_SLOT = 192;  // after the 17 barriers
-constexpr uint32_t OFF_ABORT = 200;
+constexpr uint32_t OFF_TMEM_SLOT = 224;  // after the 25 barriers
+constexpr uint32_t OFF_ABORT = 232;
 
 // wait sites recorded with a timeout
 enum { SITE_PROD_EMPTY = 1, SITE_MMA_ACC_EMPTY, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN,
@@ -304,13 +305,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ew = warp - 2;
+    const int cbeg = (ew >> 2) * (BN / 2);  // first column (within the tile) of this warpgroup
     const uint32_t ebuf = sbase + SMEM_EPI + static_cast<uint32_t>(ew) * C::EPI_WARP_BYTES;
     const bool out_bf = p.out_type == ELEM_BF16;
     const bool y_bf = p.ab_bf16 != 0;
     const uint64_t pol_out = policy_evict_first();
     int it = 0;
     if constexpr (YS) {
-      // Gate with Y staged by TMA: the warp's 32 x 256 block of Y lands in its 16 KB region (four
+      // Gate with Y staged by TMA: the warp's 32 x 128 block of Y lands in its 8 KB region (two
       // 128-byte-swizzled 32 x 64 chunks) while the tile's main loop still runs; the epilogue reads
       // y from there, writes the result over it, and stores each chunk with one TMA store.
       const uint32_t ybar = bar(BAR_Y + ew);
@@ -320,13 +322,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + 32 * q;
         if (r0 >= p.M) return false;
         int nchunks = 0;
-        for (int c = 0; c < w.width / CH; ++c)
-          if (w.col0 + c * CH < p.N) ++nchunks;
+        for (int c = cbeg; c < cbeg + BN / 2 && c < w.width; c += CH)
+          if (w.col0 + c < p.N) ++nchunks;
+        if (nchunks == 0) return false;
         if (lane == 0) {
           bulk_wait_read<0>();  // the stores that last read this region are done with it
           mbar_arrive_expect_tx(ybar, static_cast<uint32_t>(nchunks) * EPI_BUF_BYTES);
-          for (int c = 0; c < nchunks; ++c)
-            tma_load_2d(ebuf + c * EPI_BUF_BYTES, &tmY, ybar, w.col0 + c * CH, r0, pol_out);
+          for (int j = 0; j < nchunks; ++j)
+            tma_load_2d(ebuf + j * EPI_BUF_BYTES, &tmY, ybar, w.col0 + cbeg + j * CH, r0, pol_out);
         }
         return true;
       };
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
 #pragma unroll 1
-        for (int c = 0; c < nch; ++c) {
+        for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
           const int col0 = n0 + c * CH;
           if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
           uint32_t acc[CH];
@@ -362,7 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld32(taddr, a1, c * CH + 32);
             tmem_ld_wait();
           }
-          const uint32_t sb = ebuf + static_cast<uint32_t>(c) * EPI_BUF_BYTES;
+          const uint32_t sb = ebuf + static_cast<uint32_t>(c - cbeg / CH) * EPI_BUF_BYTES;
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             // 128-byte swizzle: granule g of row `lane` sits at slot g ^ (lane & 7)
@@ -409,7 +412,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       // After an abort a prefetched Y block may still be landing: wait for it (bounded).
       if (y_issued) drain_wait(ybar, y_par, tmo, p.err);
     } else {
-    uint32_t nstore = 0;
     for (int t = unit; t < p.num_items; t += units, ++it) {
       const Work wk = work_of(p, t);
       const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = wk.col0;
@@ -427,7 +429,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
 
 #pragma unroll 1
-      for (int c = 0; c < nch; ++c) {
+      for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
         const int col0 = n0 + c * CH;
         if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
 
@@ -458,8 +460,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
 
         // Staging buffer: wait until the store that last read it has finished reading.
-        const uint32_t sb = ebuf + (nstore & 1u) * EPI_BUF_BYTES;
-        if (lane == 0) bulk_wait_read<1>();
+        const uint32_t sb = ebuf;
+        if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
 
 #pragma unroll
@@ -513,7 +515,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_store_2d(&tmOut, sb, col0, row0, pol_out);
           bulk_commit();
         }
-        ++nstore;
       }
       // This warp has finished reading accumulator b: release it to the MMA warp.
       tc_fence_before();
