@@ -52,6 +52,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete may sleep up to
+// `hint_ns` before the instruction returns (for roles that wait long and are not latency-critical).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait like mbar_wait below, for long, non-critical waits (suspends between polls).
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity,
+                                                 volatile int* abort_flag, uint64_t timeout_ns,
+                                                 int* err, int site) {
+  uint64_t start = 0;
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 2000u)) return true;
+    if (*abort_flag) return false;
+    const uint64_t now = global_ns();
+    if (start == 0) {
+      start = now;
+    } else if (now - start > timeout_ns) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, 6 /* FGEMM_ERR_TIMEOUT */ | (site << 8));
+      return false;
+    }
+  }
+}
+
 // Bounded wait for the phase with parity `parity` of barrier `bar` to complete.  Returns false if
 // the CTA's abort flag is raised or the wait exceeds `timeout_ns`; in the latter case it raises
 // the abort flag and records `site` in the device error word.

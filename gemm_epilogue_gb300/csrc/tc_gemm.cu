@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int row0 = m0 + 32 * q;
         const bool rows_live = row0 < p.M;  // warp-uniform
 
-        if (!mbar_wait(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
+        if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
           break;
         tc_fence_after();
         if (y_issued) {
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int row = row0 + lane;
       const bool rows_live = row0 < p.M;  // warp-uniform
 
-      if (!mbar_wait(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
+      if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
         break;
       tc_fence_after();
       const uint32_t taddr =

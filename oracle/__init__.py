@@ -23,17 +23,17 @@ import threading
 import numpy as np
 
 F16, BF16, F32 = 1, 2, 3
-EPI_RELU, EPI_GATE, EPI_LINEAR = 0, 1, 2
+EPI_RELU, EPI_GATE, EPI_LINEAR, EPI_RESIDUAL = 0, 1, 2, 3
 
 # Negative controls: deliberate mistakes the oracle can be asked to make, so
 # that the tests can show each pin rejects a plausible slip.  OK = the oracle.
 OK = 0
 MUT_RELU_FIRST, MUT_BIAS_ROW, MUT_BIAS_IN_SUM, MUT_DROP_GEMM = 1, 2, 3, 4
-MUT_TRANSPOSE_B, MUT_DROP_LAST_K, MUT_GATE_SIGN = 5, 6, 7
+MUT_TRANSPOSE_B, MUT_DROP_LAST_K, MUT_GATE_SIGN, MUT_RESID_AFTER = 5, 6, 7, 8
 MUTANTS = {"relu_first": MUT_RELU_FIRST, "bias_row": MUT_BIAS_ROW,
            "bias_in_sum": MUT_BIAS_IN_SUM, "drop_gemm": MUT_DROP_GEMM,
            "transpose_b": MUT_TRANSPOSE_B, "drop_last_k": MUT_DROP_LAST_K,
-           "gate_sign": MUT_GATE_SIGN}
+           "gate_sign": MUT_GATE_SIGN, "resid_after": MUT_RESID_AFTER}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -124,7 +124,7 @@ def gemm_epilogue(A, B, bias, M: int, N: int, K: int, ab_type: int, bias_type: i
     A = _bits(A, ab_type) if K > 0 else (None if A is None else _bits(A, ab_type))
     B = _bits(B, ab_type) if K > 0 else (None if B is None else _bits(B, ab_type))
     bias = _bits(bias, bias_type)
-    if epi == EPI_GATE:
+    if epi in (EPI_GATE, EPI_RESIDUAL):
         Y = _bits(Y, ab_type)
     if rows is None:
         nrows, rows_arr = M, None
@@ -138,7 +138,7 @@ def gemm_epilogue(A, B, bias, M: int, N: int, K: int, ab_type: int, bias_type: i
     absdot = np.empty((nrows, N), dtype=np.float64) if want_ref else None
     th = threads or default_threads()
     used = _load().orc_gemm_epilogue(
-        _ptr(A), _ptr(B), _ptr(bias), _ptr(Y if epi == EPI_GATE else None),
+        _ptr(A), _ptr(B), _ptr(bias), _ptr(Y if epi in (EPI_GATE, EPI_RESIDUAL) else None),
         _ptr(out), _ptr(ref), _ptr(absdot), M, N, K, _ptr(rows_arr), nrows,
         ab_type, bias_type, out_type, epi, mutant, th)
     if used < 0:
@@ -154,6 +154,11 @@ def bias_relu(A, B, bias, M, N, K, ab_type, bias_type, out_type, **kw) -> Result
 def addmm_gate(A, B, bias, Y, M, N, K, ab_type, bias_type, out_type, **kw) -> Result:
     """X = A @ B + bias;  out = RNE(X + X * Y) -- X never rounded before the gate."""
     return gemm_epilogue(A, B, bias, M, N, K, ab_type, bias_type, out_type, EPI_GATE, Y=Y, **kw)
+
+
+def bias_residual_relu(A, B, bias, R, M, N, K, ab_type, bias_type, out_type, **kw) -> Result:
+    """out = RNE(max(0, A @ B + bias + R)) -- the residual added before the activation."""
+    return gemm_epilogue(A, B, bias, M, N, K, ab_type, bias_type, out_type, EPI_RESIDUAL, Y=R, **kw)
 
 
 def linear(A, B, bias, M, N, K, ab_type, bias_type, out_type, **kw) -> Result:

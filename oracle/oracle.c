@@ -21,6 +21,12 @@
  *       "Optimizing GEMM + Activation on CDNA4 with TLX", "The GLU Block".
  *       X is never rounded before the gate: the result is rounded once.
  *
+ *   residual  out[i,j] = RNE( max(0, s[i,j] + bias[j] + R[i,j]) )
+ *       "Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "Variants": a same-shape residual
+ *       tile is loaded after the K loop and added to the accumulator before the activation.
+ *       The bias is added first, then R (fp64, so the order only matters at the last bit of a
+ *       sum that is rounded once anyway).
+ *
  *   linear  out[i,j] = RNE( s[i,j] + bias[j] )  (no activation; used only to
  *       pin the reduction against a library matmul and to check the unfused
  *       chain's intermediate).
@@ -54,7 +60,7 @@
 #include <string.h>
 
 enum { ORC_F16 = 1, ORC_BF16 = 2, ORC_F32 = 3 };
-enum { ORC_EPI_RELU = 0, ORC_EPI_GATE = 1, ORC_EPI_LINEAR = 2 };
+enum { ORC_EPI_RELU = 0, ORC_EPI_GATE = 1, ORC_EPI_LINEAR = 2, ORC_EPI_RESIDUAL = 3 };
 
 /*
  * Deliberate mistakes, selectable only to show that the tests' pins catch
@@ -67,10 +73,11 @@ enum { ORC_EPI_RELU = 0, ORC_EPI_GATE = 1, ORC_EPI_LINEAR = 2 };
  *   TRANSPOSE_B   B read as if it were N x K
  *   DROP_LAST_K   the last k term left out
  *   GATE_SIGN     X - X*Y instead of X + X*Y
+ *   RESID_AFTER   ReLU(AB + bias) + R: the residual added after the activation
  */
 enum { ORC_OK = 0, ORC_MUT_RELU_FIRST = 1, ORC_MUT_BIAS_ROW = 2, ORC_MUT_BIAS_IN_SUM = 3,
        ORC_MUT_DROP_GEMM = 4, ORC_MUT_TRANSPOSE_B = 5, ORC_MUT_DROP_LAST_K = 6,
-       ORC_MUT_GATE_SIGN = 7 };
+       ORC_MUT_GATE_SIGN = 7, ORC_MUT_RESID_AFTER = 8 };
 
 /* ---- decoding (definitions of the formats) ---------------------------- */
 
@@ -210,6 +217,11 @@ static double epilogue(int epi, double s, double bias_j, double y, int mutant)
         if (mutant == ORC_MUT_GATE_SIGN)
             return v - v * y;
         return v + v * y;                            /* X + X * Y */
+    case ORC_EPI_RESIDUAL:
+        if (mutant == ORC_MUT_RESID_AFTER)
+            return ((v > 0.0) ? v : 0.0) + y;
+        v = v + y;                                   /* + R[i,j] before the activation */
+        return (v > 0.0) ? v : 0.0;
     default: return v;                               /* linear */
     }
 }
@@ -256,7 +268,8 @@ static void *row_worker(void *arg)
         }
         for (int64_t j = 0; j < N; ++j) {
             const double b = decode(w->bias, (mut == ORC_MUT_BIAS_ROW) ? i % N : j, w->bias_type);
-            const double y = (w->epi == ORC_EPI_GATE) ? decode(w->Y, i * N + j, w->ab_type) : 0.0;
+            const double y = (w->epi == ORC_EPI_GATE || w->epi == ORC_EPI_RESIDUAL)
+                                 ? decode(w->Y, i * N + j, w->ab_type) : 0.0;
             const double v = epilogue(w->epi, (mut == ORC_MUT_BIAS_IN_SUM) ? s[j] - b : s[j], b, y, mut);
             store(w->out, r * N + j, w->out_type, v);
             if (w->ref)
@@ -275,7 +288,7 @@ static void *row_worker(void *arg)
  *   A      M x K row-major (ab_type), may be NULL when K == 0
  *   B      K x N row-major (ab_type), may be NULL when K == 0
  *   bias   N (bias_type)
- *   Y      M x N row-major (ab_type), gate only
+ *   Y      M x N row-major (ab_type): the gate's Y, or the residual R
  *   rows   nrows row indices, or NULL for rows 0..nrows-1
  *   out    nrows x N (out_type): the rounded result for each listed row
  *   ref    nrows x N fp64: the value before the final rounding (may be NULL)

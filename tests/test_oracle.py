@@ -287,6 +287,44 @@ def test_bias_broadcast_direction_rectangular(oracle_mod):
     assert np.array_equal(r.ref, np.tile(np.maximum(np.arange(N) - 2.0, 0), (M, 1)))
 
 
+# ------------------------------------------------------------- residual add --
+
+def test_residual_zero_equals_bias_relu(oracle_mod):
+    M, N, K = 9, 13, 21
+    p = gen.random_problem(M, N, K, BF16, F32, seed=70)
+    zero = np.zeros((M, N), dtype=np.uint16)
+    r = oracle_mod.bias_residual_relu(p.A, p.B, p.bias, zero, M, N, K, BF16, F32, BF16)
+    q = oracle_mod.bias_relu(p.A, p.B, p.bias, M, N, K, BF16, F32, BF16)
+    assert np.array_equal(r.out, q.out) and np.array_equal(r.ref, q.ref)
+
+
+def test_residual_closed_form_and_k_zero(oracle_mod):
+    # B = 0 (and K = 0): out = ReLU(bias + R), the residual added before the activation
+    M, N, K = 4, 6, 5
+    bias = np.array([-3.0, -1.0, 0.0, 1.0, 2.5, -0.5])
+    R = np.array([[1, 2, -1, 0, -3, 0.5]] * M, dtype=np.float64) * np.arange(1, M + 1)[:, None]
+    bb, Rb = enc(oracle_mod, bias, F16), enc(oracle_mod, R, F16)
+    A = enc(oracle_mod, np.ones((M, K)), F16)
+    B = enc(oracle_mod, np.zeros((K, N)), F16)
+    want = np.maximum(bias[None, :] + R, 0.0)
+    assert np.array_equal(oracle_mod.bias_residual_relu(A, B, bb, Rb, M, N, K, F16, F16, F32).ref, want)
+    assert np.array_equal(oracle_mod.bias_residual_relu(None, None, bb, Rb, M, N, 0, F16, F16, F32).ref, want)
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 5, 2), (7, 4, 9), (11, 13, 6)])
+def test_residual_brute_force_and_library_chain(oracle_mod, M, N, K):
+    p = gen.integer_problem(M, N, K, F16, F16, seed=M + K, gate=True)   # Y serves as R
+    r = oracle_mod.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, F16, F16, F16)
+    A64, B64, b64, R64 = (oracle_mod.decode(x, F16) for x in (p.A, p.B, p.bias, p.Y))
+    chain = np.maximum(np.matmul(A64, B64) + b64[None, :] + R64, 0.0)
+    assert np.array_equal(r.ref, chain)
+    assert np.array_equal(r.out, chain.astype(np.float16).view(np.uint16))
+    for i, j in itertools.product(range(M), range(N)):
+        e = sum((Fraction(float(A64[i, k])) * Fraction(float(B64[k, j])) for k in range(K)), Fraction(0))
+        e = max(e + Fraction(float(b64[j])) + Fraction(float(R64[i, j])), Fraction(0))
+        assert Fraction(r.ref[i, j]) == e
+
+
 # --------------------------------------------------------- negative controls --
 
 def _pins_pass(oracle_mod, mutant):
@@ -312,6 +350,11 @@ def _pins_pass(oracle_mod, mutant):
     A64, B64, b64, Y64 = (oracle_mod.decode(x, F16) for x in (p.A, p.B, p.bias, p.Y))
     X = A64 @ B64 + b64[None, :]
     ok &= np.array_equal(gg.ref, X + X * Y64)
+    # residual: added before the activation, checked against the library chain
+    p = gen.integer_problem(5, 4, 3, F16, F16, seed=51, gate=True)
+    rr = oracle_mod.bias_residual_relu(p.A, p.B, p.bias, p.Y, 5, 4, 3, F16, F16, F32, mutant=mutant)
+    A64, B64, b64, R64 = (oracle_mod.decode(x, F16) for x in (p.A, p.B, p.bias, p.Y))
+    ok &= np.array_equal(rr.ref, np.maximum(A64 @ B64 + b64[None, :] + R64, 0.0))
     # rectangular non-symmetric matmul against numpy (catches transposed operands)
     p = gen.random_problem(7, 5, 9, BF16, F32, seed=60)
     zero = np.zeros(5, dtype=np.float32)
@@ -326,6 +369,6 @@ def test_pins_accept_the_oracle(oracle_mod):
 
 
 @pytest.mark.parametrize("name", ["relu_first", "bias_row", "bias_in_sum", "drop_gemm",
-                                  "transpose_b", "drop_last_k", "gate_sign"])
+                                  "transpose_b", "drop_last_k", "gate_sign", "resid_after"])
 def test_pins_reject_each_planted_mistake(oracle_mod, name):
     assert not _pins_pass(oracle_mod, oracle_mod.MUTANTS[name])
