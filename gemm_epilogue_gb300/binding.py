@@ -24,6 +24,9 @@ OUT_SAME, OUT_F32 = 0x000, 0x100
 OK, ERR_INVALID_VALUE, ERR_UNSUPPORTED_DTYPE, ERR_MISALIGNED = 0, 1, 2, 3
 ERR_NO_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSPACE = 4, 5, 6, 7
 
+# epilogue codes (fgemm_plan)
+EPI_RELU, EPI_GATE, EPI_RESIDUAL_RELU = 0, 1, 2
+
 # paths
 PATH_AUTO, PATH_TC, PATH_SKINNY, PATH_GENERIC, PATH_KZERO, PATH_NONE = 0, 1, 2, 3, 4, 5
 PATH_NAMES = {PATH_TC: "tc", PATH_SKINNY: "skinny", PATH_GENERIC: "generic",
@@ -58,6 +61,9 @@ _vp, _i64, _int, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_s
 _SIGS = {
     "fgemm_bias_relu": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "fgemm_addmm_gate": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
+    "fgemm_bias_residual_relu": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
+    "fgemm_bias_residual_relu_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp,
+                                           ctypes.POINTER(Opts), ctypes.POINTER(_int)]),
     "fgemm_bias_relu_ex": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp,
                                   ctypes.POINTER(Opts), ctypes.POINTER(_int)]),
     "fgemm_addmm_gate_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp,
@@ -142,6 +148,21 @@ def fgemm_addmm_gate(A, B, bias, Y, out, M, N, K, dtype, stream=None) -> None:
                                   dtype, _stream(stream)), "fgemm_addmm_gate")
 
 
+def fgemm_bias_residual_relu(A, B, bias, R, out, M, N, K, dtype, stream=None) -> None:
+    _check(lib().fgemm_bias_residual_relu(_ptr(A), _ptr(B), _ptr(bias), _ptr(R), _ptr(out), M, N,
+                                          K, dtype, _stream(stream)), "fgemm_bias_residual_relu")
+
+
+def fgemm_bias_residual_relu_ex(A, B, bias, R, out, M, N, K, dtype, stream=None, opts=None) -> int:
+    taken = ctypes.c_int(-1)
+    o = _opts(opts)
+    _check(lib().fgemm_bias_residual_relu_ex(_ptr(A), _ptr(B), _ptr(bias), _ptr(R), _ptr(out), M, N,
+                                             K, dtype, _stream(stream),
+                                             ctypes.byref(o) if o else None, ctypes.byref(taken)),
+           "fgemm_bias_residual_relu_ex")
+    return taken.value
+
+
 def fgemm_bias_relu_ex(A, B, bias, out, M, N, K, dtype, stream=None, opts=None) -> int:
     """Returns the path that ran (PATH_*)."""
     taken = ctypes.c_int(-1)
@@ -200,12 +221,13 @@ def fgemm_device_status(stream=None) -> int:
     return code.value
 
 
-def fgemm_plan(A, B, bias, Y, out, M, N, K, dtype, gate=False, opts=None) -> dict:
-    """Launch plan of a fused call (nothing is launched)."""
+def fgemm_plan(A, B, bias, Y, out, M, N, K, dtype, gate=False, opts=None, epilogue=None) -> dict:
+    """Launch plan of a fused call (nothing is launched).  epilogue: EPI_* (default: gate or relu)."""
     info = PlanInfo()
     o = _opts(opts)
+    epi = epilogue if epilogue is not None else (EPI_GATE if gate else EPI_RELU)
     _check(lib().fgemm_plan(_ptr(A), _ptr(B), _ptr(bias), _ptr(Y), _ptr(out), M, N, K, dtype,
-                            int(bool(gate)), ctypes.byref(o) if o else None, ctypes.byref(info)),
+                            epi, ctypes.byref(o) if o else None, ctypes.byref(info)),
            "fgemm_plan")
     return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if name != "reserved"}
 

@@ -143,7 +143,8 @@ int validate(const Call& c, bool* nothing) {
     *nothing = true;
     return FGEMM_OK;
   }
-  if (!c.out || (c.epi != EPI_NONE && !c.bias) || (c.epi == EPI_GATE && !c.Y))
+  if (!c.out || (c.epi != EPI_NONE && !c.bias) ||
+      ((c.epi == EPI_GATE || c.epi == EPI_RESID) && !c.Y))
     return FGEMM_ERR_INVALID_VALUE;
   if (c.K > 0 && (!c.A || !c.B)) return FGEMM_ERR_INVALID_VALUE;
   const size_t eab = elem_bytes(c.t.ab);
@@ -265,7 +266,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
       !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
       !encode_2d(&tmO, c.t.out, c.out, c.M, c.N, 32, out_box_cols))
     return FGEMM_ERR_LAUNCH;
-  if (c.epi == EPI_GATE && c.t.out != ELEM_F32) {
+  if ((c.epi == EPI_GATE || c.epi == EPI_RESID) && c.t.out != ELEM_F32) {
     if (!encode_2d(&tmY, c.t.ab, c.Y, c.M, c.N, 32, 64)) return FGEMM_ERR_LAUNCH;
   } else {
     tmY = tmO;  // unused
@@ -418,6 +419,20 @@ int fgemm_addmm_gate_ex(const void* A, const void* B, const void* bias, const vo
   return fused(c, path_taken);
 }
 
+int fgemm_bias_residual_relu_ex(const void* A, const void* B, const void* bias, const void* R,
+                                void* out, int64_t M, int64_t N, int64_t K, int dtype,
+                                void* stream, const fgemm_opts* opts, int* path_taken) {
+  Call c{A, B, bias, R, out, M, N, K, {}, EPI_RESID, static_cast<cudaStream_t>(stream), opts};
+  const int st = parse_dtype(dtype, &c.t);
+  if (st != FGEMM_OK) return st;
+  return fused(c, path_taken);
+}
+
+int fgemm_bias_residual_relu(const void* A, const void* B, const void* bias, const void* R,
+                             void* out, int64_t M, int64_t N, int64_t K, int dtype, void* stream) {
+  return fgemm_bias_residual_relu_ex(A, B, bias, R, out, M, N, K, dtype, stream, nullptr, nullptr);
+}
+
 int fgemm_bias_relu(const void* A, const void* B, const void* bias, void* out, int64_t M,
                     int64_t N, int64_t K, int dtype, void* stream) {
   return fgemm_bias_relu_ex(A, B, bias, out, M, N, K, dtype, stream, nullptr, nullptr);
@@ -520,13 +535,16 @@ const char* fgemm_status_string(int s) {
 }
 
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
-               int64_t M, int64_t N, int64_t K, int dtype, int gate, const fgemm_opts* opts,
+               int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
                fgemm_plan_info* info) {
   if (!info) return FGEMM_ERR_INVALID_VALUE;
   *info = fgemm_plan_info{};
   info->path = FGEMM_PATH_NONE;
-  Call c{A, B, bias, gate ? Y : nullptr, const_cast<void*>(out), M, N, K, {},
-         gate ? EPI_GATE : EPI_RELU, nullptr, opts};
+  if (epilogue < FGEMM_EPI_RELU || epilogue > FGEMM_EPI_RESIDUAL_RELU) return FGEMM_ERR_INVALID_VALUE;
+  const int epi = epilogue == FGEMM_EPI_GATE ? EPI_GATE
+                : epilogue == FGEMM_EPI_RESIDUAL_RELU ? EPI_RESID : EPI_RELU;
+  Call c{A, B, bias, epi == EPI_RELU ? nullptr : Y, const_cast<void*>(out), M, N, K, {}, epi,
+         nullptr, opts};
   int st = parse_dtype(dtype, &c.t);
   if (st != FGEMM_OK) return st;
   bool nothing = false;

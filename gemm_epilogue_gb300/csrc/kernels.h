@@ -6,7 +6,8 @@
 
 namespace fgemm {
 
-enum Epi : int { EPI_RELU = 0, EPI_GATE = 1, EPI_NONE = 2 };
+// EPI_RESID: out = ReLU(acc + bias + R) with R (M x N, operand type) passed where the gate's Y is.
+enum Epi : int { EPI_RELU = 0, EPI_GATE = 1, EPI_NONE = 2, EPI_RESID = 3 };
 enum Elem : int { ELEM_F16 = 0, ELEM_BF16 = 1, ELEM_F32 = 2 };
 
 inline int elem_bytes(int e) { return e == ELEM_F32 ? 4 : 2; }

@@ -27,6 +27,7 @@ __device__ __forceinline__ float epilogue(float acc, float bias, float y) {
   if constexpr (EPI == EPI_NONE) return acc;
   const float x = acc + bias;
   if constexpr (EPI == EPI_RELU) return fmaxf(x, 0.0f);
+  if constexpr (EPI == EPI_RESID) return fmaxf(x + y, 0.0f);  // residual before the activation
   return fmaf(x, y, x);  // X + X * Y
 }
 
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(gen::THREADS) generic_kernel(const SimtParams 
       const int gm = m0 + ty * 4 + i;
       if (gm >= p.M) continue;
       const int64_t idx = static_cast<int64_t>(gm) * p.N + gn;
-      const float y = (EPI == EPI_GATE) ? ld_elem(p.Y, idx, p.ab_type) : 0.f;
+      const float y = (EPI == EPI_GATE || EPI == EPI_RESID) ? ld_elem(p.Y, idx, p.ab_type) : 0.f;
       st_elem(p.out, idx, p.out_type, epilogue<EPI>(acc[i][j], bj, y));
     }
   }
@@ -107,6 +108,7 @@ cudaError_t launch_generic(int epi, const SimtParams& p, cudaStream_t s) {
   switch (epi) {
     case EPI_RELU: generic_kernel<EPI_RELU><<<grid, gen::THREADS, 0, s>>>(p); break;
     case EPI_GATE: generic_kernel<EPI_GATE><<<grid, gen::THREADS, 0, s>>>(p); break;
+    case EPI_RESID: generic_kernel<EPI_RESID><<<grid, gen::THREADS, 0, s>>>(p); break;
     default: generic_kernel<EPI_NONE><<<grid, gen::THREADS, 0, s>>>(p); break;
   }
   return cudaGetLastError();
@@ -157,7 +159,8 @@ __device__ __forceinline__ void st8(void* p, int64_t i, int type, const Vec8& x)
   }
 }
 
-enum EwOp { EW_BIAS_INPLACE = 0, EW_RELU = 1, EW_BIAS_GATE = 2, EW_KZERO_RELU = 3, EW_KZERO_GATE = 4 };
+enum EwOp { EW_BIAS_INPLACE = 0, EW_RELU = 1, EW_BIAS_GATE = 2, EW_KZERO_RELU = 3, EW_KZERO_GATE = 4,
+            EW_KZERO_RESID = 5 };
 
 struct EwParams {
   const void* src;   // I (the intermediate) or NULL for K = 0
@@ -180,6 +183,7 @@ __device__ __forceinline__ float ew_apply(float s, float b, float y) {
     return fmaf(x, y, x);
   }
   if constexpr (OP == EW_KZERO_RELU) return fmaxf(0.0f + b, 0.0f);
+  if constexpr (OP == EW_KZERO_RESID) return fmaxf((0.0f + b) + y, 0.0f);
   const float x = 0.0f + b;  // EW_KZERO_GATE
   return fmaf(x, y, x);
 }
@@ -188,7 +192,7 @@ template <int OP, bool VEC>
 __global__ void __launch_bounds__(256) ew_kernel(const EwParams p) {
   constexpr bool uses_src = (OP == EW_BIAS_INPLACE || OP == EW_RELU || OP == EW_BIAS_GATE);
   constexpr bool uses_bias = (OP != EW_RELU);
-  constexpr bool uses_y = (OP == EW_BIAS_GATE || OP == EW_KZERO_GATE);
+  constexpr bool uses_y = (OP == EW_BIAS_GATE || OP == EW_KZERO_GATE || OP == EW_KZERO_RESID);
   const int64_t total = static_cast<int64_t>(p.M) * p.N;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   if constexpr (VEC) {
@@ -235,6 +239,7 @@ static cudaError_t launch_ew(const EwParams& p, int num_sms, cudaStream_t s) {
 cudaError_t launch_kzero(int epi, const SimtParams& sp, int num_sms, cudaStream_t s) {
   EwParams p{nullptr, 0, sp.bias, sp.bias_type, sp.Y, sp.ab_type, sp.out, sp.out_type, sp.M, sp.N};
   if (epi == EPI_GATE) return launch_ew<EW_KZERO_GATE>(p, num_sms, s);
+  if (epi == EPI_RESID) return launch_ew<EW_KZERO_RESID>(p, num_sms, s);
   return launch_ew<EW_KZERO_RELU>(p, num_sms, s);
 }
 

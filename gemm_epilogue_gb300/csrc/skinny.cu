@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float v = s4[e] + b;
         if constexpr (EPI == EPI_RELU) v = fmaxf(v, 0.0f);
         if constexpr (EPI == EPI_GATE) v = fmaf(v, ld_any(p.Y, o, p.ab_type), v);
+        if constexpr (EPI == EPI_RESID) v = fmaxf(v + ld_any(p.Y, o, p.ab_type), 0.0f);
         st_any(p.out, o, p.out_type, v);
       }
     }
@@ -353,6 +354,7 @@ cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tm
   switch (epi) {
     case EPI_RELU: return sk::launch_one<EPI_RELU>(tmB, tmA, p, ctas, s);
     case EPI_GATE: return sk::launch_one<EPI_GATE>(tmB, tmA, p, ctas, s);
+    case EPI_RESID: return sk::launch_one<EPI_RESID>(tmB, tmA, p, ctas, s);
     default: return sk::launch_one<EPI_NONE>(tmB, tmA, p, ctas, s);
   }
 }

@@ -20,9 +20,11 @@
 //               buffer -> one TMA store, which clips rows >= M and columns >= N (the store mask).
 //               The bias is read only here, after the reduction ("Triton: Fused Matmul + Bias +
 //               ReLU (Epilogue Fusion)", "Pitfalls": load the bias after the K loop; mask it with
-//               j < N).  The gate's Y chunk is loaded straight into registers ahead of the TMEM
-//               read ("Optimizing GEMM + Activation on CDNA4 with TLX", "Version 4": Y prefetched
-//               into registers, not staged through shared memory) with a streaming hint.
+//               j < N).  For the gate (and the residual add, "Triton: Fused Matmul + Bias +
+//               ReLU (Epilogue Fusion)", "Variants") the second M x N operand is prefetched by TMA
+//               into the epilogue's own buffers while the next tile's main loop runs, and the
+//               result is written over it and stored from there; with fp32 outputs it is loaded
+//               straight into registers ahead of the TMEM read.
 // The accumulator goes from TMEM to registers to the single store; it never touches HBM.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -144,7 +146,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int CH = 128 / OUT_BYTES;  // output columns per 128-byte staging row
   constexpr int G = 16 / OUT_BYTES;    // columns per 16-byte granule
   constexpr int NG = CH / G;           // granules per chunk (8)
-  constexpr bool YS = (EPI == EPI_GATE) && (OUT_BYTES == 2);
+  // the gate's Y and the residual R are staged the same way (16-bit outputs)
+  constexpr bool YS = (EPI == EPI_GATE || EPI == EPI_RESID) && (OUT_BYTES == 2);
   using C = Cfg<PAIR, YS>;
   constexpr int STAGES = C::STAGES;
   constexpr int CG = PAIR ? 2 : 1;
@@ -384,8 +387,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               const float2 y2 = unpack2(y[e], y_bf);
               float x0 = __uint_as_float(acc[g * G + 2 * e]) + bv[2 * e];  // bias once
               float x1 = __uint_as_float(acc[g * G + 2 * e + 1]) + bv[2 * e + 1];
-              x0 = fmaf(x0, y2.x, x0);  // X + X * Y
-              x1 = fmaf(x1, y2.y, x1);
+              if constexpr (EPI == EPI_GATE) {
+                x0 = fmaf(x0, y2.x, x0);  // X + X * Y
+                x1 = fmaf(x1, y2.y, x1);
+              } else {                    // residual before the activation
+                x0 = fmaxf(x0 + y2.x, 0.0f);
+                x1 = fmaxf(x1 + y2.y, 0.0f);
+              }
               packed[e] = pack2(x0, x1, out_bf);
             }
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[0]),
@@ -434,8 +442,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
 
         // Gate: this thread's row of Y for the chunk, loaded before the TMEM read.
-        uint4 yv[EPI == EPI_GATE ? NG * G / 8 : 1];
-        if constexpr (EPI == EPI_GATE) {
+        constexpr bool HAS_Y = EPI == EPI_GATE || EPI == EPI_RESID;
+        uint4 yv[HAS_Y ? NG * G / 8 : 1];
+        if constexpr (HAS_Y) {
           const uint16_t* yrow = static_cast<const uint16_t*>(p.Y) + static_cast<int64_t>(row) * p.N;
 #pragma unroll
           for (int v = 0; v < NG * G / 8; ++v) {
@@ -478,16 +487,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int e = 0; e < G; ++e) v[e] = fmaxf(v[e], 0.0f);  // branchless clamp
           }
-          if constexpr (EPI == EPI_GATE) {
-            // 16-bit Y: granule g covers columns g*G .. g*G+G-1 of the chunk
+          if constexpr (HAS_Y) {
+            // 16-bit Y (or R): granule g covers columns g*G .. g*G+G-1 of the chunk
 #pragma unroll
             for (int e = 0; e < G; e += 2) {
               const int idx = g * G + e;  // column within the chunk
               const uint4 u = yv[idx / 8];
               const uint32_t w = (idx % 8 < 2) ? u.x : (idx % 8 < 4) ? u.y : (idx % 8 < 6) ? u.z : u.w;
               const float2 y2 = unpack2(w, y_bf);
-              v[e] = fmaf(v[e], y2.x, v[e]);          // X + X * Y
-              v[e + 1] = fmaf(v[e + 1], y2.y, v[e + 1]);
+              if constexpr (EPI == EPI_GATE) {
+                v[e] = fmaf(v[e], y2.x, v[e]);          // X + X * Y
+                v[e + 1] = fmaf(v[e + 1], y2.y, v[e + 1]);
+              } else {                                  // residual before the activation
+                v[e] = fmaxf(v[e] + y2.x, 0.0f);
+                v[e + 1] = fmaxf(v[e + 1] + y2.y, 0.0f);
+              }
             }
           }
           uint4 packed;
@@ -546,7 +560,8 @@ template <int EPI, int OUT_BYTES, bool PAIR>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                        const CUtensorMap& y, const TcParams& p, int grid, cudaStream_t s) {
   auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR>;
-  constexpr uint32_t smem = Cfg<PAIR, EPI == EPI_GATE && OUT_BYTES == 2>::SMEM_BYTES;
+  constexpr uint32_t smem =
+      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2>::SMEM_BYTES;
   static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -580,7 +595,8 @@ int max_pairs() {
   int& cached = cached_dev[dev];
   if (cached == 0) {
     auto k = tc_gemm_kernel<EPI, OUT_BYTES, true>;
-    constexpr uint32_t smem = Cfg<true, EPI == EPI_GATE && OUT_BYTES == 2>::SMEM_BYTES;
+    constexpr uint32_t smem =
+        Cfg<true, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2>::SMEM_BYTES;
     int n = 0;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
       cudaLaunchConfig_t cfg{};
@@ -617,6 +633,7 @@ int tc_max_active_pairs(int epi, int out_type) {
   switch (epi) {
     case EPI_RELU: return f32 ? tc::max_pairs<EPI_RELU, 4>() : tc::max_pairs<EPI_RELU, 2>();
     case EPI_GATE: return f32 ? tc::max_pairs<EPI_GATE, 4>() : tc::max_pairs<EPI_GATE, 2>();
+    case EPI_RESID: return f32 ? tc::max_pairs<EPI_RESID, 4>() : tc::max_pairs<EPI_RESID, 2>();
     default: return f32 ? tc::max_pairs<EPI_NONE, 4>() : tc::max_pairs<EPI_NONE, 2>();
   }
 }
@@ -633,6 +650,8 @@ cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const
                               : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, y, p, grid, pair, s);
     case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4>(a, b, o, y, p, grid, pair, s)
                               : tc::launch_pair_or_not<EPI_GATE, 2>(a, b, o, y, p, grid, pair, s);
+    case EPI_RESID: return f32 ? tc::launch_pair_or_not<EPI_RESID, 4>(a, b, o, y, p, grid, pair, s)
+                               : tc::launch_pair_or_not<EPI_RESID, 2>(a, b, o, y, p, grid, pair, s);
     default: return f32 ? tc::launch_pair_or_not<EPI_NONE, 4>(a, b, o, y, p, grid, pair, s)
                         : tc::launch_pair_or_not<EPI_NONE, 2>(a, b, o, y, p, grid, pair, s);
   }

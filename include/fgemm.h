@@ -1,7 +1,7 @@
 /*
  * fgemm.h -- C ABI of the fused GEMM + epilogue library for NVIDIA GB300 (sm_103a).
  *
- * Two fused operations, each one kernel launch in which the fp32 accumulator never leaves the chip
+ * Fused operations, each one kernel launch in which the fp32 accumulator never leaves the chip
  * (tensor memory) between the end of the K reduction and the single store:
  *
  *   fgemm_bias_relu   out[i,j] = max(0, sum_k A[i,k] B[k,j] + bias[j])
@@ -65,6 +65,11 @@ typedef enum {
 #define FGEMM_OUT_SAME 0x000 /* out has the operand type */
 #define FGEMM_OUT_F32 0x100  /* out is fp32 */
 
+/* Epilogue codes (fgemm_plan). */
+#define FGEMM_EPI_RELU 0          /* fgemm_bias_relu */
+#define FGEMM_EPI_GATE 1          /* fgemm_addmm_gate */
+#define FGEMM_EPI_RESIDUAL_RELU 2 /* fgemm_bias_residual_relu */
+
 /* Kernel paths (fgemm_opts.path, and *path_taken of the _ex entries). */
 #define FGEMM_PATH_AUTO 0    /* library choice */
 #define FGEMM_PATH_TC 1      /* persistent TMA + tcgen05 kernel, grouped-M tile order */
@@ -107,6 +112,14 @@ int fgemm_bias_relu(const void* A, const void* B, const void* bias, void* out, i
 int fgemm_addmm_gate(const void* A, const void* B, const void* bias, const void* Y, void* out,
                      int64_t M, int64_t N, int64_t K, int dtype, void* stream);
 
+/*
+ * out = ReLU(A @ B + bias + R), R: M x N of the operand type, added after the K loop and before
+ * the activation ("Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "Variants": matmul +
+ * residual add).  Same conventions as fgemm_bias_relu.  Returns an fgemm_status.
+ */
+int fgemm_bias_residual_relu(const void* A, const void* B, const void* bias, const void* R,
+                             void* out, int64_t M, int64_t N, int64_t K, int dtype, void* stream);
+
 /* As above, with options (may be NULL) and the path that ran (may be NULL). */
 int fgemm_bias_relu_ex(const void* A, const void* B, const void* bias, void* out, int64_t M,
                        int64_t N, int64_t K, int dtype, void* stream, const fgemm_opts* opts,
@@ -114,6 +127,9 @@ int fgemm_bias_relu_ex(const void* A, const void* B, const void* bias, void* out
 int fgemm_addmm_gate_ex(const void* A, const void* B, const void* bias, const void* Y, void* out,
                         int64_t M, int64_t N, int64_t K, int dtype, void* stream,
                         const fgemm_opts* opts, int* path_taken);
+int fgemm_bias_residual_relu_ex(const void* A, const void* B, const void* bias, const void* R,
+                                void* out, int64_t M, int64_t N, int64_t K, int dtype,
+                                void* stream, const fgemm_opts* opts, int* path_taken);
 
 /*
  * Unfused comparison chain (for measuring the traffic that fusion removes; not a fast path).
@@ -173,8 +189,8 @@ const char* fgemm_status_string(int status);
 /*
  * Launch plan of a fused call, computed without launching anything: the path, grid and cluster
  * shape, the tile count and how the persistent grid's last round is cut.  Same arguments and
- * validation as fgemm_bias_relu_ex (gate = 0) or fgemm_addmm_gate_ex (gate = 1); the buffers are
- * inspected for alignment only.
+ * validation as the _ex entry of `epilogue` (FGEMM_EPI_*; Y is the gate's Y or the residual R);
+ * the buffers are inspected for alignment only.
  */
 typedef struct {
   int path;           /* FGEMM_PATH_* that would run */
@@ -188,7 +204,7 @@ typedef struct {
   int reserved;
 } fgemm_plan_info;
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
-               int64_t M, int64_t N, int64_t K, int dtype, int gate, const fgemm_opts* opts,
+               int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
                fgemm_plan_info* info);
 
 /*

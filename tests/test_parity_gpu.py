@@ -195,6 +195,49 @@ def test_skinny_matches_square_tile_path():
         check_close(down(x, F16), ref, K, F16, bias64=oracle.decode(p.bias, F16), what="skinny/tc")
 
 
+# ------------------------------------------------------------- residual add --
+
+RESID_CASES = [  # M, N, K, opts, expected path
+    (300, 520, 200, {"cta_pair": 2}, 1), (300, 520, 200, {"cta_pair": 1}, 1),
+    (777, 1288, 328, None, 1), (16, 1032, 512, None, 2), (100, 264, 72, {"split_k": 3}, 2),
+    (7, 9, 13, None, 3), (37, 70, 0, None, 4)]
+
+
+@pytest.mark.parametrize("M,N,K,opts,want_path", RESID_CASES)
+def test_residual_integer_bit_exact(M, N, K, opts, want_path):
+    # "Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "Variants": residual tile added after
+    # the K loop, before the activation; every path, 16-bit and fp32 outputs
+    for ab, ot in ((BF16, BF16), (F16, F32)):
+        p = gen.integer_problem(M, N, K, ab, ab, seed=M + N + K, gate=True)  # Y serves as R
+        A = up(p.A, ab) if K else None
+        B = up(p.B, ab) if K else None
+        bias, R = up(p.bias, ab), up(p.Y, ab)
+        out = torch.empty(M, N, dtype={F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}[ot],
+                          device="cuda")
+        path = fg.fgemm_bias_residual_relu_ex(A, B, bias, R, out, M, N, K, dtype_word(ab, ab, ot),
+                                              opts=opts)
+        torch.cuda.synchronize()
+        assert path == want_path
+        ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, ab, ab, ot)
+        assert np.array_equal(down(out, ot), ref.out)
+
+
+def test_residual_random_tolerance_and_guards():
+    M, N, K = 513, 776, 1024
+    p = gen.random_problem(M, N, K, BF16, BF16, seed=15, gate=True)
+    guard = 4096
+    buf = torch.full((guard + M * N + guard,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + M * N].view(M, N)
+    fg.fgemm_bias_residual_relu(up(p.A, BF16), up(p.B, BF16), up(p.bias, BF16), up(p.Y, BF16), out,
+                                M, N, K, fg.BF16)
+    torch.cuda.synchronize()
+    b = buf.cpu()
+    assert torch.isnan(b[:guard]).all() and torch.isnan(b[guard + M * N:]).all()
+    ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, BF16, BF16, BF16)
+    check_close(down(out, BF16), ref, K, BF16, bias64=oracle.decode(p.bias, BF16) + 0.0,
+                Y64=None, what="residual")
+
+
 # ----------------------------------------------------------- float tolerance --
 
 def test_small_ragged_workload_tc_and_generic():
