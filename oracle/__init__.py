@@ -10,8 +10,9 @@ rows); this module compiles it with gcc and marshals numpy arrays through
 ctypes.  ``schedule.py`` holds the grouped tile ordering written from the page
 "I3. Fuse a GEMM epilogue and change tile scheduling".
 
-Element types are passed as codes: F16 = 1, BF16 = 2, F32 = 3.  16-bit inputs
-are numpy ``uint16`` arrays holding the raw bit patterns; F32 is ``float32``.
+Element types are passed as codes: F16 = 1, BF16 = 2, F32 = 3, E4M3 = 4.  16-bit
+values are numpy ``uint16`` arrays holding the raw bit patterns, fp8 e4m3 values
+``uint8`` bit patterns; F32 is ``float32``.
 """
 from __future__ import annotations
 
@@ -22,18 +23,20 @@ import threading
 
 import numpy as np
 
-F16, BF16, F32 = 1, 2, 3
-EPI_RELU, EPI_GATE, EPI_LINEAR, EPI_RESIDUAL = 0, 1, 2, 3
+F16, BF16, F32, E4M3 = 1, 2, 3, 4
+EPI_RELU, EPI_GATE, EPI_LINEAR, EPI_RESIDUAL, EPI_QUANT = 0, 1, 2, 3, 4
 
 # Negative controls: deliberate mistakes the oracle can be asked to make, so
 # that the tests can show each pin rejects a plausible slip.  OK = the oracle.
 OK = 0
 MUT_RELU_FIRST, MUT_BIAS_ROW, MUT_BIAS_IN_SUM, MUT_DROP_GEMM = 1, 2, 3, 4
 MUT_TRANSPOSE_B, MUT_DROP_LAST_K, MUT_GATE_SIGN, MUT_RESID_AFTER = 5, 6, 7, 8
+MUT_SCALE_FIRST = 9
 MUTANTS = {"relu_first": MUT_RELU_FIRST, "bias_row": MUT_BIAS_ROW,
            "bias_in_sum": MUT_BIAS_IN_SUM, "drop_gemm": MUT_DROP_GEMM,
            "transpose_b": MUT_TRANSPOSE_B, "drop_last_k": MUT_DROP_LAST_K,
-           "gate_sign": MUT_GATE_SIGN, "resid_after": MUT_RESID_AFTER}
+           "gate_sign": MUT_GATE_SIGN, "resid_after": MUT_RESID_AFTER,
+           "scale_first": MUT_SCALE_FIRST}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -64,7 +67,7 @@ def _load():
             lib.orc_gemm_epilogue.argtypes = (
                 [ctypes.c_void_p] * 7
                 + [ctypes.c_int64] * 3 + [ctypes.c_void_p, ctypes.c_int64]
-                + [ctypes.c_int] * 6)
+                + [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int])
             lib.orc_encode.restype = None
             lib.orc_encode.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
             lib.orc_decode.restype = None
@@ -81,11 +84,15 @@ def _ptr(a):
     return None if a is None else a.ctypes.data
 
 
+def _storage(t):
+    return {F32: np.float32, E4M3: np.uint8}.get(t, np.uint16)
+
+
 def _bits(a, t):
     if a is None:
         return None
     a = np.ascontiguousarray(a)
-    want = np.float32 if t == F32 else np.uint16
+    want = _storage(t)
     if a.dtype != want:
         raise TypeError(f"oracle expects {np.dtype(want)} storage for type code {t}, got {a.dtype}")
     return a
@@ -94,7 +101,7 @@ def _bits(a, t):
 def encode(x, t: int) -> np.ndarray:
     """Round fp64 values to type ``t`` (RNE), returning raw bits (uint16) or float32."""
     x = np.ascontiguousarray(x, dtype=np.float64)
-    out = np.empty(x.shape, dtype=np.float32 if t == F32 else np.uint16)
+    out = np.empty(x.shape, dtype=_storage(t))
     _load().orc_encode(_ptr(x), _ptr(out), x.size, t)
     return out
 
@@ -119,7 +126,7 @@ class Result:
 
 def gemm_epilogue(A, B, bias, M: int, N: int, K: int, ab_type: int, bias_type: int,
                   out_type: int, epi: int, Y=None, rows=None, threads: int | None = None,
-                  want_ref: bool = True, mutant: int = OK) -> Result:
+                  want_ref: bool = True, mutant: int = OK, scale: float = 1.0) -> Result:
     """Run the oracle on all rows, or on the listed ``rows`` of the M x N output."""
     A = _bits(A, ab_type) if K > 0 else (None if A is None else _bits(A, ab_type))
     B = _bits(B, ab_type) if K > 0 else (None if B is None else _bits(B, ab_type))
@@ -133,14 +140,14 @@ def gemm_epilogue(A, B, bias, M: int, N: int, K: int, ab_type: int, bias_type: i
         if rows_arr.size and (rows_arr.min() < 0 or rows_arr.max() >= M):
             raise IndexError("row index out of range")
         nrows = rows_arr.size
-    out = np.empty((nrows, N), dtype=np.float32 if out_type == F32 else np.uint16)
+    out = np.empty((nrows, N), dtype=_storage(out_type))
     ref = np.empty((nrows, N), dtype=np.float64) if want_ref else None
     absdot = np.empty((nrows, N), dtype=np.float64) if want_ref else None
     th = threads or default_threads()
     used = _load().orc_gemm_epilogue(
         _ptr(A), _ptr(B), _ptr(bias), _ptr(Y if epi in (EPI_GATE, EPI_RESIDUAL) else None),
         _ptr(out), _ptr(ref), _ptr(absdot), M, N, K, _ptr(rows_arr), nrows,
-        ab_type, bias_type, out_type, epi, mutant, th)
+        ab_type, bias_type, out_type, epi, mutant, float(scale), th)
     if used < 0:
         raise ValueError("oracle rejected its arguments")
     return Result(out, ref, absdot, used)
@@ -159,6 +166,11 @@ def addmm_gate(A, B, bias, Y, M, N, K, ab_type, bias_type, out_type, **kw) -> Re
 def bias_residual_relu(A, B, bias, R, M, N, K, ab_type, bias_type, out_type, **kw) -> Result:
     """out = RNE(max(0, A @ B + bias + R)) -- the residual added before the activation."""
     return gemm_epilogue(A, B, bias, M, N, K, ab_type, bias_type, out_type, EPI_RESIDUAL, Y=R, **kw)
+
+
+def bias_relu_quant(A, B, bias, M, N, K, ab_type, bias_type, scale, **kw) -> Result:
+    """out = e4m3(clamp(scale * max(0, A @ B + bias), -448, 448)), fp8 output (uint8 bits)."""
+    return gemm_epilogue(A, B, bias, M, N, K, ab_type, bias_type, E4M3, EPI_QUANT, scale=scale, **kw)
 
 
 def linear(A, B, bias, M, N, K, ab_type, bias_type, out_type, **kw) -> Result:

@@ -27,6 +27,12 @@
  *       The bias is added first, then R (fp64, so the order only matters at the last bit of a
  *       sum that is rounded once anyway).
  *
+ *   quantized  out[i,j] = RNE_e4m3( clamp(scale * max(0, s[i,j] + bias[j]), -448, 448) )
+ *       "Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "Variants": matmul + quantized
+ *       output -- a scale and a clamp applied to the (biased, activated) accumulator, then the
+ *       cast to fp8 before the store.  e4m3 ("fn": no infinities, largest finite 448) is
+ *       written here from its definition: 1 sign, 4 exponent (bias 7) and 3 fraction bits.
+ *
  *   linear  out[i,j] = RNE( s[i,j] + bias[j] )  (no activation; used only to
  *       pin the reduction against a library matmul and to check the unfused
  *       chain's intermediate).
@@ -59,8 +65,9 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F16 = 1, ORC_BF16 = 2, ORC_F32 = 3 };
-enum { ORC_EPI_RELU = 0, ORC_EPI_GATE = 1, ORC_EPI_LINEAR = 2, ORC_EPI_RESIDUAL = 3 };
+enum { ORC_F16 = 1, ORC_BF16 = 2, ORC_F32 = 3, ORC_E4M3 = 4 };
+enum { ORC_EPI_RELU = 0, ORC_EPI_GATE = 1, ORC_EPI_LINEAR = 2, ORC_EPI_RESIDUAL = 3,
+       ORC_EPI_QUANT = 4 };
 
 /*
  * Deliberate mistakes, selectable only to show that the tests' pins catch
@@ -74,10 +81,11 @@ enum { ORC_EPI_RELU = 0, ORC_EPI_GATE = 1, ORC_EPI_LINEAR = 2, ORC_EPI_RESIDUAL 
  *   DROP_LAST_K   the last k term left out
  *   GATE_SIGN     X - X*Y instead of X + X*Y
  *   RESID_AFTER   ReLU(AB + bias) + R: the residual added after the activation
+ *   SCALE_FIRST   quantized output with the scale applied before the bias: ReLU(scale*AB + bias)
  */
 enum { ORC_OK = 0, ORC_MUT_RELU_FIRST = 1, ORC_MUT_BIAS_ROW = 2, ORC_MUT_BIAS_IN_SUM = 3,
        ORC_MUT_DROP_GEMM = 4, ORC_MUT_TRANSPOSE_B = 5, ORC_MUT_DROP_LAST_K = 6,
-       ORC_MUT_GATE_SIGN = 7, ORC_MUT_RESID_AFTER = 8 };
+       ORC_MUT_GATE_SIGN = 7, ORC_MUT_RESID_AFTER = 8, ORC_MUT_SCALE_FIRST = 9 };
 
 /* ---- decoding (definitions of the formats) ---------------------------- */
 
@@ -113,11 +121,28 @@ static double decode_bf16(uint16_t h)
     return sign ? -v : v;
 }
 
+/* fp8 e4m3 ("fn"): 1 sign, 4 exponent (bias 7), 3 fraction bits; S.1111.111 is NaN, no inf. */
+static double decode_e4m3(uint8_t h)
+{
+    int sign = (h >> 7) & 1;
+    int expo = (h >> 3) & 0xf;
+    int frac = h & 0x7;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -9);                  /* subnormal / zero */
+    else if (expo == 15 && frac == 7)
+        v = NAN;
+    else
+        v = ldexp((double)(8 + frac), expo - 10);     /* (1.f) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
 static double decode(const void *p, int64_t idx, int type)
 {
     switch (type) {
     case ORC_F16: return decode_f16(((const uint16_t *)p)[idx]);
     case ORC_BF16: return decode_bf16(((const uint16_t *)p)[idx]);
+    case ORC_E4M3: return decode_e4m3(((const uint8_t *)p)[idx]);
     default: return (double)((const float *)p)[idx];
     }
 }
@@ -182,11 +207,31 @@ static uint16_t encode_bf16(double x)
     return s | (uint16_t)(biased << 7) | frac;
 }
 
+/* RNE to e4m3; magnitudes that round beyond 448 saturate to 448 (satfinite). */
+static uint8_t encode_e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7f;
+    double r = round_to_format(x, 4, -6, 8);
+    uint8_t s = signbit(r) ? 0x80 : 0;
+    double a = fabs(r);
+    if (isinf(a) || a > 448.0)
+        return s | 0x7e;
+    if (a < ldexp(1.0, -6))                        /* subnormal or zero */
+        return s | (uint8_t)(a / ldexp(1.0, -9));
+    int e;
+    double f = frexp(a, &e);
+    uint8_t biased = (uint8_t)(e - 1 + 7);
+    uint8_t frac = (uint8_t)((f * 2.0 - 1.0) * 8.0);
+    return s | (uint8_t)(biased << 3) | frac;
+}
+
 static void store(void *p, int64_t idx, int type, double v)
 {
     switch (type) {
     case ORC_F16: ((uint16_t *)p)[idx] = encode_f16(v); break;
     case ORC_BF16: ((uint16_t *)p)[idx] = encode_bf16(v); break;
+    case ORC_E4M3: ((uint8_t *)p)[idx] = encode_e4m3(v); break;
     default: ((float *)p)[idx] = (float)v; break;   /* C conversion: RNE */
     }
 }
@@ -206,7 +251,7 @@ void orc_decode(const void *p, double *out, int64_t n, int type)
 
 /* ---- the epilogue ------------------------------------------------------ */
 
-static double epilogue(int epi, double s, double bias_j, double y, int mutant)
+static double epilogue(int epi, double s, double bias_j, double y, int mutant, double scale)
 {
     if (mutant == ORC_MUT_RELU_FIRST && epi == ORC_EPI_RELU)
         return ((s > 0.0) ? s : 0.0) + bias_j;
@@ -222,6 +267,17 @@ static double epilogue(int epi, double s, double bias_j, double y, int mutant)
             return ((v > 0.0) ? v : 0.0) + y;
         v = v + y;                                   /* + R[i,j] before the activation */
         return (v > 0.0) ? v : 0.0;
+    case ORC_EPI_QUANT:
+        if (mutant == ORC_MUT_SCALE_FIRST) {
+            v = scale * s + bias_j;
+            v = (v > 0.0) ? v : 0.0;
+        } else {
+            v = (v > 0.0) ? v : 0.0;                 /* activation */
+            v = scale * v;                           /* scale */
+        }
+        if (v > 448.0) v = 448.0;                    /* clamp to the fp8 range */
+        if (v < -448.0) v = -448.0;
+        return v;                                    /* the cast happens at the store */
     default: return v;                               /* linear */
     }
 }
@@ -237,6 +293,7 @@ typedef struct {
     const int64_t *rows;     /* row indices into A / Y, or NULL = 0..nrows-1 */
     int64_t N, K;
     int ab_type, bias_type, out_type, epi, mutant;
+    double scale;            /* quantized epilogue only */
     int64_t r_begin, r_end;  /* this worker's slice of the row list */
 } work_t;
 
@@ -270,7 +327,8 @@ static void *row_worker(void *arg)
             const double b = decode(w->bias, (mut == ORC_MUT_BIAS_ROW) ? i % N : j, w->bias_type);
             const double y = (w->epi == ORC_EPI_GATE || w->epi == ORC_EPI_RESIDUAL)
                                  ? decode(w->Y, i * N + j, w->ab_type) : 0.0;
-            const double v = epilogue(w->epi, (mut == ORC_MUT_BIAS_IN_SUM) ? s[j] - b : s[j], b, y, mut);
+            const double v = epilogue(w->epi, (mut == ORC_MUT_BIAS_IN_SUM) ? s[j] - b : s[j], b, y,
+                                      mut, w->scale);
             store(w->out, r * N + j, w->out_type, v);
             if (w->ref)
                 w->ref[r * N + j] = v;
@@ -294,13 +352,14 @@ static void *row_worker(void *arg)
  *   ref    nrows x N fp64: the value before the final rounding (may be NULL)
  *   absdot nrows x N fp64: sum_k |A[i,k] B[k,j]| (may be NULL)
  *   mutant ORC_OK for the oracle; any other value selects a negative control
+ *   scale  the quantized epilogue's scale (ignored otherwise)
  * Returns the number of threads used, or -1 on a bad argument.
  */
 int orc_gemm_epilogue(const void *A, const void *B, const void *bias, const void *Y,
                       void *out, double *ref, double *absdot,
                       int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
                       int ab_type, int bias_type, int out_type, int epi, int mutant,
-                      int nthreads)
+                      double scale, int nthreads)
 {
     if (M < 0 || N < 0 || K < 0 || nrows < 0 || nthreads < 1)
         return -1;
@@ -318,7 +377,7 @@ int orc_gemm_epilogue(const void *A, const void *B, const void *bias, const void
     work_t *w = (work_t *)malloc(sizeof(work_t) * (size_t)nthreads);
     for (int t = 0; t < nthreads; ++t) {
         w[t] = (work_t){A, bias, Y, Bd, out, ref, absdot, rows, N, K,
-                        ab_type, bias_type, out_type, epi, mutant,
+                        ab_type, bias_type, out_type, epi, mutant, scale,
                         nrows * t / nthreads, nrows * (t + 1) / nthreads};
         pthread_create(&th[t], NULL, row_worker, &w[t]);
     }

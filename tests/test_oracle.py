@@ -325,6 +325,68 @@ def test_residual_brute_force_and_library_chain(oracle_mod, M, N, K):
         assert Fraction(r.ref[i, j]) == e
 
 
+# ------------------------------------------------------- quantized fp8 output --
+
+E4M3 = 4
+
+
+def test_decode_e4m3_every_pattern(oracle_mod):
+    pats = np.arange(256, dtype=np.uint16).astype(np.uint8)
+    got = oracle_mod.decode(pats, E4M3)
+    want = torch.from_numpy(pats.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+
+
+def test_encode_e4m3_matches_torch_in_range(oracle_mod):
+    rng = np.random.default_rng(12)
+    x = rng.uniform(-448, 448, 20000) * np.exp2(rng.integers(-14, 1, 20000))
+    ties = [(m + 0.5) * 2.0 ** -9 for m in range(8)] + [(8 + m + 0.5) * 2.0 ** (e - 10)
+                                                     for e in range(1, 16) for m in range(7)]
+    x = np.concatenate([x, ties, -np.array(ties)]).astype(np.float32).astype(np.float64)
+    x = x[np.abs(x) <= 448]
+    got = oracle_mod.encode(x, E4M3)
+    want = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
+
+
+def test_encode_e4m3_hand_cases(oracle_mod):
+    # worked out from the e4m3 definition (4 significand bits, largest finite 448, no inf)
+    cases = {464.0: 0x7E,                     # tie between 448 (even) and 480 (not finite) -> 448
+             1000.0: 0x7E, -1e9: 0xFE,         # saturate (satfinite)
+             2.0 ** -10: 0x00,                 # half the smallest subnormal: tie -> 0
+             3 * 2.0 ** -10: 0x02,             # tie between 1 and 2 subnormal units -> 2
+             0.5 + 2.0 ** -5: 0x30,            # tie between 0.5 and 0.5625 -> 0.5 (even)
+             0.5 + 2.0 ** -5 + 2.0 ** -30: 0x31,
+             2.0 ** -6: 0x08, 448.0: 0x7E, -2.0: 0xC0}
+    got = oracle_mod.encode(np.array(list(cases)), E4M3)
+    assert [int(g) for g in got] == list(cases.values())
+
+
+@pytest.mark.parametrize("scale", [0.25, 1.0, 8.0])
+def test_quant_epilogue_against_library_chain(oracle_mod, scale):
+    # "Variants": matmul + quantized output; integer inputs and power-of-two scales are exact
+    M, N, K = 9, 14, 5
+    p = gen.integer_problem(M, N, K, BF16, F32, seed=int(scale * 4))
+    r = oracle_mod.bias_relu_quant(p.A, p.B, p.bias, M, N, K, BF16, F32, scale)
+    A64, B64, b64 = oracle_mod.decode(p.A, BF16), oracle_mod.decode(p.B, BF16), oracle_mod.decode(p.bias, F32)
+    v = np.clip(scale * np.maximum(A64 @ B64 + b64[None, :], 0.0), -448, 448)
+    assert np.array_equal(r.ref, v)
+    assert np.array_equal(r.out, torch.from_numpy(v.astype(np.float32)).to(torch.float8_e4m3fn)
+                          .view(torch.uint8).numpy())
+
+
+def test_quant_closed_forms(oracle_mod):
+    M, N, K = 3, 5, 4
+    bias = np.array([-1.0, 0.0, 3.0, 100.0, 1e4])
+    A = enc(oracle_mod, np.zeros((M, K)), F16)
+    B = enc(oracle_mod, np.ones((K, N)), F16)
+    r = oracle_mod.bias_relu_quant(A, B, enc(oracle_mod, bias, F32), M, N, K, F16, F32, 2.0)
+    assert np.array_equal(r.ref, np.tile([0.0, 0.0, 6.0, 200.0, 448.0], (M, 1)))   # clamp at 448
+    assert np.array_equal(oracle_mod.decode(r.out, E4M3), np.tile([0.0, 0.0, 6.0, 192.0, 448.0], (M, 1)))
+
+
 # --------------------------------------------------------- negative controls --
 
 def _pins_pass(oracle_mod, mutant):
@@ -355,6 +417,11 @@ def _pins_pass(oracle_mod, mutant):
     rr = oracle_mod.bias_residual_relu(p.A, p.B, p.bias, p.Y, 5, 4, 3, F16, F16, F32, mutant=mutant)
     A64, B64, b64, R64 = (oracle_mod.decode(x, F16) for x in (p.A, p.B, p.bias, p.Y))
     ok &= np.array_equal(rr.ref, np.maximum(A64 @ B64 + b64[None, :] + R64, 0.0))
+    # quantized output: scale after bias and activation
+    p = gen.integer_problem(6, 5, 3, BF16, F32, seed=52)
+    qq = oracle_mod.bias_relu_quant(p.A, p.B, p.bias, 6, 5, 3, BF16, F32, 0.5, mutant=mutant)
+    A64, B64, b64 = oracle_mod.decode(p.A, BF16), oracle_mod.decode(p.B, BF16), oracle_mod.decode(p.bias, F32)
+    ok &= np.array_equal(qq.ref, np.clip(0.5 * np.maximum(A64 @ B64 + b64[None, :], 0), -448, 448))
     # rectangular non-symmetric matmul against numpy (catches transposed operands)
     p = gen.random_problem(7, 5, 9, BF16, F32, seed=60)
     zero = np.zeros(5, dtype=np.float32)
@@ -369,6 +436,7 @@ def test_pins_accept_the_oracle(oracle_mod):
 
 
 @pytest.mark.parametrize("name", ["relu_first", "bias_row", "bias_in_sum", "drop_gemm",
-                                  "transpose_b", "drop_last_k", "gate_sign", "resid_after"])
+                                  "transpose_b", "drop_last_k", "gate_sign", "resid_after",
+                                  "scale_first"])
 def test_pins_reject_each_planted_mistake(oracle_mod, name):
     assert not _pins_pass(oracle_mod, oracle_mod.MUTANTS[name])
