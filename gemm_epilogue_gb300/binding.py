@@ -18,14 +18,14 @@ LIB_PATH = os.path.join(_HERE, "libfgemm.so")
 # dtype word (include/fgemm.h)
 F16, BF16 = 0x1, 0x2
 BIAS_SAME, BIAS_F32 = 0x00, 0x10
-OUT_SAME, OUT_F32 = 0x000, 0x100
+OUT_SAME, OUT_F32, OUT_E4M3 = 0x000, 0x100, 0x200
 
 # status codes
 OK, ERR_INVALID_VALUE, ERR_UNSUPPORTED_DTYPE, ERR_MISALIGNED = 0, 1, 2, 3
 ERR_NO_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSPACE = 4, 5, 6, 7
 
 # epilogue codes (fgemm_plan)
-EPI_RELU, EPI_GATE, EPI_RESIDUAL_RELU = 0, 1, 2
+EPI_RELU, EPI_GATE, EPI_RESIDUAL_RELU, EPI_RELU_QUANT = 0, 1, 2, 3
 
 # paths
 PATH_AUTO, PATH_TC, PATH_SKINNY, PATH_GENERIC, PATH_KZERO, PATH_NONE = 0, 1, 2, 3, 4, 5
@@ -64,6 +64,10 @@ _SIGS = {
     "fgemm_bias_residual_relu": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]),
     "fgemm_bias_residual_relu_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp,
                                            ctypes.POINTER(Opts), ctypes.POINTER(_int)]),
+    "fgemm_bias_relu_quant": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, ctypes.c_float,
+                                     _vp]),
+    "fgemm_bias_relu_quant_ex": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, ctypes.c_float,
+                                        _vp, ctypes.POINTER(Opts), ctypes.POINTER(_int)]),
     "fgemm_bias_relu_ex": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp,
                                   ctypes.POINTER(Opts), ctypes.POINTER(_int)]),
     "fgemm_addmm_gate_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp,
@@ -160,6 +164,21 @@ def fgemm_bias_residual_relu_ex(A, B, bias, R, out, M, N, K, dtype, stream=None,
                                              K, dtype, _stream(stream),
                                              ctypes.byref(o) if o else None, ctypes.byref(taken)),
            "fgemm_bias_residual_relu_ex")
+    return taken.value
+
+
+def fgemm_bias_relu_quant(A, B, bias, out, M, N, K, dtype, scale, stream=None) -> None:
+    _check(lib().fgemm_bias_relu_quant(_ptr(A), _ptr(B), _ptr(bias), _ptr(out), M, N, K, dtype,
+                                       float(scale), _stream(stream)), "fgemm_bias_relu_quant")
+
+
+def fgemm_bias_relu_quant_ex(A, B, bias, out, M, N, K, dtype, scale, stream=None, opts=None) -> int:
+    taken = ctypes.c_int(-1)
+    o = _opts(opts)
+    _check(lib().fgemm_bias_relu_quant_ex(_ptr(A), _ptr(B), _ptr(bias), _ptr(out), M, N, K, dtype,
+                                          float(scale), _stream(stream),
+                                          ctypes.byref(o) if o else None, ctypes.byref(taken)),
+           "fgemm_bias_relu_quant_ex")
     return taken.value
 
 

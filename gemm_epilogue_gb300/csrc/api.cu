@@ -2,6 +2,7 @@
 // encoding and launches on the caller's stream.  Host code only, apart from the error word.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -82,24 +83,29 @@ struct Types {
   int ab, bias, out;  // Elem codes
 };
 
-int parse_dtype(int dtype, Types* t) {
+// fp8_out: the entry produces fp8 e4m3 (FGEMM_OUT_E4M3 required); otherwise it is refused.
+int parse_dtype(int dtype, Types* t, bool fp8_out = false) {
   const int ab = dtype & 0xF, bias = dtype & 0xF0, out = dtype & 0xF00;
   if ((dtype & ~0xFFF) != 0) return FGEMM_ERR_UNSUPPORTED_DTYPE;
   if (ab != FGEMM_F16 && ab != FGEMM_BF16) return FGEMM_ERR_UNSUPPORTED_DTYPE;
   if (bias != FGEMM_BIAS_SAME && bias != FGEMM_BIAS_F32) return FGEMM_ERR_UNSUPPORTED_DTYPE;
-  if (out != FGEMM_OUT_SAME && out != FGEMM_OUT_F32) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (fp8_out ? (out != FGEMM_OUT_E4M3) : (out != FGEMM_OUT_SAME && out != FGEMM_OUT_F32))
+    return FGEMM_ERR_UNSUPPORTED_DTYPE;
   t->ab = (ab == FGEMM_BF16) ? ELEM_BF16 : ELEM_F16;
   t->bias = (bias == FGEMM_BIAS_F32) ? ELEM_F32 : t->ab;
-  t->out = (out == FGEMM_OUT_F32) ? ELEM_F32 : t->ab;
+  t->out = (out == FGEMM_OUT_F32) ? ELEM_F32 : (out == FGEMM_OUT_E4M3 ? ELEM_E4M3 : t->ab);
   return FGEMM_OK;
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 CUtensorMapDataType tma_type(int e) {
-  return e == ELEM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                       : (e == ELEM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+  switch (e) {
+    case ELEM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    case ELEM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case ELEM_E4M3: return CU_TENSOR_MAP_DATA_TYPE_UINT8;  // stored bytes; no TMA conversion
+    default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  }
 }
 
 // Row-major matrix of `rows` x `cols` elements; box of box_rows x box_cols, 128-byte swizzle.
@@ -124,6 +130,7 @@ struct Call {
   int epi;  // Epi
   cudaStream_t stream;
   const fgemm_opts* opts;
+  float out_scale = 1.0f;  // quantized epilogue only
 };
 
 int status_of(cudaError_t e) {
@@ -165,6 +172,7 @@ int validate(const Call& c, bool* nothing) {
 
 bool tc_eligible(const Call& c) {
   if (c.K % 8 != 0 || c.N % 8 != 0) return false;  // 16-byte row strides for TMA
+  if (c.t.out == ELEM_E4M3 && c.N % 16 != 0) return false;  // 1-byte outputs: N bytes per row
   return aligned(c.A, 16) && aligned(c.B, 16) && aligned(c.out, 16) &&
          (c.bias == nullptr || aligned(c.bias, 16)) && (c.Y == nullptr || aligned(c.Y, 16));
 }
@@ -207,7 +215,8 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
   int split = 1;
   const bool allow = !(c.opts && c.opts->tail_split == 1);
   if (allow && rem > 0 && t.num_tiles > units) {
-    const int max_split = t.pair ? 2 : 4;
+    // fp8 outputs are stored 128 columns at a time: pieces stay >= 128 columns wide
+    const int max_split = (t.pair || c.t.out == ELEM_E4M3) ? 2 : 4;
     while (split * 2 <= max_split && rem * split * 2 <= units) split *= 2;
   }
   t.tail_split = split;
@@ -261,7 +270,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   const int BM = tc_block_m(), BN = tc_block_n();
   const int TILE_M = t.pair ? 2 * BM : BM;
   CUtensorMap tmA, tmB, tmO, tmY;
-  const uint32_t out_box_cols = (c.t.out == ELEM_F32) ? 32 : 64;
+  const uint32_t out_box_cols = 128u / static_cast<uint32_t>(elem_bytes(c.t.out));
   if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, 64) ||
       !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
       !encode_2d(&tmO, c.t.out, c.out, c.M, c.N, 32, out_box_cols))
@@ -287,6 +296,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.out_type = c.t.out;
   p.bias = c.bias;
   p.Y = c.Y;
+  p.out_scale = c.out_scale;
   p.idesc = idesc_f16_f32acc(p.ab_bf16 != 0, TILE_M, BN, /*a_mn=*/false, /*b_mn=*/true);
   const bool swap = c.opts && c.opts->b_desc_swap;
   p.b_lbo = swap ? 1024u : 64u * 64u * 2u;  // distance between 64-column boxes of B
@@ -320,6 +330,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   p.bias = c.bias;
   p.Y = c.Y;
   p.out = c.out;
+  p.out_scale = c.out_scale;
   p.idesc = idesc_f16_f32acc(c.t.ab == ELEM_BF16, skinny_block_n(), s.mpad, /*a_mn=*/true,
                              /*b_mn=*/false);
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
@@ -343,6 +354,7 @@ SimtParams simt_params(const Call& c) {
   p.ab_type = c.t.ab;
   p.bias_type = c.t.bias;
   p.out_type = c.t.out;
+  p.out_scale = c.out_scale;
   return p;
 }
 
@@ -431,6 +443,22 @@ int fgemm_bias_residual_relu_ex(const void* A, const void* B, const void* bias, 
 int fgemm_bias_residual_relu(const void* A, const void* B, const void* bias, const void* R,
                              void* out, int64_t M, int64_t N, int64_t K, int dtype, void* stream) {
   return fgemm_bias_residual_relu_ex(A, B, bias, R, out, M, N, K, dtype, stream, nullptr, nullptr);
+}
+
+int fgemm_bias_relu_quant_ex(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                             int64_t N, int64_t K, int dtype, float scale, void* stream,
+                             const fgemm_opts* opts, int* path_taken) {
+  Call c{A, B, bias, nullptr, out, M, N, K, {}, EPI_QUANT, static_cast<cudaStream_t>(stream), opts};
+  c.out_scale = scale;
+  const int st = parse_dtype(dtype, &c.t, /*fp8_out=*/true);
+  if (st != FGEMM_OK) return st;
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return FGEMM_ERR_INVALID_VALUE;
+  return fused(c, path_taken);
+}
+
+int fgemm_bias_relu_quant(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                          int64_t N, int64_t K, int dtype, float scale, void* stream) {
+  return fgemm_bias_relu_quant_ex(A, B, bias, out, M, N, K, dtype, scale, stream, nullptr, nullptr);
 }
 
 int fgemm_bias_relu(const void* A, const void* B, const void* bias, void* out, int64_t M,
@@ -540,12 +568,13 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
   if (!info) return FGEMM_ERR_INVALID_VALUE;
   *info = fgemm_plan_info{};
   info->path = FGEMM_PATH_NONE;
-  if (epilogue < FGEMM_EPI_RELU || epilogue > FGEMM_EPI_RESIDUAL_RELU) return FGEMM_ERR_INVALID_VALUE;
+  if (epilogue < FGEMM_EPI_RELU || epilogue > FGEMM_EPI_RELU_QUANT) return FGEMM_ERR_INVALID_VALUE;
   const int epi = epilogue == FGEMM_EPI_GATE ? EPI_GATE
-                : epilogue == FGEMM_EPI_RESIDUAL_RELU ? EPI_RESID : EPI_RELU;
-  Call c{A, B, bias, epi == EPI_RELU ? nullptr : Y, const_cast<void*>(out), M, N, K, {}, epi,
-         nullptr, opts};
-  int st = parse_dtype(dtype, &c.t);
+                : epilogue == FGEMM_EPI_RESIDUAL_RELU ? EPI_RESID
+                : epilogue == FGEMM_EPI_RELU_QUANT ? EPI_QUANT : EPI_RELU;
+  Call c{A, B, bias, (epi == EPI_GATE || epi == EPI_RESID) ? Y : nullptr, const_cast<void*>(out),
+         M, N, K, {}, epi, nullptr, opts};
+  int st = parse_dtype(dtype, &c.t, epi == EPI_QUANT);
   if (st != FGEMM_OK) return st;
   bool nothing = false;
   st = validate(c, &nothing);

@@ -7,10 +7,11 @@
 namespace fgemm {
 
 // EPI_RESID: out = ReLU(acc + bias + R) with R (M x N, operand type) passed where the gate's Y is.
-enum Epi : int { EPI_RELU = 0, EPI_GATE = 1, EPI_NONE = 2, EPI_RESID = 3 };
-enum Elem : int { ELEM_F16 = 0, ELEM_BF16 = 1, ELEM_F32 = 2 };
+// EPI_QUANT: out = e4m3(clamp(out_scale * ReLU(acc + bias), -448, 448)), fp8 output.
+enum Epi : int { EPI_RELU = 0, EPI_GATE = 1, EPI_NONE = 2, EPI_RESID = 3, EPI_QUANT = 4 };
+enum Elem : int { ELEM_F16 = 0, ELEM_BF16 = 1, ELEM_F32 = 2, ELEM_E4M3 = 3 };
 
-inline int elem_bytes(int e) { return e == ELEM_F32 ? 4 : 2; }
+inline int elem_bytes(int e) { return e == ELEM_F32 ? 4 : (e == ELEM_E4M3 ? 1 : 2); }
 
 // Arguments of the persistent tensor-core kernel (tensor maps travel separately as
 // __grid_constant__ parameters).
@@ -26,6 +27,7 @@ struct TcParams {
   int out_type;    // Elem of out
   const void* bias;
   const void* Y;   // gate only, M x N operand type
+  float out_scale; // quantized epilogue only
   uint32_t idesc;  // tcgen05 instruction descriptor
   uint32_t b_lbo, b_sbo;  // B (MN-major) descriptor byte offsets
   uint64_t timeout_ns;
@@ -44,6 +46,7 @@ struct SimtParams {
   int ab_type;    // Elem
   int bias_type;  // Elem
   int out_type;   // Elem
+  float out_scale;  // quantized epilogue only
 };
 
 // pair = true: 2-CTA clusters (grid even), 256 x 256 tiles, tiles_m counted in 256-row tiles.
@@ -69,6 +72,7 @@ struct SkParams {
   const void* bias;
   const void* Y;
   void* out;
+  float out_scale;  // quantized epilogue only
   uint32_t idesc;
   uint64_t timeout_ns;
   int* err;

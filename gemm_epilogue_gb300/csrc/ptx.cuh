@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace fgemm {
@@ -252,6 +253,11 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   }
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+// Two floats to two fp8 e4m3 values (round to nearest even, saturating at +-448), low byte first.
+__device__ __forceinline__ uint32_t pack2_e4m3(float lo, float hi) {
+  return static_cast<uint32_t>(
+      __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
 }
 __device__ __forceinline__ float2 unpack2(uint32_t v, bool bf16) {
   if (bf16) {

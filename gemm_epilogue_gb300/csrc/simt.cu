@@ -15,17 +15,23 @@ __device__ __forceinline__ float ld_elem(const void* p, int64_t i, int type) {
 
 __device__ __forceinline__ void st_elem(void* p, int64_t i, int type, float v) {
   switch (type) {
+    case ELEM_E4M3:
+      static_cast<uint8_t*>(p)[i] =
+          static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+      break;
     case ELEM_F16: static_cast<__half*>(p)[i] = __float2half_rn(v); break;
     case ELEM_BF16: static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v); break;
     default: static_cast<float*>(p)[i] = v; break;
   }
 }
 
-// The epilogue on one element: x = acc + bias, then ReLU or the gate.  fp32 throughout.
+// The epilogue on one element: x = acc + bias, then ReLU, the gate, the residual add + ReLU, or
+// ReLU + scale + clamp to the fp8 range (the cast happens at the store).  fp32 throughout.
 template <int EPI>
-__device__ __forceinline__ float epilogue(float acc, float bias, float y) {
+__device__ __forceinline__ float epilogue(float acc, float bias, float y, float scale = 1.0f) {
   if constexpr (EPI == EPI_NONE) return acc;
   const float x = acc + bias;
+  if constexpr (EPI == EPI_QUANT) return fminf(fmaxf(fmaxf(x, 0.0f) * scale, -448.0f), 448.0f);
   if constexpr (EPI == EPI_RELU) return fmaxf(x, 0.0f);
   if constexpr (EPI == EPI_RESID) return fmaxf(x + y, 0.0f);  // residual before the activation
   return fmaf(x, y, x);  // X + X * Y
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(gen::THREADS) generic_kernel(const SimtParams 
       if (gm >= p.M) continue;
       const int64_t idx = static_cast<int64_t>(gm) * p.N + gn;
       const float y = (EPI == EPI_GATE || EPI == EPI_RESID) ? ld_elem(p.Y, idx, p.ab_type) : 0.f;
-      st_elem(p.out, idx, p.out_type, epilogue<EPI>(acc[i][j], bj, y));
+      st_elem(p.out, idx, p.out_type, epilogue<EPI>(acc[i][j], bj, y, p.out_scale));
     }
   }
 }
@@ -109,6 +115,7 @@ cudaError_t launch_generic(int epi, const SimtParams& p, cudaStream_t s) {
     case EPI_RELU: generic_kernel<EPI_RELU><<<grid, gen::THREADS, 0, s>>>(p); break;
     case EPI_GATE: generic_kernel<EPI_GATE><<<grid, gen::THREADS, 0, s>>>(p); break;
     case EPI_RESID: generic_kernel<EPI_RESID><<<grid, gen::THREADS, 0, s>>>(p); break;
+    case EPI_QUANT: generic_kernel<EPI_QUANT><<<grid, gen::THREADS, 0, s>>>(p); break;
     default: generic_kernel<EPI_NONE><<<grid, gen::THREADS, 0, s>>>(p); break;
   }
   return cudaGetLastError();
@@ -144,7 +151,12 @@ __device__ __forceinline__ Vec8 ld8(const void* p, int64_t i, int type) {
 }
 
 __device__ __forceinline__ void st8(void* p, int64_t i, int type, const Vec8& x) {
-  if (type == ELEM_F32) {
+  if (type == ELEM_E4M3) {
+    uint2 u;
+    u.x = pack2_e4m3(x.v[0], x.v[1]) | (pack2_e4m3(x.v[2], x.v[3]) << 16);
+    u.y = pack2_e4m3(x.v[4], x.v[5]) | (pack2_e4m3(x.v[6], x.v[7]) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p) + i) = u;
+  } else if (type == ELEM_F32) {
     float4* q = reinterpret_cast<float4*>(static_cast<float*>(p) + i);
     q[0] = make_float4(x.v[0], x.v[1], x.v[2], x.v[3]);
     q[1] = make_float4(x.v[4], x.v[5], x.v[6], x.v[7]);
@@ -160,9 +172,10 @@ __device__ __forceinline__ void st8(void* p, int64_t i, int type, const Vec8& x)
 }
 
 enum EwOp { EW_BIAS_INPLACE = 0, EW_RELU = 1, EW_BIAS_GATE = 2, EW_KZERO_RELU = 3, EW_KZERO_GATE = 4,
-            EW_KZERO_RESID = 5 };
+            EW_KZERO_RESID = 5, EW_KZERO_QUANT = 6 };
 
 struct EwParams {
+  float scale;       // quantized K = 0 epilogue only
   const void* src;   // I (the intermediate) or NULL for K = 0
   int src_type;
   const void* bias;
@@ -175,7 +188,9 @@ struct EwParams {
 };
 
 template <int OP>
-__device__ __forceinline__ float ew_apply(float s, float b, float y) {
+__device__ __forceinline__ float ew_apply(float s, float b, float y, float scale) {
+  if constexpr (OP == EW_KZERO_QUANT)
+    return fminf(fmaxf(fmaxf(0.0f + b, 0.0f) * scale, -448.0f), 448.0f);
   if constexpr (OP == EW_BIAS_INPLACE) return s + b;
   if constexpr (OP == EW_RELU) return fmaxf(s, 0.0f);
   if constexpr (OP == EW_BIAS_GATE) {
@@ -204,7 +219,7 @@ __global__ void __launch_bounds__(256) ew_kernel(const EwParams p) {
       if constexpr (uses_bias) b = ld8(p.bias, col, p.bias_type);
       if constexpr (uses_y) y = ld8(p.Y, i, p.y_type);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o.v[e] = ew_apply<OP>(s.v[e], b.v[e], y.v[e]);
+      for (int e = 0; e < 8; ++e) o.v[e] = ew_apply<OP>(s.v[e], b.v[e], y.v[e], p.scale);
       st8(p.dst, i, p.dst_type, o);
     }
   } else {
@@ -213,7 +228,7 @@ __global__ void __launch_bounds__(256) ew_kernel(const EwParams p) {
       const float s = uses_src ? ld_elem(p.src, i, p.src_type) : 0.f;
       const float b = uses_bias ? ld_elem(p.bias, col, p.bias_type) : 0.f;
       const float y = uses_y ? ld_elem(p.Y, i, p.y_type) : 0.f;
-      st_elem(p.dst, i, p.dst_type, ew_apply<OP>(s, b, y));
+      st_elem(p.dst, i, p.dst_type, ew_apply<OP>(s, b, y, p.scale));
     }
   }
 }
@@ -224,7 +239,8 @@ template <int OP>
 static cudaError_t launch_ew(const EwParams& p, int num_sms, cudaStream_t s) {
   const int64_t total = static_cast<int64_t>(p.M) * p.N;
   if (total == 0) return cudaSuccess;
-  const bool vec = (p.N % 8 == 0) && aligned16(p.src) && aligned16(p.bias) && aligned16(p.Y) && aligned16(p.dst);
+  const bool vec = (p.N % 8 == 0) && aligned16(p.src) && aligned16(p.bias) && aligned16(p.Y) &&
+                   aligned16(p.dst);  // (8 fp8 outputs are 8 bytes: 8-byte aligned when dst is)
   const int64_t work = vec ? (total + 7) / 8 : total;
   int64_t blocks = (work + 255) / 256;
   const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 16;
@@ -237,7 +253,9 @@ static cudaError_t launch_ew(const EwParams& p, int num_sms, cudaStream_t s) {
 }
 
 cudaError_t launch_kzero(int epi, const SimtParams& sp, int num_sms, cudaStream_t s) {
-  EwParams p{nullptr, 0, sp.bias, sp.bias_type, sp.Y, sp.ab_type, sp.out, sp.out_type, sp.M, sp.N};
+  EwParams p{sp.out_scale, nullptr, 0, sp.bias, sp.bias_type, sp.Y, sp.ab_type, sp.out, sp.out_type,
+             sp.M, sp.N};
+  if (epi == EPI_QUANT) return launch_ew<EW_KZERO_QUANT>(p, num_sms, s);
   if (epi == EPI_GATE) return launch_ew<EW_KZERO_GATE>(p, num_sms, s);
   if (epi == EPI_RESID) return launch_ew<EW_KZERO_RESID>(p, num_sms, s);
   return launch_ew<EW_KZERO_RELU>(p, num_sms, s);
@@ -245,20 +263,20 @@ cudaError_t launch_kzero(int epi, const SimtParams& sp, int num_sms, cudaStream_
 
 cudaError_t launch_ew_bias_inplace(void* I, int inter_type, const void* bias, int bias_type, int M,
                                    int N, int num_sms, cudaStream_t s) {
-  EwParams p{I, inter_type, bias, bias_type, nullptr, 0, I, inter_type, M, N};
+  EwParams p{1.0f, I, inter_type, bias, bias_type, nullptr, 0, I, inter_type, M, N};
   return launch_ew<EW_BIAS_INPLACE>(p, num_sms, s);
 }
 
 cudaError_t launch_ew_relu(const void* I, int inter_type, void* out, int out_type, int M, int N,
                            int num_sms, cudaStream_t s) {
-  EwParams p{I, inter_type, nullptr, 0, nullptr, 0, out, out_type, M, N};
+  EwParams p{1.0f, I, inter_type, nullptr, 0, nullptr, 0, out, out_type, M, N};
   return launch_ew<EW_RELU>(p, num_sms, s);
 }
 
 cudaError_t launch_ew_bias_gate(const void* I, int inter_type, const void* bias, int bias_type,
                                 const void* Y, int y_type, void* out, int out_type, int M, int N,
                                 int num_sms, cudaStream_t s) {
-  EwParams p{I, inter_type, bias, bias_type, Y, y_type, out, out_type, M, N};
+  EwParams p{1.0f, I, inter_type, bias, bias_type, Y, y_type, out, out_type, M, N};
   return launch_ew<EW_BIAS_GATE>(p, num_sms, s);
 }
 

@@ -71,6 +71,10 @@ __device__ __forceinline__ float ld_any(const void* p, int64_t i, int type) {
 }
 __device__ __forceinline__ void st_any(void* p, int64_t i, int type, float v) {
   switch (type) {
+    case ELEM_E4M3:
+      static_cast<uint8_t*>(p)[i] =
+          static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+      break;
     case ELEM_F16: static_cast<__half*>(p)[i] = __float2half_rn(v); break;
     case ELEM_BF16: static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v); break;
     default: static_cast<float*>(p)[i] = v; break;
@@ -294,6 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int64_t o = static_cast<int64_t>(m + e) * p.N + n;
         float v = s4[e] + b;
         if constexpr (EPI == EPI_RELU) v = fmaxf(v, 0.0f);
+        if constexpr (EPI == EPI_QUANT) v = fminf(fmaxf(fmaxf(v, 0.0f) * p.out_scale, -448.0f), 448.0f);
         if constexpr (EPI == EPI_GATE) v = fmaf(v, ld_any(p.Y, o, p.ab_type), v);
         if constexpr (EPI == EPI_RESID) v = fmaxf(v + ld_any(p.Y, o, p.ab_type), 0.0f);
         st_any(p.out, o, p.out_type, v);
@@ -355,6 +360,7 @@ cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tm
     case EPI_RELU: return sk::launch_one<EPI_RELU>(tmB, tmA, p, ctas, s);
     case EPI_GATE: return sk::launch_one<EPI_GATE>(tmB, tmA, p, ctas, s);
     case EPI_RESID: return sk::launch_one<EPI_RESID>(tmB, tmA, p, ctas, s);
+    case EPI_QUANT: return sk::launch_one<EPI_QUANT>(tmB, tmA, p, ctas, s);
     default: return sk::launch_one<EPI_NONE>(tmB, tmA, p, ctas, s);
   }
 }

@@ -104,9 +104,9 @@ __device__ __forceinline__ Work work_of(const TcParams& p, int item) {
   return w;
 }
 
-template <int OUT_BYTES>
-__device__ __forceinline__ void load_bias_granule(const TcParams& p, int col, float (&b)[16 / OUT_BYTES]) {
-  constexpr int G = 16 / OUT_BYTES;
+// Bias values of columns col .. col+G-1 as fp32 (zeros past N; N is a multiple of G here).
+template <int G>
+__device__ __forceinline__ void load_bias(const TcParams& p, int col, float (&b)[G]) {
   if (col >= p.N) {
 #pragma unroll
     for (int e = 0; e < G; ++e) b[e] = 0.f;
@@ -122,13 +122,17 @@ __device__ __forceinline__ void load_bias_granule(const TcParams& p, int col, fl
   } else {
     const bool bf = p.bias_type == ELEM_BF16;
     const uint16_t* src = static_cast<const uint16_t*>(p.bias) + col;
-    if (G == 8) {
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if constexpr (G >= 8) {
 #pragma unroll
-      for (int v = 0; v < 4 && v < G / 2; ++v) {
-        const float2 f = unpack2(w[v], bf);
-        b[2 * v] = f.x; b[2 * v + 1] = f.y;
+      for (int v = 0; v < G / 8; ++v) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + v);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = unpack2(w[k], bf);
+          b[8 * v + 2 * k] = f.x;
+          b[8 * v + 2 * k + 1] = f.y;
+        }
       }
     } else {  // G == 4: 4 x 16-bit = 8 bytes
       const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
@@ -380,7 +384,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                          : "r"(addr)
                          : "memory");
             float bv[G];
-            load_bias_granule<OUT_BYTES>(p, col0 + g * G, bv);
+            load_bias<G>(p, col0 + g * G, bv);
             uint32_t packed[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -441,6 +445,55 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int col0 = n0 + c * CH;
         if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
 
+        if constexpr (OUT_BYTES == 1) {
+          // fp8 output: one 128-byte staging row holds 128 columns; work on them 64 at a time.
+          const uint32_t sb = ebuf;
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            uint32_t acc[64];
+            __syncwarp();  // tcgen05.ld is warp-collective
+            {
+              uint32_t(&a0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[0]);
+              uint32_t(&a1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&acc[32]);
+              tmem_ld32(taddr, a0, c * CH + 64 * h);
+              tmem_ld32(taddr, a1, c * CH + 64 * h + 32);
+              tmem_ld_wait();
+            }
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi) {
+              const int g = 4 * h + gi;  // 16-column granule within the 128-column row
+              float bv[16];
+              load_bias<16>(p, col0 + g * 16, bv);
+              uint32_t packed[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                float x[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int j = 16 * gi + 4 * e + k;
+                  float v = fmaxf(__uint_as_float(acc[j]) + bv[4 * e + k], 0.0f);  // bias, ReLU
+                  v = fminf(fmaxf(v * p.out_scale, -448.0f), 448.0f);              // scale, clamp
+                  x[k] = v;
+                }
+                packed[e] = pack2_e4m3(x[0], x[1]) | (pack2_e4m3(x[2], x[3]) << 16);
+              }
+              const uint32_t dst = sb + static_cast<uint32_t>(lane) * 128u +
+                                   (static_cast<uint32_t>(g ^ (lane & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(packed[0]),
+                           "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
+                           : "memory");
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmOut, sb, col0, row0, pol_out);
+            bulk_commit();
+          }
+          continue;
+        } else {
         // Gate: this thread's row of Y for the chunk, loaded before the TMEM read.
         constexpr bool HAS_Y = EPI == EPI_GATE || EPI == EPI_RESID;
         uint4 yv[HAS_Y ? NG * G / 8 : 1];
@@ -476,7 +529,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           float bv[G];
-          if constexpr (EPI != EPI_NONE) load_bias_granule<OUT_BYTES>(p, col0 + g * G, bv);
+          if constexpr (EPI != EPI_NONE) load_bias<G>(p, col0 + g * G, bv);
           float v[G];
 #pragma unroll
           for (int e = 0; e < G; ++e) {
@@ -529,6 +582,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_store_2d(&tmOut, sb, col0, row0, pol_out);
           bulk_commit();
         }
+        }  // OUT_BYTES != 1
       }
       // This warp has finished reading accumulator b: release it to the MMA warp.
       tc_fence_before();
@@ -630,6 +684,7 @@ cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const
 
 int tc_max_active_pairs(int epi, int out_type) {
   const bool f32 = out_type == ELEM_F32;
+  if (epi == EPI_QUANT) return tc::max_pairs<EPI_QUANT, 1>();
   switch (epi) {
     case EPI_RELU: return f32 ? tc::max_pairs<EPI_RELU, 4>() : tc::max_pairs<EPI_RELU, 2>();
     case EPI_GATE: return f32 ? tc::max_pairs<EPI_GATE, 4>() : tc::max_pairs<EPI_GATE, 2>();
@@ -645,6 +700,7 @@ cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const
                       const CUtensorMap& y, const TcParams& p, int grid, bool pair,
                       cudaStream_t s) {
   const bool f32 = p.out_type == ELEM_F32;
+  if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1>(a, b, o, y, p, grid, pair, s);
   switch (epi) {
     case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, y, p, grid, pair, s)
                               : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, y, p, grid, pair, s);

@@ -64,11 +64,13 @@ typedef enum {
 #define FGEMM_BIAS_F32 0x10  /* bias is fp32 */
 #define FGEMM_OUT_SAME 0x000 /* out has the operand type */
 #define FGEMM_OUT_F32 0x100  /* out is fp32 */
+#define FGEMM_OUT_E4M3 0x200 /* out is fp8 e4m3 (fgemm_bias_relu_quant only) */
 
 /* Epilogue codes (fgemm_plan). */
 #define FGEMM_EPI_RELU 0          /* fgemm_bias_relu */
 #define FGEMM_EPI_GATE 1          /* fgemm_addmm_gate */
 #define FGEMM_EPI_RESIDUAL_RELU 2 /* fgemm_bias_residual_relu */
+#define FGEMM_EPI_RELU_QUANT 3    /* fgemm_bias_relu_quant */
 
 /* Kernel paths (fgemm_opts.path, and *path_taken of the _ex entries). */
 #define FGEMM_PATH_AUTO 0    /* library choice */
@@ -120,6 +122,16 @@ int fgemm_addmm_gate(const void* A, const void* B, const void* bias, const void*
 int fgemm_bias_residual_relu(const void* A, const void* B, const void* bias, const void* R,
                              void* out, int64_t M, int64_t N, int64_t K, int dtype, void* stream);
 
+/*
+ * Quantized output: out = e4m3(clamp(scale * ReLU(A @ B + bias), -448, 448)), one byte per element
+ * (fp8 e4m3, round to nearest even).  "Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)",
+ * "Variants": matmul + quantized output -- a scale and a clamp applied to the accumulator, then
+ * the cast before the store.  dtype = operand type | bias type | FGEMM_OUT_E4M3.  scale must be
+ * finite (else FGEMM_ERR_INVALID_VALUE).  The tensor-core path needs N to be a multiple of 16.
+ */
+int fgemm_bias_relu_quant(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                          int64_t N, int64_t K, int dtype, float scale, void* stream);
+
 /* As above, with options (may be NULL) and the path that ran (may be NULL). */
 int fgemm_bias_relu_ex(const void* A, const void* B, const void* bias, void* out, int64_t M,
                        int64_t N, int64_t K, int dtype, void* stream, const fgemm_opts* opts,
@@ -130,6 +142,9 @@ int fgemm_addmm_gate_ex(const void* A, const void* B, const void* bias, const vo
 int fgemm_bias_residual_relu_ex(const void* A, const void* B, const void* bias, const void* R,
                                 void* out, int64_t M, int64_t N, int64_t K, int dtype,
                                 void* stream, const fgemm_opts* opts, int* path_taken);
+int fgemm_bias_relu_quant_ex(const void* A, const void* B, const void* bias, void* out, int64_t M,
+                             int64_t N, int64_t K, int dtype, float scale, void* stream,
+                             const fgemm_opts* opts, int* path_taken);
 
 /*
  * Unfused comparison chain (for measuring the traffic that fusion removes; not a fast path).

@@ -238,6 +238,56 @@ def test_residual_random_tolerance_and_guards():
                 Y64=None, what="residual")
 
 
+# ------------------------------------------------------- quantized fp8 output --
+
+E4M3 = 4
+QUANT_CASES = [  # M, N, K, opts, expected path
+    (300, 528, 200, {"cta_pair": 2}, 1), (300, 528, 200, {"cta_pair": 1, "max_ctas": 20}, 1),
+    (777, 1296, 328, None, 1), (16, 1040, 512, None, 2), (100, 272, 72, {"split_k": 3}, 2),
+    (7, 37, 13, None, 3), (300, 520, 200, None, 3), (37, 80, 0, None, 4)]
+
+
+def _run_quant(p, M, N, K, ab, bt, scale, opts=None):
+    A = up(p.A, ab) if K else None
+    B = up(p.B, ab) if K else None
+    out = torch.empty(M, N, dtype=torch.uint8, device="cuda")
+    w = (fg.F16 if ab == F16 else fg.BF16) | (fg.BIAS_F32 if bt == F32 else 0) | fg.OUT_E4M3
+    path = fg.fgemm_bias_relu_quant_ex(A, B, up(p.bias, bt), out, M, N, K, w, scale, opts=opts)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), path
+
+
+@pytest.mark.parametrize("M,N,K,opts,want_path", QUANT_CASES)
+def test_quant_integer_bit_exact(M, N, K, opts, want_path):
+    # "Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "Variants": matmul + quantized output.
+    # Integer inputs and power-of-two scales keep every value exact until the fp8 rounding, which
+    # both sides then take from the same number (saturating at 448 for the large sums).
+    for ab, bt, scale in ((BF16, BF16, 0.25), (F16, F32, 2.0)):
+        p = gen.integer_problem(M, N, K, ab, bt, seed=M + N + K)
+        got, path = _run_quant(p, M, N, K, ab, bt, scale, opts)
+        assert path == want_path
+        ref = oracle.bias_relu_quant(p.A, p.B, p.bias, M, N, K, ab, bt, scale)
+        if not np.array_equal(got, ref.out):
+            bad = np.argwhere(got != ref.out)
+            pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
+
+
+def test_quant_random_within_one_fp8_step():
+    M, N, K = 513, 784, 1024
+    p = gen.random_problem(M, N, K, BF16, BF16, seed=16, scale=K ** -0.25)
+    scale = 3.7
+    got, path = _run_quant(p, M, N, K, BF16, BF16, scale)
+    assert path == fg.PATH_TC
+    ref = oracle.bias_relu_quant(p.A, p.B, p.bias, M, N, K, BF16, BF16, scale)
+    g = oracle.decode(got, E4M3)
+    r = oracle.decode(ref.out, E4M3)
+    exact = ref.ref
+    # fp8 spacing at |exact| (3 fraction bits, subnormal spacing 2^-9)
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 2.0 ** -6))) - 3)
+    assert np.all(np.abs(g - r) <= step + 1e-12)
+    assert np.mean(g == r) > 0.99
+
+
 # ----------------------------------------------------------- float tolerance --
 
 def test_small_ragged_workload_tc_and_generic():
