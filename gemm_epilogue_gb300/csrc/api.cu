@@ -84,16 +84,24 @@ struct Types {
 };
 
 // fp8_out: the entry produces fp8 e4m3 (FGEMM_OUT_E4M3 required); otherwise it is refused.
+// fp8 operands (FGEMM_E4M3) take an explicit bias type (fp32 / bf16) and output type.
 int parse_dtype(int dtype, Types* t, bool fp8_out = false) {
   const int ab = dtype & 0xF, bias = dtype & 0xF0, out = dtype & 0xF00;
   if ((dtype & ~0xFFF) != 0) return FGEMM_ERR_UNSUPPORTED_DTYPE;
-  if (ab != FGEMM_F16 && ab != FGEMM_BF16) return FGEMM_ERR_UNSUPPORTED_DTYPE;
-  if (bias != FGEMM_BIAS_SAME && bias != FGEMM_BIAS_F32) return FGEMM_ERR_UNSUPPORTED_DTYPE;
-  if (fp8_out ? (out != FGEMM_OUT_E4M3) : (out != FGEMM_OUT_SAME && out != FGEMM_OUT_F32))
+  if (ab != FGEMM_F16 && ab != FGEMM_BF16 && ab != FGEMM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (bias != FGEMM_BIAS_SAME && bias != FGEMM_BIAS_F32 && bias != FGEMM_BIAS_BF16)
     return FGEMM_ERR_UNSUPPORTED_DTYPE;
-  t->ab = (ab == FGEMM_BF16) ? ELEM_BF16 : ELEM_F16;
-  t->bias = (bias == FGEMM_BIAS_F32) ? ELEM_F32 : t->ab;
-  t->out = (out == FGEMM_OUT_F32) ? ELEM_F32 : (out == FGEMM_OUT_E4M3 ? ELEM_E4M3 : t->ab);
+  if (fp8_out ? (out != FGEMM_OUT_E4M3)
+              : (out != FGEMM_OUT_SAME && out != FGEMM_OUT_F32 && out != FGEMM_OUT_BF16))
+    return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  const bool f8 = ab == FGEMM_E4M3;
+  if (f8 && (bias == FGEMM_BIAS_SAME || out == FGEMM_OUT_SAME)) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  t->ab = f8 ? ELEM_E4M3 : ((ab == FGEMM_BF16) ? ELEM_BF16 : ELEM_F16);
+  t->bias = (bias == FGEMM_BIAS_F32) ? ELEM_F32 : (bias == FGEMM_BIAS_BF16 ? ELEM_BF16 : t->ab);
+  t->out = (out == FGEMM_OUT_F32)    ? ELEM_F32
+           : (out == FGEMM_OUT_E4M3) ? ELEM_E4M3
+           : (out == FGEMM_OUT_BF16) ? ELEM_BF16
+                                     : t->ab;
   return FGEMM_OK;
 }
 
@@ -172,6 +180,7 @@ int validate(const Call& c, bool* nothing) {
 
 bool tc_eligible(const Call& c) {
   if (c.K % 8 != 0 || c.N % 8 != 0) return false;  // 16-byte row strides for TMA
+  if (c.t.ab == ELEM_E4M3 && (c.K % 16 != 0 || c.N % 16 != 0)) return false;  // 1-byte operands
   if (c.t.out == ELEM_E4M3 && c.N % 16 != 0) return false;  // 1-byte outputs: N bytes per row
   return aligned(c.A, 16) && aligned(c.B, 16) && aligned(c.out, 16) &&
          (c.bias == nullptr || aligned(c.bias, 16)) && (c.Y == nullptr || aligned(c.Y, 16));
@@ -215,8 +224,10 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
   int split = 1;
   const bool allow = !(c.opts && c.opts->tail_split == 1);
   if (allow && rem > 0 && t.num_tiles > units) {
-    // fp8 outputs are stored 128 columns at a time: pieces stay >= 128 columns wide
-    const int max_split = (t.pair || c.t.out == ELEM_E4M3) ? 2 : 4;
+    // fp8 outputs are stored 128 columns at a time: pieces stay >= 128 columns wide; fp8
+    // operands stage B in 128-column boxes per CTA: pieces stay >= 128 columns per CTA
+    int max_split = (t.pair || c.t.out == ELEM_E4M3) ? 2 : 4;
+    if (c.t.ab == ELEM_E4M3) max_split = t.pair ? 1 : 2;
     while (split * 2 <= max_split && rem * split * 2 <= units) split *= 2;
   }
   t.tail_split = split;
@@ -271,8 +282,9 @@ int run_tc(const Call& c, DeviceInfo* d) {
   const int TILE_M = t.pair ? 2 * BM : BM;
   CUtensorMap tmA, tmB, tmO, tmY;
   const uint32_t out_box_cols = 128u / static_cast<uint32_t>(elem_bytes(c.t.out));
-  if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, 64) ||
-      !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
+  const uint32_t kb_elems = 128u / static_cast<uint32_t>(elem_bytes(c.t.ab));  // one 128-B row
+  if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, kb_elems) ||
+      !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, kb_elems, kb_elems) ||
       !encode_2d(&tmO, c.t.out, c.out, c.M, c.N, 32, out_box_cols))
     return FGEMM_ERR_LAUNCH;
   if ((c.epi == EPI_GATE || c.epi == EPI_RESID) && c.t.out != ELEM_F32) {
@@ -292,6 +304,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.num_items = t.num_items;
   p.group = (c.opts && c.opts->group_m > 0) ? c.opts->group_m : 8;
   p.ab_bf16 = c.t.ab == ELEM_BF16;
+  p.ab_f8 = c.t.ab == ELEM_E4M3;
   p.bias_type = c.t.bias;
   p.out_type = c.t.out;
   p.bias = c.bias;
@@ -299,8 +312,9 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.out_scale = c.out_scale;
   p.idesc = idesc_f16_f32acc(p.ab_bf16 != 0, TILE_M, BN, /*a_mn=*/false, /*b_mn=*/true);
   const bool swap = c.opts && c.opts->b_desc_swap;
-  p.b_lbo = swap ? 1024u : 64u * 64u * 2u;  // distance between 64-column boxes of B
-  p.b_sbo = swap ? 64u * 64u * 2u : 1024u;  // distance between 8-row groups along K
+  const uint32_t box_bytes = kb_elems * kb_elems * static_cast<uint32_t>(elem_bytes(c.t.ab));
+  p.b_lbo = swap ? 1024u : box_bytes;  // distance between the 128-byte-wide column boxes of B
+  p.b_sbo = swap ? box_bytes : 1024u;  // distance between 8-row groups along K
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
@@ -368,11 +382,12 @@ int choose_path(const Call& c, int* out_path) {
     else if (!tc_eligible(c))
       path = FGEMM_PATH_GENERIC;
     else
-      path = (c.M <= skinny_max_m()) ? FGEMM_PATH_SKINNY : FGEMM_PATH_TC;
+      path = (c.M <= skinny_max_m() && c.t.ab != ELEM_E4M3) ? FGEMM_PATH_SKINNY : FGEMM_PATH_TC;
   } else {
     path = forced;
     if (path == FGEMM_PATH_TC && (c.K == 0 || !tc_eligible(c))) return FGEMM_ERR_INVALID_VALUE;
-    if (path == FGEMM_PATH_SKINNY && (c.K == 0 || !tc_eligible(c) || c.M > skinny_max_m()))
+    if (path == FGEMM_PATH_SKINNY &&
+        (c.K == 0 || !tc_eligible(c) || c.M > skinny_max_m() || c.t.ab == ELEM_E4M3))
       return FGEMM_ERR_INVALID_VALUE;
     if (path == FGEMM_PATH_KZERO && (c.K != 0 || c.epi == EPI_NONE)) return FGEMM_ERR_INVALID_VALUE;
   }
@@ -428,6 +443,7 @@ int fgemm_addmm_gate_ex(const void* A, const void* B, const void* bias, const vo
   Call c{A, B, bias, Y, out, M, N, K, {}, EPI_GATE, static_cast<cudaStream_t>(stream), opts};
   const int st = parse_dtype(dtype, &c.t);
   if (st != FGEMM_OK) return st;
+  if (c.t.ab == ELEM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;  // Y has the operand type
   return fused(c, path_taken);
 }
 
@@ -437,6 +453,7 @@ int fgemm_bias_residual_relu_ex(const void* A, const void* B, const void* bias, 
   Call c{A, B, bias, R, out, M, N, K, {}, EPI_RESID, static_cast<cudaStream_t>(stream), opts};
   const int st = parse_dtype(dtype, &c.t);
   if (st != FGEMM_OK) return st;
+  if (c.t.ab == ELEM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;  // R has the operand type
   return fused(c, path_taken);
 }
 
@@ -484,6 +501,7 @@ static int unfused(const void* A, const void* B, const void* bias, const void* Y
   Call fin{A, B, bias, Y, out, M, N, K, {}, epi, static_cast<cudaStream_t>(stream), nullptr};
   int st = parse_dtype(dtype, &fin.t);
   if (st != FGEMM_OK) return st;
+  if (fin.t.ab == ELEM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;
   bool nothing = false;
   st = validate(fin, &nothing);
   if (st != FGEMM_OK || nothing) return st;

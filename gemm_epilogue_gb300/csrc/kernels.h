@@ -23,6 +23,7 @@ struct TcParams {
   // (256 / tail_split columns each) so that the last round takes a fraction of a tile's time.
   int full_tiles, tail_split, num_items;
   int ab_bf16;     // operand (and Y) type: 0 = f16, 1 = bf16
+  int ab_f8;       // 1: A and B are fp8 e4m3 (kind::f8f6f4 MMAs, 128-element K blocks)
   int bias_type;   // Elem of the bias
   int out_type;    // Elem of out
   const void* bias;

@@ -235,8 +235,9 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
-// Instruction descriptor, kind::f16 with fp32 accumulator.
-//   bits 4-5 D type (1 = f32)   bits 7-9 A type, 10-12 B type (0 = f16, 1 = bf16)
+// Instruction descriptor, kind::f16 (or kind::f8f6f4) with fp32 accumulator.
+//   bits 4-5 D type (1 = f32)   bits 7-9 A type, 10-12 B type (kind::f16: 0 = f16, 1 = bf16;
+//   kind::f8f6f4: 0 = e4m3, 1 = e5m2 -- so an e4m3 descriptor is the f16 one with bf16 = false)
 //   bit 15 A MN-major, bit 16 B MN-major   bits 17-22 N >> 3   bits 24-28 M >> 4
 __host__ __device__ constexpr uint32_t idesc_f16_f32acc(bool bf16, int m, int n, bool a_mn,
                                                         bool b_mn) {
@@ -366,6 +367,26 @@ __device__ __forceinline__ void umma_f16_cg(uint32_t d_tmem, uint64_t adesc, uin
   else
     umma_f16(d_tmem, adesc, bdesc, idesc, accumulate);
 }
+// D[tmem] (+)= A * B with fp8 e4m3 / e5m2 operands (kind::f8f6f4), fp32 accumulate.
+template <int CG>
+__device__ __forceinline__ void umma_f8_cg(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  if constexpr (CG == 2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Commit arriving on barrier offset `bar` of every CTA in `mask` (CG == 2), or of this CTA.
 template <int CG>
 __device__ __forceinline__ void umma_commit_cg(uint32_t bar, uint16_t mask) {

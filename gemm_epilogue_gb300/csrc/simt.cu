@@ -7,6 +7,11 @@ namespace fgemm {
 
 __device__ __forceinline__ float ld_elem(const void* p, int64_t i, int type) {
   switch (type) {
+    case ELEM_E4M3: {
+      const __half_raw h =
+          __nv_cvt_fp8_to_halfraw(static_cast<const __nv_fp8_storage_t*>(p)[i], __NV_E4M3);
+      return __half2float(__half(h));
+    }
     case ELEM_F16: return __half2float(static_cast<const __half*>(p)[i]);
     case ELEM_BF16: return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
     default: return static_cast<const float*>(p)[i];

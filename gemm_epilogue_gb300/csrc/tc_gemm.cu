@@ -33,7 +33,7 @@
 namespace fgemm {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64;  // per-CTA rows, tile columns, K per stage
+constexpr int BM = 128, BN = 256, BK = 64;  // per-CTA rows, tile columns, 16-bit K per stage
 constexpr int EPI_WARPS = 8;  // two warpgroups: each owns half (128) of a tile's columns
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
@@ -142,7 +142,7 @@ __device__ __forceinline__ void load_bias(const TcParams& p, int col, float (&b)
   }
 }
 
-template <int EPI, int OUT_BYTES, bool PAIR>
+template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmY,
@@ -153,6 +153,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   // the gate's Y and the residual R are staged the same way (16-bit outputs)
   constexpr bool YS = (EPI == EPI_GATE || EPI == EPI_RESID) && (OUT_BYTES == 2);
   using C = Cfg<PAIR, YS>;
+  // Operand element size: one stage holds one 128-byte swizzle row of K per A row (64 16-bit or
+  // 128 fp8 elements) and B as boxes of (128 bytes of N) x (that K); the stage byte counts and
+  // the ring are the same for both.
+  constexpr int EB = F8 ? 1 : 2;
+  constexpr int KB_ELEMS = 128 / EB;                      // K per stage
+  constexpr int BOXC = 128 / EB;                          // B box columns
+  constexpr uint32_t BBOX = static_cast<uint32_t>(KB_ELEMS * BOXC * EB);  // 8 KB / 16 KB
+  constexpr int KSTEP = F8 ? 32 : 16;                     // K per MMA instruction
+  constexpr uint32_t B_KADV = static_cast<uint32_t>(KSTEP) * 128u;  // MN-major B bytes per MMA
   constexpr int STAGES = C::STAGES;
   constexpr int CG = PAIR ? 2 : 1;
   constexpr uint32_t SMEM_A = C::SMEM_A, SMEM_B = C::SMEM_B, SMEM_EPI = C::SMEM_EPI,
@@ -206,7 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_kb = (p.K + BK - 1) / BK;
+  const int num_kb = (p.K + KB_ELEMS - 1) / KB_ELEMS;
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
@@ -222,8 +231,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // each CTA of a pair stages half of the piece's columns
         const int cols = PAIR ? wk.width / 2 : wk.width;
         const int nb0 = wk.col0 + static_cast<int>(rank) * cols;
-        const int boxes = cols / 64;
-        const uint32_t tx = (PAIR ? 2u : 1u) * (A_STAGE_BYTES + static_cast<uint32_t>(boxes) * B_BOX_BYTES);
+        const int boxes = (cols + BOXC - 1) / BOXC;
+        const uint32_t tx = (PAIR ? 2u : 1u) * (A_STAGE_BYTES + static_cast<uint32_t>(boxes) * BBOX);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err,
                          SITE_PROD_EMPTY)) {
@@ -240,13 +249,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (stall) {
           } else if constexpr (PAIR) {
             const uint32_t lfb = lead_bar(BAR_FULL + stage);
-            tma_load_2d_pair(a_dst, &tmA, lfb, kb * BK, m0, pol);
+            tma_load_2d_pair(a_dst, &tmA, lfb, kb * KB_ELEMS, m0, pol);
             for (int c = 0; c < boxes; ++c)
-              tma_load_2d_pair(b_dst + c * B_BOX_BYTES, &tmB, lfb, nb0 + 64 * c, kb * BK, pol);
+              tma_load_2d_pair(b_dst + c * BBOX, &tmB, lfb, nb0 + BOXC * c, kb * KB_ELEMS, pol);
           } else {
-            tma_load_2d(a_dst, &tmA, fb, kb * BK, m0, pol);
+            tma_load_2d(a_dst, &tmA, fb, kb * KB_ELEMS, m0, pol);
             for (int c = 0; c < boxes; ++c)
-              tma_load_2d(b_dst + c * B_BOX_BYTES, &tmB, fb, nb0 + 64 * c, kb * BK, pol);
+              tma_load_2d(b_dst + c * BBOX, &tmB, fb, nb0 + BOXC * c, kb * KB_ELEMS, pol);
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -290,10 +299,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a_addr = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_addr = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
+          for (int k = 0; k < KB_ELEMS / KSTEP; ++k) {  // 32 bytes of K per MMA
             const uint64_t ad = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
-            const uint64_t bd = sdesc_sw128(b_addr + 2048u * k, p.b_lbo, p.b_sbo);
-            umma_f16_cg<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, p.b_lbo, p.b_sbo);
+            if constexpr (F8)
+              umma_f8_cg<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              umma_f16_cg<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit_cg<CG>(bar(BAR_EMPTY + stage), kPair);  // stage free (both CTAs) once read
           if (++stage == STAGES) {
@@ -610,10 +622,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int EPI, int OUT_BYTES, bool PAIR>
+template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                        const CUtensorMap& y, const TcParams& p, int grid, cudaStream_t s) {
-  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR>;
+  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8>;
   constexpr uint32_t smem =
       Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2>::SMEM_BYTES;
   static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
@@ -672,12 +684,12 @@ int max_pairs() {
   return cached;
 }
 
-template <int EPI, int OUT_BYTES>
+template <int EPI, int OUT_BYTES, bool F8 = false>
 cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                                const CUtensorMap& y, const TcParams& p, int grid, bool pair,
                                cudaStream_t s) {
-  return pair ? launch_one<EPI, OUT_BYTES, true>(a, b, o, y, p, grid, s)
-              : launch_one<EPI, OUT_BYTES, false>(a, b, o, y, p, grid, s);
+  return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, p, grid, s)
+              : launch_one<EPI, OUT_BYTES, false, F8>(a, b, o, y, p, grid, s);
 }
 
 }  // namespace tc
@@ -700,6 +712,12 @@ cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const
                       const CUtensorMap& y, const TcParams& p, int grid, bool pair,
                       cudaStream_t s) {
   const bool f32 = p.out_type == ELEM_F32;
+  if (p.ab_f8) {  // fp8 operands: bias + ReLU (bf16 / fp32 out) and the quantized epilogue
+    if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1, true>(a, b, o, y, p, grid, pair, s);
+    if (epi != EPI_RELU) return cudaErrorNotSupported;
+    return f32 ? tc::launch_pair_or_not<EPI_RELU, 4, true>(a, b, o, y, p, grid, pair, s)
+               : tc::launch_pair_or_not<EPI_RELU, 2, true>(a, b, o, y, p, grid, pair, s);
+  }
   if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1>(a, b, o, y, p, grid, pair, s);
   switch (epi) {
     case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, y, p, grid, pair, s)

@@ -23,9 +23,10 @@ import math
 
 import numpy as np
 
-# element type codes (match include/fgemm.h and the oracle's codes)
-F16, BF16, F32 = 1, 2, 3
-TYPE_NAMES = {F16: "f16", BF16: "bf16", F32: "f32"}
+# element type codes (the oracle's codes)
+F16, BF16, F32, E4M3 = 1, 2, 3, 4
+TYPE_NAMES = {F16: "f16", BF16: "bf16", F32: "f32", E4M3: "e4m3"}
+ELEM_BYTES = {F16: 2, BF16: 2, F32: 4, E4M3: 1}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -48,7 +49,7 @@ class Workload:
 
     def unavoidable_bytes(self) -> int:
         """A + B + bias + (Y) + out, each touched once."""
-        es = {F16: 2, BF16: 2, F32: 4}
+        es = ELEM_BYTES
         b = self.M * self.K * es[self.ab_type] + self.K * self.N * es[self.ab_type]
         b += self.N * es[self.bias_type] + self.M * self.N * es[self.out_type]
         if self.epilogue == "gate":
@@ -72,6 +73,12 @@ for _k in (256, 512, 1024):
     WORKLOADS[f"glu_gate_1024x21568x{_k}"] = Workload(f"glu_gate_1024x21568x{_k}", 1024, 21568, _k,
                                                       F16, F16, F16, "gate", 1.0 / 64.0, "normal",
                                                       5)
+# fp8 e4m3 operands (fp32 bias, bf16 out): the FFN up-projection and the square layer
+WORKLOADS["ffn_up_fp8_8192x14336x4096"] = Workload("ffn_up_fp8_8192x14336x4096", 8192, 14336, 4096,
+                                                   E4M3, F32, BF16, "bias_relu", 1.0 / 8.0,
+                                                   "uniform", 6)
+WORKLOADS["square_fp8_4096"] = Workload("square_fp8_4096", 4096, 4096, 4096, E4M3, F32, BF16,
+                                        "bias_relu", 1.0 / 8.0, "normal", 7)
 for _m in (1, 16, 64, 128):
     WORKLOADS[f"skinny_M{_m}_8192"] = Workload(f"skinny_M{_m}_8192", _m, 8192, 8192, BF16, BF16,
                                                BF16, "bias_relu", 1.0 / 90.0, "normal", 4)
@@ -80,10 +87,14 @@ for _m in (1, 16, 64, 128):
 def quantize(x: np.ndarray, t: int) -> np.ndarray:
     """Round float32/float64 values to storage type ``t`` once (RNE).
 
-    Returns uint16 bit patterns for F16/BF16 and float32 for F32.
+    Returns uint16 bit patterns for F16/BF16, uint8 for fp8 e4m3, float32 for F32.
     """
     if t == F32:
         return np.ascontiguousarray(x, dtype=np.float32)
+    if t == E4M3:
+        import torch
+        src = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+        return src.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
     if t == F16:
         return np.ascontiguousarray(x).astype(np.float16).view(np.uint16)
     if t == BF16:

@@ -60,11 +60,16 @@ typedef enum {
 /* dtype word = operand type | bias type | output type.  Y has the operand type. */
 #define FGEMM_F16 0x1        /* A, B (and Y) are IEEE binary16 */
 #define FGEMM_BF16 0x2       /* A, B (and Y) are bfloat16 */
-#define FGEMM_BIAS_SAME 0x00 /* bias has the operand type */
+#define FGEMM_E4M3 0x3       /* A, B are fp8 e4m3 (bias+ReLU and the quantized entry only; the
+                                bias and output types must then be given explicitly; tensor-core
+                                path for K, N multiples of 16, CUDA-core path otherwise) */
+#define FGEMM_BIAS_SAME 0x00 /* bias has the operand type (16-bit operands) */
 #define FGEMM_BIAS_F32 0x10  /* bias is fp32 */
-#define FGEMM_OUT_SAME 0x000 /* out has the operand type */
+#define FGEMM_BIAS_BF16 0x20 /* bias is bfloat16 */
+#define FGEMM_OUT_SAME 0x000 /* out has the operand type (16-bit operands) */
 #define FGEMM_OUT_F32 0x100  /* out is fp32 */
 #define FGEMM_OUT_E4M3 0x200 /* out is fp8 e4m3 (fgemm_bias_relu_quant only) */
+#define FGEMM_OUT_BF16 0x300 /* out is bfloat16 */
 
 /* Epilogue codes (fgemm_plan). */
 #define FGEMM_EPI_RELU 0          /* fgemm_bias_relu */

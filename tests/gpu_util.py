@@ -5,12 +5,12 @@ import numpy as np
 
 import oracle
 
-F16, BF16, F32 = 1, 2, 3
+F16, BF16, F32, E4M3 = 1, 2, 3, 4
 
 
 def torch_dtype(t):
     import torch
-    return {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32}[t]
+    return {F16: torch.float16, BF16: torch.bfloat16, F32: torch.float32, E4M3: torch.uint8}[t]
 
 
 def up(a, t, dev="cuda"):
@@ -20,6 +20,8 @@ def up(a, t, dev="cuda"):
         return None
     if t == F32:
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    if t == E4M3:
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).to(dev)
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch_dtype(t)).to(dev)
 
 
@@ -29,27 +31,35 @@ def down(x, t):
     x = x.detach().cpu().contiguous()
     if t == F32:
         return x.numpy().astype(np.float32)
+    if t == E4M3:
+        return x.numpy().astype(np.uint8)
     return x.view(torch.int16).numpy().view(np.uint16)
 
 
 def dtype_word(ab, bias, out):
     import gemm_epilogue_gb300.binding as fg
-    w = fg.F16 if ab == F16 else fg.BF16
+    w = {F16: fg.F16, BF16: fg.BF16, E4M3: fg.E4M3}[ab]
     if bias == F32:
         w |= fg.BIAS_F32
+    elif bias == BF16 and ab != BF16:
+        w |= fg.BIAS_BF16
     elif bias != ab:
-        raise ValueError("bias type must be the operand type or f32")
+        raise ValueError("unsupported bias type")
     if out == F32:
         w |= fg.OUT_F32
+    elif out == E4M3:
+        w |= fg.OUT_E4M3
+    elif out == BF16 and ab != BF16:
+        w |= fg.OUT_BF16
     elif out != ab:
-        raise ValueError("out type must be the operand type or f32")
+        raise ValueError("unsupported out type")
     return w
 
 
 def ulp(x, t):
     """Spacing of type t at |x| (the gap to the next representable magnitude)."""
     ax = np.abs(np.asarray(x, dtype=np.float64))
-    p, emin = {F16: (11, -14), BF16: (8, -126), F32: (24, -126)}[t]
+    p, emin = {F16: (11, -14), BF16: (8, -126), F32: (24, -126), E4M3: (4, -6)}[t]
     e = np.floor(np.log2(np.maximum(ax, 2.0 ** emin)))
     return np.exp2(np.maximum(e, emin) - (p - 1))
 

@@ -7,7 +7,7 @@ import pytest
 import oracle
 from conftest import parse_matrix, read_golden
 from gemm_epilogue_gb300 import inputs as gen
-from gpu_util import (BF16, F16, F32, check_close, down, dtype_word, sample_rows, up)
+from gpu_util import (BF16, E4M3, F16, F32, check_close, down, dtype_word, sample_rows, up)
 
 pytestmark = pytest.mark.gpu
 
@@ -240,7 +240,6 @@ def test_residual_random_tolerance_and_guards():
 
 # ------------------------------------------------------- quantized fp8 output --
 
-E4M3 = 4
 QUANT_CASES = [  # M, N, K, opts, expected path
     (300, 528, 200, {"cta_pair": 2}, 1), (300, 528, 200, {"cta_pair": 1, "max_ctas": 20}, 1),
     (777, 1296, 328, None, 1), (16, 1040, 512, None, 2), (100, 272, 72, {"split_k": 3}, 2),
@@ -286,6 +285,63 @@ def test_quant_random_within_one_fp8_step():
     step = np.exp2(np.floor(np.log2(np.maximum(np.abs(exact), 2.0 ** -6))) - 3)
     assert np.all(np.abs(g - r) <= step + 1e-12)
     assert np.mean(g == r) > 0.99
+
+
+# ------------------------------------------------------------ fp8 operands --
+
+FP8_CASES = [  # M, N, K, opts, expected path
+    (300, 528, 256, {"cta_pair": 2}, 1), (300, 528, 256, {"cta_pair": 1, "max_ctas": 20}, 1),
+    (777, 1296, 336, None, 1), (96, 1040, 512, None, 1), (7, 40, 24, None, 3),
+    (300, 520, 200, None, 3)]
+
+
+@pytest.mark.parametrize("M,N,K,opts,want_path", FP8_CASES)
+def test_fp8_operands_integer_bit_exact(M, N, K, opts, want_path):
+    # fp8 e4m3 A and B (tcgen05 kind::f8f6f4 on the tensor-core path): integer inputs are exact in
+    # e4m3 and every sum is exact in fp32, so the only rounding is the output's.
+    for bt, ot in ((F32, BF16), (BF16, F32)):
+        p = gen.integer_problem(M, N, K, E4M3, bt, seed=M + K)
+        out = torch.empty(M, N, dtype={BF16: torch.bfloat16, F32: torch.float32}[ot], device="cuda")
+        path = fg.fgemm_bias_relu_ex(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, bt), out, M, N, K,
+                                     dtype_word(E4M3, bt, ot), opts=opts)
+        torch.cuda.synchronize()
+        assert path == want_path
+        ref = oracle.bias_relu(p.A, p.B, p.bias, M, N, K, E4M3, bt, ot)
+        got = down(out, ot)
+        if not np.array_equal(got, ref.out):
+            bad = np.argwhere(got != ref.out)
+            pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
+
+
+def test_fp8_operands_quantized_output_bit_exact():
+    M, N, K = 300, 528, 256
+    p = gen.integer_problem(M, N, K, E4M3, F32, seed=9)
+    out = torch.empty(M, N, dtype=torch.uint8, device="cuda")
+    fg.fgemm_bias_relu_quant(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32), out, M, N, K,
+                             fg.E4M3 | fg.BIAS_F32 | fg.OUT_E4M3, 0.5)
+    torch.cuda.synchronize()
+    ref = oracle.bias_relu_quant(p.A, p.B, p.bias, M, N, K, E4M3, F32, 0.5)
+    assert np.array_equal(out.cpu().numpy(), ref.out)
+
+
+def test_fp8_operands_random_tolerance():
+    M, N, K = 1000, 2064, 2048
+    p = gen.random_problem(M, N, K, E4M3, F32, seed=17, scale=K ** -0.25)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    path = fg.fgemm_bias_relu_ex(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32), out, M, N, K,
+                                 dtype_word(E4M3, F32, BF16))
+    torch.cuda.synchronize()
+    assert path == fg.PATH_TC
+    ref = oracle.bias_relu(p.A, p.B, p.bias, M, N, K, E4M3, F32, BF16)
+    check_close(down(out, BF16), ref, K, BF16, bias64=oracle.decode(p.bias, F32), what="fp8")
+
+
+def test_fp8_operands_refused_where_unsupported():
+    st = fg.call_status("fgemm_addmm_gate", None, None, None, None, None, 4, 4, 4,
+                        fg.E4M3 | fg.BIAS_F32 | fg.OUT_BF16, None)
+    assert st == fg.ERR_UNSUPPORTED_DTYPE
+    st = fg.call_status("fgemm_bias_relu", None, None, None, None, 4, 4, 4, fg.E4M3, None)
+    assert st == fg.ERR_UNSUPPORTED_DTYPE
 
 
 # ----------------------------------------------------------- float tolerance --
@@ -392,7 +448,8 @@ def test_unfused_chain_matches_oracle(inter_f32, gate):
 
 # ------------------------------------------------------------ full-size sampled --
 
-FULL = ["square_4096", "glu_gate_1024x21568x4096", "ffn_up_8192x14336x4096", "skinny_M1_8192",
+FULL = ["square_4096", "glu_gate_1024x21568x4096", "ffn_up_8192x14336x4096", "ffn_up_fp8_8192x14336x4096",
+        "square_fp8_4096", "skinny_M1_8192",
         "skinny_M16_8192", "skinny_M64_8192", "skinny_M128_8192", "glu_gate_1024x21568x256",
         "glu_gate_1024x21568x512", "glu_gate_1024x21568x1024"]
 
