@@ -387,6 +387,42 @@ def test_quant_closed_forms(oracle_mod):
     assert np.array_equal(oracle_mod.decode(r.out, E4M3), np.tile([0.0, 0.0, 6.0, 192.0, 448.0], (M, 1)))
 
 
+
+# ------------------------------------------------------------- fp8 operands --
+
+@pytest.mark.parametrize("K", [1, 17, 64])
+def test_e4m3_operands_against_library_decode(oracle_mod, K):
+    # fp8 operands ("Optimizing GEMM + Activation on CDNA4 with TLX", "Future Work": half the
+    # operand bytes): every finite e4m3 pattern is drawn, decoded by torch's own float8 type, and
+    # the fp64 matmul of the decoded values is exact here (a product of two e4m3 values has at most
+    # 8 significant bits between 2^-18 and 2^17, and 64 of them sum exactly in 53 bits).
+    M, N = 7, 12
+    rng = np.random.default_rng(300 + K)
+    finite = np.array([p for p in range(256) if p & 0x7F != 0x7F], dtype=np.uint8)
+    A = rng.choice(finite, (M, K))
+    B = rng.choice(finite, (K, N))
+    bias = rng.standard_normal(N).astype(np.float32)
+    r = oracle_mod.bias_relu(A, B, bias, M, N, K, E4M3, F32, F32)
+    dec = lambda x: torch.from_numpy(x.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    want = np.maximum(dec(A) @ dec(B) + bias.astype(np.float64)[None, :], 0.0)
+    assert np.array_equal(r.ref, want)
+    # and the one rounding to fp32 is round-to-nearest of that exact value
+    assert np.array_equal(r.out, want.astype(np.float32))
+
+
+def test_e4m3_operands_transposed_b_is_caught(oracle_mod):
+    # a square B and its transpose give different products: the oracle must read B as K x N
+    M = N = K = 6
+    rng = np.random.default_rng(310)
+    finite = np.array([p for p in range(256) if p & 0x7F != 0x7F], dtype=np.uint8)
+    A, B = rng.choice(finite, (M, K)), rng.choice(finite, (K, N))
+    bias = np.zeros(N, dtype=np.float32)
+    dec = lambda x: torch.from_numpy(x.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    r = oracle_mod.gemm_epilogue(A, B, bias, M, N, K, E4M3, F32, F32, oracle_mod.EPI_LINEAR)
+    assert np.array_equal(r.ref, dec(A) @ dec(B))
+    assert not np.array_equal(r.ref, dec(A) @ dec(B).T)
+
+
 # --------------------------------------------------------- negative controls --
 
 def _pins_pass(oracle_mod, mutant):
