@@ -464,7 +464,10 @@ def run_sweep(args):
             variants = [None] + [{"split_k": s, "skinny_tiles": t, "stages": g}
                                  for t in (1, 2) for s in (2, 4, 8) for g in (3, 4, 6)]
         else:
-            variants = [None, {"tail_split": 1}, {"cta_pair": 1}, {"cta_pair": 1, "tail_split": 1}]
+            variants = [None, {"tail_split": 1}, {"cta_pair": 1}, {"cta_pair": 1, "tail_split": 1},
+                        {"bias_init": 1}]
+        if args.sweep_variants:
+            variants = json.loads(args.sweep_variants)
         for opts in variants:
             g = (opts or {}).get("group_m")
             try:
@@ -509,6 +512,8 @@ def main():
                     help="unfused: time the GEMM -> elementwise chain instead (traffic comparison)")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-workloads", default="")
+    ap.add_argument("--sweep-variants", default="",
+                    help='JSON list of fgemm_opts dicts (null = defaults) replacing the sweep\'s own')
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -172,7 +172,8 @@ int validate(const Call& c, bool* nothing) {
     if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
         o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
-        o.inject_stall < 0 || o.inject_stall > 1)
+        o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 1 ||
+        o.full_last_n < 0 || o.full_last_n > 1)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -193,6 +194,7 @@ struct TcPlan {
   int units;       // persistent CTAs (or CTA pairs)
   int resident;    // pairs that can be resident at once (pair mode), else 0
   int tail_split, full_tiles, num_items;
+  int last_width, gran;  // width of the last column of tiles, and the width it is rounded up to
 };
 
 TcPlan plan_tc(const Call& c, DeviceInfo* d) {
@@ -233,6 +235,17 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
   t.tail_split = split;
   t.full_tiles = t.num_tiles - (split > 1 ? rem : 0);
   t.num_items = t.full_tiles + (t.num_tiles - t.full_tiles) * split;
+  // Non-power-of-two last tile ("Optimizing GEMM + Activation on CDNA4 with TLX", "Future Work":
+  // N = 21568 = 84 x 256 + 64 leaves a ragged last tile): the MMA's N can be any multiple of 16, so
+  // the last column of tiles is cut down to the columns left, rounded up to the smallest width
+  // that still fills whole 128-byte B boxes on each CTA and whole output staging rows.
+  const int box_cols = 128 / static_cast<int>(elem_bytes(c.t.ab));
+  const int out_cols = 128 / static_cast<int>(elem_bytes(c.t.out));
+  t.gran = (t.pair ? 2 : 1) * box_cols;
+  if (t.gran < out_cols) t.gran = out_cols;
+  const int left = static_cast<int>(c.N - static_cast<int64_t>(t.tiles_n - 1) * BN);
+  t.last_width = (left + t.gran - 1) / t.gran * t.gran;
+  if (t.last_width > BN || (c.opts && c.opts->full_last_n)) t.last_width = BN;
   return t;
 }
 
@@ -302,6 +315,9 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.full_tiles = t.full_tiles;
   p.tail_split = t.tail_split;
   p.num_items = t.num_items;
+  p.last_width = t.last_width;
+  p.gran = t.gran;
+  p.bias_init = (c.opts && c.opts->bias_init && c.epi != EPI_NONE) ? 1 : 0;
   p.group = (c.opts && c.opts->group_m > 0) ? c.opts->group_m : 8;
   p.ab_bf16 = c.t.ab == ELEM_BF16;
   p.ab_f8 = c.t.ab == ELEM_E4M3;
@@ -613,6 +629,7 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
     info->tiles = t.num_tiles;
     info->work_items = t.num_items;
     info->tail_split = t.tail_split;
+    info->last_tile_n = t.last_width;
     info->resident_pairs = t.resident;
   } else if (path == FGEMM_PATH_SKINNY) {
     const SkPlan s = plan_skinny(c, d);

@@ -22,6 +22,11 @@ struct TcParams {
   // (the last, partial round of the persistent grid) are each cut into `tail_split` pieces along N
   // (256 / tail_split columns each) so that the last round takes a fraction of a tile's time.
   int full_tiles, tail_split, num_items;
+  // The last column of tiles is narrowed to `last_width` columns (the columns left of N, rounded up
+  // to `gran`, the smallest width one CTA (pair) can stage and store); pieces of it that start at
+  // or past that width are `gran` wide and store nothing.
+  int last_width, gran;
+  int bias_init;   // 1: the accumulator starts at the bias (written into TMEM before the K loop)
   int ab_bf16;     // operand (and Y) type: 0 = f16, 1 = bf16
   int ab_f8;       // 1: A and B are fp8 e4m3 (kind::f8f6f4 MMAs, 128-element K blocks)
   int bias_type;   // Elem of the bias

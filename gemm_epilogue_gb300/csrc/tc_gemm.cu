@@ -101,6 +101,10 @@ __device__ __forceinline__ Work work_of(const TcParams& p, int item) {
   tile_of(tile, p.tiles_m, p.tiles_n, p.group, w.tm, w.tn);
   w.width = BN / split;
   w.col0 = w.tn * BN + piece * w.width;
+  if (w.tn == p.tiles_n - 1) {  // ragged last column of tiles: only as wide as N needs
+    const int left = p.last_width - piece * w.width;
+    if (left < w.width) w.width = left > 0 ? left : p.gran;
+  }
   return w;
 }
 
@@ -285,8 +289,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(width >> 3) << 17);
         const int b = it & 1;
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
-        if (!mbar_wait(bar(BAR_ACC_EMPTY + b), acc_phase ^ 1u, abort_flag, tmo, p.err,
-                       SITE_MMA_ACC_EMPTY))
+        // Buffer b is free once the epilogue has read its previous tile; with the bias-initialised
+        // accumulator the epilogue has also written this tile's bias row into it (one more phase).
+        const uint32_t want = p.bias_init ? acc_phase : (acc_phase ^ 1u);
+        if (!mbar_wait(bar(BAR_ACC_EMPTY + b), want, abort_flag, tmo, p.err, SITE_MMA_ACC_EMPTY))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
@@ -302,10 +308,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int k = 0; k < KB_ELEMS / KSTEP; ++k) {  // 32 bytes of K per MMA
             const uint64_t ad = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
             const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, p.b_lbo, p.b_sbo);
+            const uint32_t acc = (p.bias_init | kb | k) != 0 ? 1u : 0u;
             if constexpr (F8)
-              umma_f8_cg<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              umma_f8_cg<CG>(d_tmem, ad, bd, idesc, acc);
             else
-              umma_f16_cg<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              umma_f16_cg<CG>(d_tmem, ad, bd, idesc, acc);
           }
           umma_commit_cg<CG>(bar(BAR_EMPTY + stage), kPair);  // stage free (both CTAs) once read
           if (++stage == STAGES) {
@@ -329,6 +336,45 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool out_bf = p.out_type == ELEM_BF16;
     const bool y_bf = p.ab_bf16 != 0;
     const uint64_t pol_out = policy_evict_first();
+    const bool add_bias = !p.bias_init;  // else the accumulator already holds the bias
+    // Bias-initialised accumulator ("Optimizing GEMM + Activation on CDNA4 with TLX", V4: the
+    // accumulator starts at the bias instead of zero): this warp writes bias[col] into every lane
+    // (row) of its quarter and every column of its half of buffer bb for work item t, then hands
+    // the buffer to the MMA warp, whose first MMA of the tile accumulates onto it.
+    auto release_acc = [&](int t, int bb) {
+      if (p.bias_init && t < p.num_items) {
+        const Work w = work_of(p, t);
+        const uint32_t ta =
+            tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(bb * BN);
+#pragma unroll 1
+        for (int c = cbeg; c < cbeg + BN / 2 && c < w.width; c += 16) {
+          float b0[8], b1[8];
+          load_bias<8>(p, w.col0 + c, b0);
+          load_bias<8>(p, w.col0 + c + 8, b1);
+          uint32_t r[16];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            r[e] = __float_as_uint(b0[e]);
+            r[8 + e] = __float_as_uint(b1[e]);
+          }
+          __syncwarp();  // tcgen05.st is warp-collective
+          tmem_st16(ta + static_cast<uint32_t>(c), r);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(lead_bar(BAR_ACC_EMPTY + bb));  // the even CTA's MMA waits on it
+        else
+          mbar_arrive(bar(BAR_ACC_EMPTY + bb));
+      }
+    };
+    if (p.bias_init) {  // first use of both buffers
+      release_acc(unit, 0);
+      release_acc(unit + units, 1);
+    }
     int it = 0;
     if constexpr (YS) {
       // Gate with Y staged by TMA: the warp's 32 x 128 block of Y lands in its 8 KB region (two
@@ -396,7 +442,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                          : "r"(addr)
                          : "memory");
             float bv[G];
-            load_bias<G>(p, col0 + g * G, bv);
+            if (add_bias) {
+              load_bias<G>(p, col0 + g * G, bv);
+            } else {
+#pragma unroll
+              for (int e = 0; e < G; ++e) bv[e] = 0.f;
+            }
             uint32_t packed[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -422,14 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (lane == 0) bulk_commit();
         // This warp has finished reading accumulator b: release it to the MMA warp.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          if (PAIR)
-            mbar_arrive_cluster(lead_bar(BAR_ACC_EMPTY + b));
-          else
-            mbar_arrive(bar(BAR_ACC_EMPTY + b));
-        }
+        release_acc(t + 2 * units, b);
         // Prefetch the Y block of this CTA's next work item (its main loop runs meanwhile).
         y_issued = (t + units < p.num_items) ? issue_y(t + units) : false;
       }
@@ -477,7 +521,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int gi = 0; gi < 4; ++gi) {
               const int g = 4 * h + gi;  // 16-column granule within the 128-column row
               float bv[16];
-              load_bias<16>(p, col0 + g * 16, bv);
+              if (add_bias) {
+                load_bias<16>(p, col0 + g * 16, bv);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) bv[e] = 0.f;
+              }
               uint32_t packed[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -541,12 +590,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           float bv[G];
-          if constexpr (EPI != EPI_NONE) load_bias<G>(p, col0 + g * G, bv);
+          const bool use_bias = EPI != EPI_NONE && add_bias;
+          if (use_bias) load_bias<G>(p, col0 + g * G, bv);
           float v[G];
 #pragma unroll
           for (int e = 0; e < G; ++e) {
             v[e] = __uint_as_float(acc[g * G + e]);
-            if constexpr (EPI != EPI_NONE) v[e] += bv[e];  // bias once, after the full sum
+            if (use_bias) v[e] += bv[e];  // bias once, after the full sum
           }
           if constexpr (EPI == EPI_RELU) {
 #pragma unroll
@@ -597,14 +647,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }  // OUT_BYTES != 1
       }
       // This warp has finished reading accumulator b: release it to the MMA warp.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR)
-          mbar_arrive_cluster(lead_bar(BAR_ACC_EMPTY + b));  // the even CTA's MMA waits on it
-        else
-          mbar_arrive(bar(BAR_ACC_EMPTY + b));
-      }
+      release_acc(t + 2 * units, b);
     }
     }
     if (lane == 0) bulk_wait<0>();

@@ -105,6 +105,12 @@ typedef struct {
                        on that stage can never complete; it expires after timeout_ms, the kernel
                        drains and exits, and fgemm_device_status reports FGEMM_ERR_TIMEOUT.
                        The output of that call is undefined.  Tensor-core and skinny paths. */
+  int bias_init;  /* tensor-core path: 1 = start each tile's accumulator at the bias (written into
+                     tensor memory before the K loop) instead of adding it after the reduction;
+                     same result up to the rounding order ("Optimizing GEMM + Activation on CDNA4
+                     with TLX", V4).  Ignored by the other paths and by the plain GEMM. */
+  int full_last_n; /* tensor-core path, diagnostic: 1 = run the last column of tiles at the full
+                      256-column width instead of narrowing it to the columns left of N */
   int reserved;
 } fgemm_opts;
 
@@ -221,6 +227,9 @@ typedef struct {
   int tail_split;     /* pieces per tile of the last round (1 = whole tiles); on the skinny
                          path: 128-column tiles per CTA */
   int resident_pairs; /* CTA pairs resident at once (pair mode; 0 otherwise) */
+  int last_tile_n;    /* tensor-core path: MMA width of the last column of tiles (the columns left
+                         of N rounded up to what one CTA or pair stages and stores; 256 when N is a
+                         multiple of 256); 0 on other paths */
   int reserved;
 } fgemm_plan_info;
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,

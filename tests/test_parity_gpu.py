@@ -344,6 +344,112 @@ def test_fp8_operands_refused_where_unsupported():
     assert st == fg.ERR_UNSUPPORTED_DTYPE
 
 
+# ------------------------------------- narrowed last tile, bias-initialised accumulator --
+
+@pytest.mark.parametrize("N", [264, 320, 328, 384, 392, 448, 456, 504, 512])
+@pytest.mark.parametrize("pair", [1, 2])
+def test_narrowed_last_tile_integer_bit_exact(N, pair):
+    # "Optimizing GEMM + Activation on CDNA4 with TLX", "Future Work": a last N tile narrower than
+    # 256 columns.  Every remainder class of N mod 256 against the narrowing granule (64 columns on
+    # one CTA, 128 on a pair), with the gate; the full-width diagnostic must give the same bits.
+    M, K = 300, 136
+    gran = 64 * pair
+    left = N - (N - 1) // 256 * 256
+    want_width = min(256, -(-left // gran) * gran)
+    for gate in (False, True):
+        p = gen.integer_problem(M, N, K, F16, F16, seed=N + pair, gate=gate)
+        opts = {"path": fg.PATH_TC, "cta_pair": pair}
+        plan = fg.fgemm_plan(up(p.A, F16), up(p.B, F16), up(p.bias, F16),
+                             up(p.Y, F16) if gate else None,
+                             torch.empty(M, N, dtype=torch.float16, device="cuda"), M, N, K, fg.F16,
+                             gate=gate, opts=opts)
+        assert plan["last_tile_n"] == want_width
+        out, path = run_fused(p, M, N, K, F16, F16, F16, gate=gate, opts=opts)
+        assert path == fg.PATH_TC
+        ref = oracle_run(p, M, N, K, F16, F16, F16, gate=gate)
+        assert np.array_equal(down(out, F16), ref.out)
+        full, _ = run_fused(p, M, N, K, F16, F16, F16, gate=gate, opts=dict(opts, full_last_n=1))
+        assert torch.equal(full, out)
+
+
+BIAS_INIT_CASES = [  # M, N, K, opts
+    (300, 520, 200, {"cta_pair": 2}), (300, 520, 200, {"cta_pair": 1}),
+    (700, 1800, 200, {"cta_pair": 1, "max_ctas": 44}), (700, 1800, 200, {"cta_pair": 2, "max_ctas": 20}),
+    (129, 264, 8, None), (1, 8, 64, None)]
+
+
+def _same_values(got_bits, ref_bits, t):
+    """Equal as numbers (-0 == +0), every element."""
+    return np.array_equal(oracle.decode(got_bits, t), oracle.decode(ref_bits, t))
+
+
+@pytest.mark.parametrize("M,N,K,opts", BIAS_INIT_CASES)
+def test_bias_init_integer_exact(M, N, K, opts):
+    # "Optimizing GEMM + Activation on CDNA4 with TLX", V4: the accumulator starts at the bias.
+    # With integer inputs every partial sum is exact in either order, so each epilogue must match
+    # the oracle (bias added once after the sum) exactly; covers tail pieces, the narrowed last
+    # tile, one-K-block tiles and both CTA modes.  Values are compared, so that an exact zero may
+    # carry either sign (the sign of a zero sum depends on the order of the terms).
+    o = dict(opts or {}, bias_init=1, path=fg.PATH_TC)
+    for gate in (False, True):
+        p = gen.integer_problem(M, N, K, BF16, BF16, seed=M + N + K + gate, gate=gate)
+        out, path = run_fused(p, M, N, K, BF16, BF16, BF16, gate=gate, opts=o)
+        assert path == fg.PATH_TC
+        assert _same_values(down(out, BF16), oracle_run(p, M, N, K, BF16, BF16, BF16, gate=gate).out, BF16)
+    # fp32 bias and output
+    p = gen.integer_problem(M, N, K, F16, F32, seed=M + 3)
+    out, _ = run_fused(p, M, N, K, F16, F32, F32, opts=o)
+    assert _same_values(down(out, F32), oracle_run(p, M, N, K, F16, F32, F32).out, F32)
+    # residual add
+    p = gen.integer_problem(M, N, K, F16, F16, seed=M + 5, gate=True)
+    out = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    fg.fgemm_bias_residual_relu_ex(up(p.A, F16), up(p.B, F16), up(p.bias, F16), up(p.Y, F16), out,
+                                   M, N, K, fg.F16, opts=o)
+    torch.cuda.synchronize()
+    ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, F16, F16, F16)
+    assert _same_values(down(out, F16), ref.out, F16)
+    # quantized fp8 output (N a multiple of 16)
+    if N % 16 == 0:
+        p = gen.integer_problem(M, N, K, BF16, F32, seed=M + 7)
+        got, path = _run_quant(p, M, N, K, BF16, F32, 0.25, o)
+        assert path == fg.PATH_TC
+        assert _same_values(got, oracle.bias_relu_quant(p.A, p.B, p.bias, M, N, K, BF16, F32, 0.25).out, E4M3)
+    # fp8 operands (K and N multiples of 16)
+    if N % 16 == 0 and K % 16 == 0:
+        p = gen.integer_problem(M, N, K, E4M3, F32, seed=M + 9)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        fg.fgemm_bias_relu_ex(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32), out, M, N, K,
+                              dtype_word(E4M3, F32, BF16), opts=o)
+        torch.cuda.synchronize()
+        assert _same_values(down(out, BF16),
+                            oracle.bias_relu(p.A, p.B, p.bias, M, N, K, E4M3, F32, BF16).out, BF16)
+
+
+@pytest.mark.parametrize("gate", [False, True])
+def test_bias_init_random_tolerance(gate):
+    # random inputs: bias first changes only the rounding order of the fp32 sum
+    M, N, K = 513, 1288, 1024
+    p = gen.random_problem(M, N, K, F16, F16, seed=18, gate=gate)
+    out, path = run_fused(p, M, N, K, F16, F16, F16, gate=gate, opts={"bias_init": 1})
+    assert path == fg.PATH_TC
+    ref = oracle_run(p, M, N, K, F16, F16, F16, gate=gate)
+    check_close(down(out, F16), ref, K, F16, Y64=oracle.decode(p.Y, F16) if gate else None,
+                bias64=oracle.decode(p.bias, F16), what="bias-init")
+
+
+def test_bias_init_full_size_gate_sampled_rows():
+    w = gen.WORKLOADS["glu_gate_1024x21568x4096"]
+    x = gen.make(w)
+    out, path = run_fused(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, gate=True,
+                          opts={"bias_init": 1})
+    assert path == fg.PATH_TC
+    rows = sample_rows(w.M)
+    ref = oracle_run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, gate=True, rows=rows)
+    check_close(down(out, w.out_type)[rows], ref, w.K, w.out_type,
+                Y64=oracle.decode(x.Y[rows], w.ab_type), bias64=oracle.decode(x.bias, w.bias_type),
+                what="gate bias-init")
+
+
 # ----------------------------------------------------------- float tolerance --
 
 def test_small_ragged_workload_tc_and_generic():
