@@ -42,10 +42,14 @@ constexpr uint32_t EPI_BUF_BYTES = 32 * 128;     // 32 rows x 128 bytes
 constexpr uint32_t TMEM_COLS = 512;
 
 // YS: the gate's Y is staged through shared memory by TMA (16-bit outputs), which costs one ring
-// stage of shared memory for a 64 KB Y / output block.
-template <bool PAIR, bool YS = false>
+// stage of shared memory for a 64 KB Y / output block.  YB = 2 (CTA pairs, short K loops) keeps two
+// such blocks per epilogue warp, so that Y is fetched two tiles ahead, in exchange for three stages
+// of the ring: with few K blocks per tile the epilogue's streams of Y and out, not the main loop,
+// set the pace.
+template <bool PAIR, bool YS = false, int YB = 1>
 struct Cfg {
-  static constexpr int STAGES = PAIR ? (YS ? 5 : 6) : (YS ? 3 : 4);
+  static_assert(YB == 1 || (YB == 2 && PAIR && YS), "double Y buffers: staged Y on CTA pairs");
+  static constexpr int STAGES = PAIR ? (YS ? (YB == 2 ? 3 : 5) : 6) : (YS ? 3 : 4);
   static constexpr int B_BOXES = PAIR ? 2 : 4;                 // 64-column B boxes per CTA
   static constexpr uint32_t B_STAGE_BYTES = B_BOXES * B_BOX_BYTES;
   static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
@@ -55,9 +59,10 @@ struct Cfg {
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
   static constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
   // per epilogue warp: its 32 x 128 block of Y and results (YS), or one 32-row staging buffer
-  static constexpr uint32_t EPI_WARP_BYTES = YS ? 2 * EPI_BUF_BYTES : EPI_BUF_BYTES;
+  static constexpr uint32_t Y_BLOCK_BYTES = 2 * EPI_BUF_BYTES;  // a warp's 32 x 128 block of Y
+  static constexpr uint32_t EPI_WARP_BYTES = YS ? YB * Y_BLOCK_BYTES : EPI_BUF_BYTES;
   static constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * EPI_WARP_BYTES;
-  static constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + barriers + 1024-B alignment slack
+  static constexpr uint32_t SMEM_BYTES = SMEM_BAR + 512 + 1024;  // + barriers + 1024-B alignment slack
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -68,9 +73,9 @@ constexpr int BAR_EMPTY = MAX_STAGES;
 constexpr int BAR_ACC_FULL = 2 * MAX_STAGES;
 constexpr int BAR_ACC_EMPTY = 2 * MAX_STAGES + 2;
 constexpr int BAR_MMA_DONE = 2 * MAX_STAGES + 4;
-constexpr int BAR_Y = 2 * MAX_STAGES + 5;  // one per epilogue warp (gate with staged Y)
-constexpr uint32_t OFF_TMEM_SLOT = 224;  // after the 25 barriers
-constexpr uint32_t OFF_ABORT = 232;
+constexpr int BAR_Y = 2 * MAX_STAGES + 5;  // one per epilogue warp and Y block (staged Y)
+constexpr uint32_t OFF_TMEM_SLOT = 272;  // after the 33 barriers
+constexpr uint32_t OFF_ABORT = 280;
 
 // wait sites recorded with a timeout
 enum { SITE_PROD_EMPTY = 1, SITE_MMA_ACC_EMPTY, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN,
@@ -146,7 +151,7 @@ __device__ __forceinline__ void load_bias(const TcParams& p, int col, float (&b)
   }
 }
 
-template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false>
+template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmY,
@@ -156,7 +161,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int NG = CH / G;           // granules per chunk (8)
   // the gate's Y and the residual R are staged the same way (16-bit outputs)
   constexpr bool YS = (EPI == EPI_GATE || EPI == EPI_RESID) && (OUT_BYTES == 2);
-  using C = Cfg<PAIR, YS>;
+  using C = Cfg<PAIR, YS, YB>;
   // Operand element size: one stage holds one 128-byte swizzle row of K per A row (64 16-bit or
   // 128 fp8 elements) and B as boxes of (128 bytes of N) x (that K); the stage byte counts and
   // the ring are the same for both.
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar(BAR_ACC_EMPTY + b), (PAIR ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(bar(BAR_MMA_DONE), 1);
-    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(bar(BAR_Y + w), 1);
+    for (int w = 0; w < YB * EPI_WARPS; ++w) mbar_init(bar(BAR_Y + w), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -377,12 +382,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     int it = 0;
     if constexpr (YS) {
-      // Gate with Y staged by TMA: the warp's 32 x 128 block of Y lands in its 8 KB region (two
-      // 128-byte-swizzled 32 x 64 chunks) while the tile's main loop still runs; the epilogue reads
-      // y from there, writes the result over it, and stores each chunk with one TMA store.
-      const uint32_t ybar = bar(BAR_Y + ew);
-      uint32_t y_par = 0;
-      auto issue_y = [&](int t) -> bool {  // warp-uniform result
+      // Gate with Y staged by TMA: the warp's 32 x 128 block of Y lands in one of its YB 8 KB
+      // blocks (two 128-byte-swizzled 32 x 64 chunks) while earlier tiles are still computed; the
+      // epilogue reads y from there, writes the result over it, and stores each chunk with one TMA
+      // store.  Work item number `it` of this CTA uses block it % YB.
+      auto ybar = [&](int yb) { return bar(BAR_Y + yb * EPI_WARPS + ew); };
+      uint32_t y_par = 0, y_issued = 0;  // bit yb: parity to wait for / a load is in flight
+      auto issue_y = [&](int t, int yb) -> bool {  // warp-uniform result
         const Work w = work_of(p, t);
         const int r0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + 32 * q;
         if (r0 >= p.M) return false;
@@ -392,13 +398,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (nchunks == 0) return false;
         if (lane == 0) {
           bulk_wait_read<0>();  // the stores that last read this region are done with it
-          mbar_arrive_expect_tx(ybar, static_cast<uint32_t>(nchunks) * EPI_BUF_BYTES);
+          const uint32_t yblk = ebuf + static_cast<uint32_t>(yb) * C::Y_BLOCK_BYTES;
+          mbar_arrive_expect_tx(ybar(yb), static_cast<uint32_t>(nchunks) * EPI_BUF_BYTES);
           for (int j = 0; j < nchunks; ++j)
-            tma_load_2d(ebuf + j * EPI_BUF_BYTES, &tmY, ybar, w.col0 + cbeg + j * CH, r0, pol_out);
+            tma_load_2d(yblk + j * EPI_BUF_BYTES, &tmY, ybar(yb), w.col0 + cbeg + j * CH, r0, pol_out);
         }
         return true;
       };
-      bool y_issued = (unit < p.num_items) ? issue_y(unit) : false;
+      for (int j = 0; j < YB; ++j)
+        if (unit + j * units < p.num_items && issue_y(unit + j * units, j)) y_issued |= 1u << j;
       for (int t = unit; t < p.num_items; t += units, ++it) {
         const Work wk = work_of(p, t);
         const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = wk.col0;
@@ -411,9 +419,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
           break;
         tc_fence_after();
-        if (y_issued) {
-          if (!mbar_wait(ybar, y_par, abort_flag, tmo, p.err, SITE_EPI_Y)) break;
-          y_par ^= 1u;
+        const int yb = YB == 1 ? 0 : (it & 1);
+        if ((y_issued >> yb) & 1u) {
+          if (!mbar_wait(ybar(yb), (y_par >> yb) & 1u, abort_flag, tmo, p.err, SITE_EPI_Y)) break;
+          y_par ^= 1u << yb;
+          y_issued &= ~(1u << yb);
         }
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
@@ -430,7 +440,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld32(taddr, a1, c * CH + 32);
             tmem_ld_wait();
           }
-          const uint32_t sb = ebuf + static_cast<uint32_t>(c - cbeg / CH) * EPI_BUF_BYTES;
+          const uint32_t sb = ebuf + static_cast<uint32_t>(yb) * C::Y_BLOCK_BYTES +
+                              static_cast<uint32_t>(c - cbeg / CH) * EPI_BUF_BYTES;
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             // 128-byte swizzle: granule g of row `lane` sits at slot g ^ (lane & 7)
@@ -474,11 +485,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) bulk_commit();
         // This warp has finished reading accumulator b: release it to the MMA warp.
         release_acc(t + 2 * units, b);
-        // Prefetch the Y block of this CTA's next work item (its main loop runs meanwhile).
-        y_issued = (t + units < p.num_items) ? issue_y(t + units) : false;
+        // Prefetch into this block the Y of the work item YB items ahead (main loops run meanwhile).
+        if (t + YB * units < p.num_items && issue_y(t + YB * units, yb)) y_issued |= 1u << yb;
       }
       // After an abort a prefetched Y block may still be landing: wait for it (bounded).
-      if (y_issued) drain_wait(ybar, y_par, tmo, p.err);
+      for (int j = 0; j < YB; ++j)
+        if ((y_issued >> j) & 1u) drain_wait(ybar(j), (y_par >> j) & 1u, tmo, p.err);
     } else {
     for (int t = unit; t < p.num_items; t += units, ++it) {
       const Work wk = work_of(p, t);
@@ -665,12 +677,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false>
+template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                        const CUtensorMap& y, const TcParams& p, int grid, cudaStream_t s) {
-  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8>;
+  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB>;
   constexpr uint32_t smem =
-      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2>::SMEM_BYTES;
+      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB>::SMEM_BYTES;
   static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -731,6 +743,9 @@ template <int EPI, int OUT_BYTES, bool F8 = false>
 cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                                const CUtensorMap& y, const TcParams& p, int grid, bool pair,
                                cudaStream_t s) {
+  if constexpr ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2 && !F8) {
+    if (pair && p.y_blocks == 2) return launch_one<EPI, OUT_BYTES, true, false, 2>(a, b, o, y, p, grid, s);
+  }
   return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, p, grid, s)
               : launch_one<EPI, OUT_BYTES, false, F8>(a, b, o, y, p, grid, s);
 }

@@ -111,6 +111,10 @@ typedef struct {
                      with TLX", V4).  Ignored by the other paths and by the plain GEMM. */
   int full_last_n; /* tensor-core path, diagnostic: 1 = run the last column of tiles at the full
                       256-column width instead of narrowing it to the columns left of N */
+  int y_blocks;   /* tensor-core path, gate and residual with 16-bit outputs on CTA pairs: blocks of
+                     the second M x N operand staged per epilogue warp; 0 = automatic (2 when
+                     K <= 256, else 1), 1 = one tile ahead (5-stage ring), 2 = two tiles ahead
+                     (3-stage ring).  Ignored elsewhere. */
   int reserved;
 } fgemm_opts;
 
@@ -230,6 +234,7 @@ typedef struct {
   int last_tile_n;    /* tensor-core path: MMA width of the last column of tiles (the columns left
                          of N rounded up to what one CTA or pair stages and stores; 256 when N is a
                          multiple of 256); 0 on other paths */
+  int y_blocks;       /* tensor-core path: staged Y blocks per epilogue warp (see fgemm_opts) */
   int reserved;
 } fgemm_plan_info;
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,

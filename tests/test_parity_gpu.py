@@ -378,6 +378,36 @@ BIAS_INIT_CASES = [  # M, N, K, opts
     (129, 264, 8, None), (1, 8, 64, None)]
 
 
+Y_BLOCK_CASES = [  # M, N, K, max_ctas (0 = every SM)
+    (300, 520, 200, 0), (700, 1800, 200, 20), (1000, 2056, 1096, 0), (513, 1288, 64, 12)]
+
+
+@pytest.mark.parametrize("M,N,K,max_ctas", Y_BLOCK_CASES)
+@pytest.mark.parametrize("y_blocks", [1, 2])
+def test_staged_y_blocks_integer_bit_exact(M, N, K, max_ctas, y_blocks):
+    # The gate's Y (and the residual's R) staged one or two tiles ahead per epilogue warp, on CTA
+    # pairs; tail pieces and the narrowed last tile included.
+    opts = {"path": fg.PATH_TC, "cta_pair": 2, "max_ctas": max_ctas, "y_blocks": y_blocks}
+    p = gen.integer_problem(M, N, K, F16, F16, seed=M + K + y_blocks, gate=True)
+    plan = fg.fgemm_plan(up(p.A, F16), up(p.B, F16), up(p.bias, F16), up(p.Y, F16),
+                         torch.empty(M, N, dtype=torch.float16, device="cuda"), M, N, K, fg.F16,
+                         gate=True, opts=opts)
+    assert plan["y_blocks"] == y_blocks
+    auto = fg.fgemm_plan(up(p.A, F16), up(p.B, F16), up(p.bias, F16), up(p.Y, F16),
+                         torch.empty(M, N, dtype=torch.float16, device="cuda"), M, N, K, fg.F16,
+                         gate=True, opts={"cta_pair": 2})
+    assert auto["y_blocks"] == (2 if K <= 256 else 1)
+    out, path = run_fused(p, M, N, K, F16, F16, F16, gate=True, opts=opts)
+    assert path == fg.PATH_TC
+    assert np.array_equal(down(out, F16), oracle_run(p, M, N, K, F16, F16, F16, gate=True).out)
+    res = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    fg.fgemm_bias_residual_relu_ex(up(p.A, F16), up(p.B, F16), up(p.bias, F16), up(p.Y, F16), res,
+                                   M, N, K, fg.F16, opts=opts)
+    torch.cuda.synchronize()
+    ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, F16, F16, F16)
+    assert np.array_equal(down(res, F16), ref.out)
+
+
 def _same_values(got_bits, ref_bits, t):
     """Equal as numbers (-0 == +0), every element."""
     return np.array_equal(oracle.decode(got_bits, t), oracle.decode(ref_bits, t))
