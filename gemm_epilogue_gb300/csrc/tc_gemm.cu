@@ -113,42 +113,30 @@ __device__ __forceinline__ Work work_of(const TcParams& p, int item) {
   return w;
 }
 
-// Bias values of columns col .. col+G-1 as fp32 (zeros past N; N is a multiple of G here).
-template <int G>
-__device__ __forceinline__ void load_bias(const TcParams& p, int col, float (&b)[G]) {
-  if (col >= p.N) {
-#pragma unroll
-    for (int e = 0; e < G; ++e) b[e] = 0.f;
-    return;
-  }
+// Bias of the 128 columns [col, col + 128) that one epilogue warpgroup owns: lane l holds columns
+// col + 4l .. col + 4l + 3 as fp32 (zeros past N; N is a multiple of 8 here).  One coalesced load
+// per warp and work item, issued before the accumulator wait so that its latency is hidden.
+__device__ __forceinline__ void load_bias_quad(const TcParams& p, int col, float (&b)[4]) {
+  const int c = col + 4 * static_cast<int>(threadIdx.x & 31);
+  b[0] = b[1] = b[2] = b[3] = 0.f;
+  if (c >= p.N) return;
   if (p.bias_type == ELEM_F32) {
-    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + col);
-#pragma unroll
-    for (int v = 0; v < G / 4; ++v) {
-      const float4 f = __ldg(src + v);
-      b[4 * v + 0] = f.x; b[4 * v + 1] = f.y; b[4 * v + 2] = f.z; b[4 * v + 3] = f.w;
-    }
+    const float4 f = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.bias) + c));
+    b[0] = f.x; b[1] = f.y; b[2] = f.z; b[3] = f.w;
   } else {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.bias) + c));
     const bool bf = p.bias_type == ELEM_BF16;
-    const uint16_t* src = static_cast<const uint16_t*>(p.bias) + col;
-    if constexpr (G >= 8) {
-#pragma unroll
-      for (int v = 0; v < G / 8; ++v) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + v);
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = unpack2(w[k], bf);
-          b[8 * v + 2 * k] = f.x;
-          b[8 * v + 2 * k + 1] = f.y;
-        }
-      }
-    } else {  // G == 4: 4 x 16-bit = 8 bytes
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
-      const float2 f0 = unpack2(u.x, bf), f1 = unpack2(u.y, bf);
-      b[0] = f0.x; b[1] = f0.y; b[2 % G] = f1.x; b[3 % G] = f1.y;
-    }
+    const float2 f0 = unpack2(u.x, bf), f1 = unpack2(u.y, bf);
+    b[0] = f0.x; b[1] = f0.y; b[2] = f1.x; b[3] = f1.y;
   }
+}
+
+// Bias of the G columns j0 .. j0 + G - 1 (warpgroup-local, j0 a multiple of 4) broadcast to every
+// lane from the lanes of load_bias_quad that hold them.  Called by all 32 lanes.
+template <int G>
+__device__ __forceinline__ void bias_granule(const float (&b)[4], int j0, float (&out)[G]) {
+#pragma unroll
+  for (int e = 0; e < G; ++e) out[e] = __shfl_sync(0xffffffffu, b[e & 3], (j0 >> 2) + (e >> 2));
 }
 
 template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1>
@@ -351,17 +339,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         const Work w = work_of(p, t);
         const uint32_t ta =
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(bb * BN);
+        float bq[4];
+        load_bias_quad(p, w.col0 + cbeg, bq);
 #pragma unroll 1
         for (int c = cbeg; c < cbeg + BN / 2 && c < w.width; c += 16) {
-          float b0[8], b1[8];
-          load_bias<8>(p, w.col0 + c, b0);
-          load_bias<8>(p, w.col0 + c + 8, b1);
+          float b16[16];
+          bias_granule<16>(bq, c - cbeg, b16);
           uint32_t r[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            r[e] = __float_as_uint(b0[e]);
-            r[8 + e] = __float_as_uint(b1[e]);
-          }
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(b16[e]);
           __syncwarp();  // tcgen05.st is warp-collective
           tmem_st16(ta + static_cast<uint32_t>(c), r);
         }
@@ -415,6 +401,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
         const int row0 = m0 + 32 * q;
         const bool rows_live = row0 < p.M;  // warp-uniform
+        float bq[4];
+        if (add_bias) load_bias_quad(p, n0 + cbeg, bq);
 
         if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
           break;
@@ -454,7 +442,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                          : "memory");
             float bv[G];
             if (add_bias) {
-              load_bias<G>(p, col0 + g * G, bv);
+              bias_granule<G>(bq, c * CH + g * G - cbeg, bv);
             } else {
 #pragma unroll
               for (int e = 0; e < G; ++e) bv[e] = 0.f;
@@ -501,6 +489,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int row0 = m0 + 32 * q;
       const int row = row0 + lane;
       const bool rows_live = row0 < p.M;  // warp-uniform
+      const bool use_bias = EPI != EPI_NONE && add_bias;
+      float bq[4];
+      if (use_bias) load_bias_quad(p, n0 + cbeg, bq);
 
       if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
         break;
@@ -534,7 +525,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               const int g = 4 * h + gi;  // 16-column granule within the 128-column row
               float bv[16];
               if (add_bias) {
-                load_bias<16>(p, col0 + g * 16, bv);
+                bias_granule<16>(bq, c * CH + g * 16 - cbeg, bv);
               } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) bv[e] = 0.f;
@@ -602,8 +593,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           float bv[G];
-          const bool use_bias = EPI != EPI_NONE && add_bias;
-          if (use_bias) load_bias<G>(p, col0 + g * G, bv);
+          if (use_bias) bias_granule<G>(bq, c * CH + g * G - cbeg, bv);
           float v[G];
 #pragma unroll
           for (int e = 0; e < G; ++e) {
