@@ -201,7 +201,11 @@ struct TcPlan {
 TcPlan plan_tc(const Call& c, DeviceInfo* d) {
   TcPlan t{};
   const int mode = c.opts ? c.opts->cta_pair : 0;
-  t.pair = (mode == 2) || (mode == 0 && c.M > 128 && d->num_sms >= 2);
+  // Pairs halve the B bytes each SM stages per MMA, which pays when the main loop is long; with
+  // at most 8 K blocks per tile (K <= 512) the per-tile hand-offs dominate and single CTAs are as
+  // fast or faster (measured on the GLU block, M = 1024, N = 21568: K = 256 29.9 vs 34.0 us,
+  // K = 512 36.9 vs 37.2 us, K = 1024 54.4 vs 45.3 us).
+  t.pair = (mode == 2) || (mode == 0 && c.M > 128 && c.K > 512 && d->num_sms >= 2);
   const int TILE_M = t.pair ? 2 * tc_block_m() : tc_block_m(), BN = tc_block_n();
   t.tiles_m = static_cast<int>((c.M + TILE_M - 1) / TILE_M);
   t.tiles_n = static_cast<int>((c.N + BN - 1) / BN);
