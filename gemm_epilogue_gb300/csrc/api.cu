@@ -173,7 +173,8 @@ int validate(const Call& c, bool* nothing) {
         o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
         o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 1 ||
-        o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 2)
+        o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 2 ||
+        o.k_rows < 0 || o.k_rows > 2)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -196,6 +197,7 @@ struct TcPlan {
   int tail_split, full_tiles, num_items;
   int last_width, gran;  // width of the last column of tiles, and the width it is rounded up to
   int y_blocks;          // staged Y blocks per epilogue warp (gate / residual, 16-bit out)
+  int k_rows;            // 128-byte K rows per ring stage
 };
 
 TcPlan plan_tc(const Call& c, DeviceInfo* d) {
@@ -262,6 +264,14 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
     const int want = c.opts ? c.opts->y_blocks : 0;
     t.y_blocks = want ? want : (c.K <= 256 ? 2 : 1);
   }
+  // Two K rows per stage on CTA pairs (half the stage hand-offs; 3 stages of 64 KB instead of 6
+  // of 32 KB).  The staged-Y epilogues keep one: their Y blocks leave room for two stages only.
+  t.k_rows = 1;
+  if (t.pair) {
+    const int want = c.opts ? c.opts->k_rows : 0;
+    t.k_rows = want ? want : (staged_y ? 1 : 2);
+    if (t.y_blocks == 2) t.k_rows = 1;
+  }
   return t;
 }
 
@@ -313,7 +323,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   const uint32_t out_box_cols = 128u / static_cast<uint32_t>(elem_bytes(c.t.out));
   const uint32_t kb_elems = 128u / static_cast<uint32_t>(elem_bytes(c.t.ab));  // one 128-B row
   if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, kb_elems) ||
-      !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, kb_elems, kb_elems) ||
+      !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, kb_elems * static_cast<uint32_t>(t.k_rows), kb_elems) ||
       !encode_2d(&tmO, c.t.out, c.out, c.M, c.N, 32, out_box_cols))
     return FGEMM_ERR_LAUNCH;
   if ((c.epi == EPI_GATE || c.epi == EPI_RESID) && c.t.out != ELEM_F32) {
@@ -335,6 +345,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.gran = t.gran;
   p.bias_init = (c.opts && c.opts->bias_init && c.epi != EPI_NONE) ? 1 : 0;
   p.y_blocks = t.y_blocks;
+  p.k_rows = t.k_rows;
   p.group = (c.opts && c.opts->group_m > 0) ? c.opts->group_m : 8;
   p.ab_bf16 = c.t.ab == ELEM_BF16;
   p.ab_f8 = c.t.ab == ELEM_E4M3;
@@ -345,7 +356,8 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.out_scale = c.out_scale;
   p.idesc = idesc_f16_f32acc(p.ab_bf16 != 0, TILE_M, BN, /*a_mn=*/false, /*b_mn=*/true);
   const bool swap = c.opts && c.opts->b_desc_swap;
-  const uint32_t box_bytes = kb_elems * kb_elems * static_cast<uint32_t>(elem_bytes(c.t.ab));
+  const uint32_t box_bytes = kb_elems * static_cast<uint32_t>(t.k_rows) * kb_elems *
+                             static_cast<uint32_t>(elem_bytes(c.t.ab));
   p.b_lbo = swap ? 1024u : box_bytes;  // distance between the 128-byte-wide column boxes of B
   p.b_sbo = swap ? box_bytes : 1024u;  // distance between 8-row groups along K
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
@@ -648,6 +660,7 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
     info->tail_split = t.tail_split;
     info->last_tile_n = t.last_width;
     info->y_blocks = t.y_blocks;
+    info->k_rows = t.k_rows;
     info->resident_pairs = t.resident;
   } else if (path == FGEMM_PATH_SKINNY) {
     const SkPlan s = plan_skinny(c, d);

@@ -33,41 +33,50 @@
 namespace fgemm {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64;  // per-CTA rows, tile columns, 16-bit K per stage
+constexpr int BM = 128, BN = 256;  // per-CTA rows, tile columns
 constexpr int EPI_WARPS = 8;  // two warpgroups: each owns half (128) of a tile's columns
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr uint32_t A_STAGE_BYTES = BM * BK * 2;  // 16 KB
-constexpr uint32_t B_BOX_BYTES = BK * 64 * 2;    // 8 KB: 64 K-rows x 64 N-columns
+// One K row of a stage is one 128-byte swizzle row per operand row: 64 16-bit or 128 fp8 elements.
+constexpr uint32_t A_ROW_BYTES = BM * 128;       // 16 KB: A's 128 rows x one K row
+constexpr uint32_t B_ROW_BYTES = 128 * 128;      // 16 KB: one K row of B for 128 columns
 constexpr uint32_t EPI_BUF_BYTES = 32 * 128;     // 32 rows x 128 bytes
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SMEM_LIMIT = 232448;          // dynamic shared memory per CTA
+constexpr int MAX_STAGES = 6;
 
 // YS: the gate's Y is staged through shared memory by TMA (16-bit outputs), which costs one ring
 // stage of shared memory for a 64 KB Y / output block.  YB = 2 (CTA pairs, short K loops) keeps two
 // such blocks per epilogue warp, so that Y is fetched two tiles ahead, in exchange for three stages
 // of the ring: with few K blocks per tile the epilogue's streams of Y and out, not the main loop,
 // set the pace.
-template <bool PAIR, bool YS = false, int YB = 1>
+// KSUB: K rows per stage (1 or 2).  A stage holds KSUB x 128 bytes of K for every operand row,
+// so two K rows halve the number of stage hand-offs (TMA completion -> MMA -> release -> reload)
+// per byte, at the price of half as many, twice as large stages in the same shared memory.
+// The ring takes whatever the epilogue's buffers leave, up to MAX_STAGES stages.
+template <bool PAIR, bool YS = false, int YB = 1, int KSUB = 1>
 struct Cfg {
   static_assert(YB == 1 || (YB == 2 && PAIR && YS), "double Y buffers: staged Y on CTA pairs");
-  static constexpr int STAGES = PAIR ? (YS ? (YB == 2 ? 3 : 5) : 6) : (YS ? 3 : 4);
-  static constexpr int B_BOXES = PAIR ? 2 : 4;                 // 64-column B boxes per CTA
-  static constexpr uint32_t B_STAGE_BYTES = B_BOXES * B_BOX_BYTES;
+  static_assert(KSUB == 1 || KSUB == 2, "one or two K rows per stage");
+  static constexpr uint32_t A_STAGE_BYTES = KSUB * A_ROW_BYTES;
+  static constexpr uint32_t B_STAGE_BYTES = KSUB * (PAIR ? 1 : 2) * B_ROW_BYTES;  // this CTA's columns
   static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-  static constexpr uint32_t STAGE_TX = (PAIR ? 2 : 1) * STAGE_BYTES;  // bytes per full barrier
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;
-  static constexpr uint32_t SMEM_A = 0;
-  static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
-  static constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
   // per epilogue warp: its 32 x 128 block of Y and results (YS), or one 32-row staging buffer
   static constexpr uint32_t Y_BLOCK_BYTES = 2 * EPI_BUF_BYTES;  // a warp's 32 x 128 block of Y
   static constexpr uint32_t EPI_WARP_BYTES = YS ? YB * Y_BLOCK_BYTES : EPI_BUF_BYTES;
+  static constexpr uint32_t RING_BUDGET = SMEM_LIMIT - 512 - 1024 - EPI_WARPS * EPI_WARP_BYTES;
+  static constexpr int STAGES =
+      RING_BUDGET / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : static_cast<int>(RING_BUDGET / STAGE_BYTES);
+  static_assert(STAGES >= 2, "at least two stages in the ring");
+  static constexpr uint32_t SMEM_A = 0;
+  static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
+  static constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
   static constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * EPI_WARP_BYTES;
   static constexpr uint32_t SMEM_BYTES = SMEM_BAR + 512 + 1024;  // + barriers + 1024-B alignment slack
-  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
 };
 
 // barrier slots (uint64 each) inside the SMEM_BAR area
-constexpr int MAX_STAGES = 6;
 constexpr int BAR_FULL = 0;
 constexpr int BAR_EMPTY = MAX_STAGES;
 constexpr int BAR_ACC_FULL = 2 * MAX_STAGES;
@@ -139,7 +148,7 @@ __device__ __forceinline__ void bias_granule(const float (&b)[4], int j0, float 
   for (int e = 0; e < G; ++e) out[e] = __shfl_sync(0xffffffffu, b[e & 3], (j0 >> 2) + (e >> 2));
 }
 
-template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1>
+template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmY,
@@ -149,16 +158,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int NG = CH / G;           // granules per chunk (8)
   // the gate's Y and the residual R are staged the same way (16-bit outputs)
   constexpr bool YS = (EPI == EPI_GATE || EPI == EPI_RESID) && (OUT_BYTES == 2);
-  using C = Cfg<PAIR, YS, YB>;
-  // Operand element size: one stage holds one 128-byte swizzle row of K per A row (64 16-bit or
-  // 128 fp8 elements) and B as boxes of (128 bytes of N) x (that K); the stage byte counts and
-  // the ring are the same for both.
+  using C = Cfg<PAIR, YS, YB, KSUB>;
+  // Operand element size: one K row of a stage is one 128-byte swizzle row per A row (64 16-bit or
+  // 128 fp8 elements); A arrives as KSUB boxes of 128 rows x one K row, B as boxes of (128 bytes
+  // of N) x (KSUB K rows); the stage byte counts and the ring are the same for both types.
   constexpr int EB = F8 ? 1 : 2;
-  constexpr int KB_ELEMS = 128 / EB;                      // K per stage
+  constexpr int KROW = 128 / EB;                          // K elements per K row
+  constexpr int KB_ELEMS = KSUB * KROW;                   // K per stage
   constexpr int BOXC = 128 / EB;                          // B box columns
-  constexpr uint32_t BBOX = static_cast<uint32_t>(KB_ELEMS * BOXC * EB);  // 8 KB / 16 KB
+  constexpr uint32_t BBOX = static_cast<uint32_t>(KB_ELEMS * BOXC * EB);  // KSUB x 8 KB / 16 KB
   constexpr int KSTEP = F8 ? 32 : 16;                     // K per MMA instruction
+  constexpr int KPR = KROW / KSTEP;                       // MMAs per K row (4)
   constexpr uint32_t B_KADV = static_cast<uint32_t>(KSTEP) * 128u;  // MN-major B bytes per MMA
+  constexpr uint32_t A_STAGE_BYTES = C::A_STAGE_BYTES;
   constexpr int STAGES = C::STAGES;
   constexpr int CG = PAIR ? 2 : 1;
   constexpr uint32_t SMEM_A = C::SMEM_A, SMEM_B = C::SMEM_B, SMEM_EPI = C::SMEM_EPI,
@@ -246,11 +258,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (stall) {
           } else if constexpr (PAIR) {
             const uint32_t lfb = lead_bar(BAR_FULL + stage);
-            tma_load_2d_pair(a_dst, &tmA, lfb, kb * KB_ELEMS, m0, pol);
+#pragma unroll
+            for (int r = 0; r < KSUB; ++r)
+              tma_load_2d_pair(a_dst + r * A_ROW_BYTES, &tmA, lfb, kb * KB_ELEMS + r * KROW, m0, pol);
             for (int c = 0; c < boxes; ++c)
               tma_load_2d_pair(b_dst + c * BBOX, &tmB, lfb, nb0 + BOXC * c, kb * KB_ELEMS, pol);
           } else {
-            tma_load_2d(a_dst, &tmA, fb, kb * KB_ELEMS, m0, pol);
+#pragma unroll
+            for (int r = 0; r < KSUB; ++r)
+              tma_load_2d(a_dst + r * A_ROW_BYTES, &tmA, fb, kb * KB_ELEMS + r * KROW, m0, pol);
             for (int c = 0; c < boxes; ++c)
               tma_load_2d(b_dst + c * BBOX, &tmB, fb, nb0 + BOXC * c, kb * KB_ELEMS, pol);
           }
@@ -299,7 +315,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t b_addr = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
 #pragma unroll
           for (int k = 0; k < KB_ELEMS / KSTEP; ++k) {  // 32 bytes of K per MMA
-            const uint64_t ad = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
+            const uint64_t ad =
+                sdesc_sw128(a_addr + (k / KPR) * A_ROW_BYTES + 32u * (k % KPR), 16u, 1024u);
             const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, p.b_lbo, p.b_sbo);
             const uint32_t acc = (p.bias_init | kb | k) != 0 ? 1u : 0u;
             if constexpr (F8)
@@ -667,12 +684,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1>
+template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                        const CUtensorMap& y, const TcParams& p, int grid, cudaStream_t s) {
-  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB>;
+  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB, KSUB>;
   constexpr uint32_t smem =
-      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB>::SMEM_BYTES;
+      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB, KSUB>::SMEM_BYTES;
   static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -736,6 +753,7 @@ cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const
   if constexpr ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2 && !F8) {
     if (pair && p.y_blocks == 2) return launch_one<EPI, OUT_BYTES, true, false, 2>(a, b, o, y, p, grid, s);
   }
+  if (pair && p.k_rows == 2) return launch_one<EPI, OUT_BYTES, true, F8, 1, 2>(a, b, o, y, p, grid, s);
   return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, p, grid, s)
               : launch_one<EPI, OUT_BYTES, false, F8>(a, b, o, y, p, grid, s);
 }

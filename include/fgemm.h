@@ -115,6 +115,10 @@ typedef struct {
                      the second M x N operand staged per epilogue warp; 0 = automatic (2 when
                      K <= 256, else 1), 1 = one tile ahead (5-stage ring), 2 = two tiles ahead
                      (3-stage ring).  Ignored elsewhere. */
+  int k_rows;     /* tensor-core path on CTA pairs: 128-byte K rows (64 16-bit or 128 fp8
+                     elements) per stage of the operand ring; 0 = automatic (2, or 1 for the
+                     gate and residual with 16-bit outputs), 1 = six stages of 32 KB per SM,
+                     2 = three stages of 64 KB.  Ignored elsewhere. */
   int reserved;
 } fgemm_opts;
 
@@ -235,6 +239,7 @@ typedef struct {
                          of N rounded up to what one CTA or pair stages and stores; 256 when N is a
                          multiple of 256); 0 on other paths */
   int y_blocks;       /* tensor-core path: staged Y blocks per epilogue warp (see fgemm_opts) */
+  int k_rows;         /* tensor-core path: 128-byte K rows per ring stage (see fgemm_opts) */
   int reserved;
 } fgemm_plan_info;
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,

@@ -408,6 +408,44 @@ def test_staged_y_blocks_integer_bit_exact(M, N, K, max_ctas, y_blocks):
     assert np.array_equal(down(res, F16), ref.out)
 
 
+K_ROW_CASES = [  # M, N, K, max_ctas (0 = every SM)
+    (300, 520, 200, 0), (700, 1800, 72, 20), (513, 1288, 136, 12), (257, 264, 1096, 0)]
+
+
+@pytest.mark.parametrize("M,N,K,max_ctas", K_ROW_CASES)
+@pytest.mark.parametrize("k_rows", [1, 2])
+def test_k_rows_per_stage_integer_bit_exact(M, N, K, max_ctas, k_rows):
+    # One or two 128-byte K rows per ring stage on CTA pairs, with K not a multiple of a stage
+    # (the last stage's second row lies past K), tail pieces and the narrowed last tile.
+    opts = {"path": fg.PATH_TC, "cta_pair": 2, "max_ctas": max_ctas, "k_rows": k_rows}
+    p = gen.integer_problem(M, N, K, BF16, BF16, seed=M + K + k_rows)
+    plan = fg.fgemm_plan(up(p.A, BF16), up(p.B, BF16), up(p.bias, BF16), None,
+                         torch.empty(M, N, dtype=torch.bfloat16, device="cuda"), M, N, K, fg.BF16,
+                         opts=opts)
+    assert plan["k_rows"] == k_rows
+    out, path = run_fused(p, M, N, K, BF16, BF16, BF16, opts=opts)
+    assert path == fg.PATH_TC
+    assert np.array_equal(down(out, BF16), oracle_run(p, M, N, K, BF16, BF16, BF16).out)
+    p = gen.integer_problem(M, N, K, F16, F32, seed=M + 1)
+    out, _ = run_fused(p, M, N, K, F16, F32, F32, opts=opts)
+    assert np.array_equal(down(out, F32), oracle_run(p, M, N, K, F16, F32, F32).out)
+    if N % 16 == 0:
+        p = gen.integer_problem(M, N, K, BF16, F32, seed=M + 2)
+        got, _ = _run_quant(p, M, N, K, BF16, F32, 0.25, opts)
+        assert np.array_equal(got, oracle.bias_relu_quant(p.A, p.B, p.bias, M, N, K, BF16, F32, 0.25).out)
+    if N % 16 == 0 and K % 16 == 0:
+        p = gen.integer_problem(M, N, K, E4M3, F32, seed=M + 3)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        fg.fgemm_bias_relu_ex(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32), out, M, N, K,
+                              dtype_word(E4M3, F32, BF16), opts=opts)
+        torch.cuda.synchronize()
+        assert np.array_equal(down(out, BF16), oracle.bias_relu(p.A, p.B, p.bias, M, N, K, E4M3, F32, BF16).out)
+    # the gate and the residual with two K rows (two-stage ring beside the staged Y)
+    p = gen.integer_problem(M, N, K, F16, F16, seed=M + 4, gate=True)
+    out, _ = run_fused(p, M, N, K, F16, F16, F16, gate=True, opts=dict(opts, y_blocks=1))
+    assert np.array_equal(down(out, F16), oracle_run(p, M, N, K, F16, F16, F16, gate=True).out)
+
+
 def _same_values(got_bits, ref_bits, t):
     """Equal as numbers (-0 == +0), every element."""
     return np.array_equal(oracle.decode(got_bits, t), oracle.decode(ref_bits, t))
