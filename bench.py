@@ -459,7 +459,7 @@ def run_sweep(args):
         prob = Problem(w, dev, l2, with_unfused=unf)
         steps = max(5, min(200, int(2e-1 / max(w.flops / 1.2e15, 1e-6))))
         if w.name.startswith("ffn"):
-            variants = [{"group_m": g} for g in (1, 4, 8)]
+            variants = [{"group_m": g} for g in (1, 4, 8, 16)]
         elif w.name.startswith("skinny"):
             variants = [None] + [{"split_k": s, "skinny_tiles": t, "stages": g}
                                  for t in (1, 2) for s in (2, 4, 8) for g in (3, 4, 6)]

@@ -87,7 +87,7 @@ typedef enum {
 
 /* Per-call options of the _ex entry points.  Zero-initialised fields mean "default". */
 typedef struct {
-  int group_m;    /* M-tiles per band of the grouped tile order (default 8; 1 = row-major) */
+  int group_m;    /* M-tiles per band of the grouped tile order (default 16; 1 = row-major) */
   int path;       /* FGEMM_PATH_*; forcing a path the shape cannot take -> INVALID_VALUE */
   int split_k;    /* skinny path: K splits (1..8, one CTA each in a cluster); 0 = automatic */
   int max_ctas;   /* persistent grid cap (default: one CTA per SM) */
