@@ -26,6 +26,8 @@
 //               result is written over it and stored from there; with fp32 outputs it is loaded
 //               straight into registers ahead of the TMEM read.
 // The accumulator goes from TMEM to registers to the single store; it never touches HBM.
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_order.h"
@@ -447,6 +449,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t sb = ebuf + static_cast<uint32_t>(yb) * C::Y_BLOCK_BYTES +
                               static_cast<uint32_t>(c - cbeg / CH) * EPI_BUF_BYTES;
+          // Y and out share the 16-bit operand type here: the chunk is compiled for fp16 and for
+          // bf16 and one of the two is taken (a warp-uniform branch), so that no conversion
+          // carries a run-time type test.
+          auto chunk = [&](auto bf_tag) {
+          constexpr bool BF = decltype(bf_tag)::value;
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             // 128-byte swizzle: granule g of row `lane` sits at slot g ^ (lane & 7)
@@ -467,7 +474,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t packed[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 y2 = unpack2(y[e], y_bf);
+              const float2 y2 = unpack2(y[e], BF);
               float x0 = __uint_as_float(acc[g * G + 2 * e]) + bv[2 * e];  // bias once
               float x1 = __uint_as_float(acc[g * G + 2 * e + 1]) + bv[2 * e + 1];
               if constexpr (EPI == EPI_GATE) {
@@ -477,12 +484,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 x0 = fmaxf(x0 + y2.x, 0.0f);
                 x1 = fmaxf(x1 + y2.y, 0.0f);
               }
-              packed[e] = pack2(x0, x1, out_bf);
+              packed[e] = pack2(x0, x1, BF);
             }
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(packed[0]),
                          "r"(packed[1]), "r"(packed[2]), "r"(packed[3])
                          : "memory");
           }
+          };
+          if (y_bf)
+            chunk(std::true_type{});
+          else
+            chunk(std::false_type{});
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tma_store_2d(&tmOut, sb, col0, row0, pol_out);
@@ -607,6 +619,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
 
+        // compiled for both 16-bit types (of out, or of Y with fp32 outputs); a warp-uniform
+        // branch picks one, so that no conversion carries a run-time type test
+        auto chunk = [&](auto bf_tag) {
+        constexpr bool BF = decltype(bf_tag)::value;
+        (void)BF;  // unused when neither out nor Y is 16-bit
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           float bv[G];
@@ -628,7 +645,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               const int idx = g * G + e;  // column within the chunk
               const uint4 u = yv[idx / 8];
               const uint32_t w = (idx % 8 < 2) ? u.x : (idx % 8 < 4) ? u.y : (idx % 8 < 6) ? u.z : u.w;
-              const float2 y2 = unpack2(w, y_bf);
+              const float2 y2 = unpack2(w, BF);
               if constexpr (EPI == EPI_GATE) {
                 v[e] = fmaf(v[e], y2.x, v[e]);          // X + X * Y
                 v[e + 1] = fmaf(v[e + 1], y2.y, v[e + 1]);
@@ -640,10 +657,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           uint4 packed;
           if constexpr (OUT_BYTES == 2) {
-            packed.x = pack2(v[0], v[1], out_bf);
-            packed.y = pack2(v[2], v[3], out_bf);
-            packed.z = pack2(v[4 % G], v[5 % G], out_bf);
-            packed.w = pack2(v[6 % G], v[7 % G], out_bf);
+            packed.x = pack2(v[0], v[1], BF);
+            packed.y = pack2(v[2], v[3], BF);
+            packed.z = pack2(v[4 % G], v[5 % G], BF);
+            packed.w = pack2(v[6 % G], v[7 % G], BF);
           } else {
             packed.x = __float_as_uint(v[0]);
             packed.y = __float_as_uint(v[1]);
@@ -657,6 +674,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                        "r"(packed.y), "r"(packed.z), "r"(packed.w)
                        : "memory");
         }
+        };
+        if ((OUT_BYTES == 2) ? out_bf : y_bf)
+          chunk(std::true_type{});
+        else
+          chunk(std::false_type{});
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
