@@ -465,7 +465,7 @@ def run_sweep(args):
                                  for t in (1, 2) for s in (2, 4, 8) for g in (3, 4, 6)]
         else:
             variants = [None, {"tail_split": 1}, {"cta_pair": 1}, {"cta_pair": 1, "tail_split": 1},
-                        {"bias_init": 1}]
+                        {"bias_init": 1}, {"bias_init": 2}]
         if args.sweep_variants:
             variants = json.loads(args.sweep_variants)
         for opts in variants:

@@ -172,7 +172,7 @@ int validate(const Call& c, bool* nothing) {
     if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
         o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
-        o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 1 ||
+        o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 2 ||
         o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 2 ||
         o.k_rows < 0 || o.k_rows > 2)
       return FGEMM_ERR_INVALID_VALUE;
@@ -343,7 +343,12 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.num_items = t.num_items;
   p.last_width = t.last_width;
   p.gran = t.gran;
-  p.bias_init = (c.opts && c.opts->bias_init && c.epi != EPI_NONE) ? 1 : 0;
+  // Bias-initialised accumulator: on by default for short K loops (K <= 1024), where the epilogue
+  // sets the pace and moving the bias out of it pays (GLU block, M = 1024, N = 21568: K = 256
+  // 27.2 vs 28.3 us, K = 1024 44.6 vs 45.1 us); with long K loops the bias write lengthens the
+  // accumulator hand-off instead (4096^3: 90.3 vs 88.1 us).
+  const int bi = c.opts ? c.opts->bias_init : 0;
+  p.bias_init = (c.epi != EPI_NONE && (bi == 1 || (bi == 0 && c.K <= 1024))) ? 1 : 0;
   p.y_blocks = t.y_blocks;
   p.k_rows = t.k_rows;
   // 16 M-tiles per band: measured best on the 8192-row FFN (577-583 vs 595-605 us for 8); the

@@ -105,10 +105,11 @@ typedef struct {
                        on that stage can never complete; it expires after timeout_ms, the kernel
                        drains and exits, and fgemm_device_status reports FGEMM_ERR_TIMEOUT.
                        The output of that call is undefined.  Tensor-core and skinny paths. */
-  int bias_init;  /* tensor-core path: 1 = start each tile's accumulator at the bias (written into
+  int bias_init;  /* tensor-core path: start each tile's accumulator at the bias (written into
                      tensor memory before the K loop) instead of adding it after the reduction;
                      same result up to the rounding order ("Optimizing GEMM + Activation on CDNA4
-                     with TLX", V4).  Ignored by the other paths and by the plain GEMM. */
+                     with TLX", V4).  0 = automatic (on when K <= 1024), 1 = on, 2 = off.
+                     Ignored by the other paths and by the plain GEMM. */
   int full_last_n; /* tensor-core path, diagnostic: 1 = run the last column of tiles at the full
                       256-column width instead of narrowing it to the columns left of N */
   int y_blocks;   /* tensor-core path, gate and residual with 16-bit outputs on CTA pairs: blocks of

@@ -493,6 +493,21 @@ def test_bias_init_integer_exact(M, N, K, opts):
                             oracle.bias_relu(p.A, p.B, p.bias, M, N, K, E4M3, F32, BF16).out, BF16)
 
 
+def test_bias_init_default_on_short_k_only():
+    # automatic choice: bias first for K <= 1024, after the sum above; forcing it off (2) gives the
+    # after-the-sum order at any K, which on integer inputs is the same value
+    M, N = 300, 520
+    for K, default_bias_first in ((200, True), (1096, False)):
+        p = gen.integer_problem(M, N, K, BF16, BF16, seed=K)
+        auto, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts={"path": fg.PATH_TC})
+        on, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts={"path": fg.PATH_TC, "bias_init": 1})
+        off, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts={"path": fg.PATH_TC, "bias_init": 2})
+        ref = oracle_run(p, M, N, K, BF16, BF16, BF16).out
+        for x in (auto, on, off):
+            assert _same_values(down(x, BF16), ref, BF16)
+        assert torch.equal(auto, on if default_bias_first else off)
+
+
 @pytest.mark.parametrize("gate", [False, True])
 def test_bias_init_random_tolerance(gate):
     # random inputs: bias first changes only the rounding order of the fp32 sum
