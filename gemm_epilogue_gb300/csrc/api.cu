@@ -173,7 +173,7 @@ int validate(const Call& c, bool* nothing) {
         o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
         o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 2 ||
-        o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 2 ||
+        o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 3 ||
         o.k_rows < 0 || o.k_rows > 2)
       return FGEMM_ERR_INVALID_VALUE;
   }
@@ -253,23 +253,29 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
   const int left = static_cast<int>(c.N - static_cast<int64_t>(t.tiles_n - 1) * BN);
   t.last_width = (left + t.gran - 1) / t.gran * t.gran;
   if (t.last_width > BN || (c.opts && c.opts->full_last_n)) t.last_width = BN;
-  // Gate / residual with 16-bit outputs on CTA pairs: with at most 4 K blocks (K <= 256) per tile
-  // the Y and out streams set the pace, so Y is staged two tiles ahead (a 3-stage ring makes room;
-  // measured on the GLU block, M = 1024, N = 21568: 4 % faster at K = 256, equal at K = 512, 20 %
-  // slower at K = 1024).
+  // Gate / residual with 16-bit outputs on CTA pairs (the Y of the second operand staged per
+  // epilogue warp; internal y_blocks: 1 = the tile's 8 KB block, 2 = two blocks, 0 = one 4 KB
+  // chunk at a time).  K > 1024: chunk at a time, which leaves the ring three two-row stages
+  // (the epilogue has a whole main loop of slack); K <= 256: two blocks (Y two tiles ahead);
+  // else one block.
   t.y_blocks = 1;
   const bool staged_y = (c.epi == EPI_GATE || c.epi == EPI_RESID) && elem_bytes(c.t.out) == 2 &&
                         c.t.ab != ELEM_E4M3;
   if (t.pair && staged_y) {
     const int want = c.opts ? c.opts->y_blocks : 0;
-    t.y_blocks = want ? want : (c.K <= 256 ? 2 : 1);
+    if (want == 3)
+      t.y_blocks = 0;
+    else if (want)
+      t.y_blocks = want;
+    else
+      t.y_blocks = c.K > 1024 ? 0 : (c.K <= 256 ? 2 : 1);
   }
   // Two K rows per stage on CTA pairs (half the stage hand-offs; 3 stages of 64 KB instead of 6
-  // of 32 KB).  The staged-Y epilogues keep one: their Y blocks leave room for two stages only.
+  // of 32 KB), unless a whole staged Y block per warp leaves room for two stages only.
   t.k_rows = 1;
   if (t.pair) {
     const int want = c.opts ? c.opts->k_rows : 0;
-    t.k_rows = want ? want : (staged_y ? 1 : 2);
+    t.k_rows = want ? want : ((staged_y && t.y_blocks > 0) ? 1 : 2);
     if (t.y_blocks == 2) t.k_rows = 1;
   }
   return t;
@@ -666,7 +672,7 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
     info->work_items = t.num_items;
     info->tail_split = t.tail_split;
     info->last_tile_n = t.last_width;
-    info->y_blocks = t.y_blocks;
+    info->y_blocks = t.y_blocks == 0 ? 3 : t.y_blocks;
     info->k_rows = t.k_rows;
     info->resident_pairs = t.resident;
   } else if (path == FGEMM_PATH_SKINNY) {

@@ -57,7 +57,7 @@ constexpr int MAX_STAGES = 6;
 // The ring takes whatever the epilogue's buffers leave, up to MAX_STAGES stages.
 template <bool PAIR, bool YS = false, int YB = 1, int KSUB = 1>
 struct Cfg {
-  static_assert(YB == 1 || (YB == 2 && PAIR && YS), "double Y buffers: staged Y on CTA pairs");
+  static_assert(YB == 1 || ((YB == 2 || YB == 0) && PAIR && YS), "Y staging variants: staged Y on CTA pairs");
   static_assert(KSUB == 1 || KSUB == 2, "one or two K rows per stage");
   static constexpr uint32_t A_STAGE_BYTES = KSUB * A_ROW_BYTES;
   static constexpr uint32_t B_STAGE_BYTES = KSUB * (PAIR ? 1 : 2) * B_ROW_BYTES;  // this CTA's columns
@@ -65,7 +65,8 @@ struct Cfg {
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;
   // per epilogue warp: its 32 x 128 block of Y and results (YS), or one 32-row staging buffer
   static constexpr uint32_t Y_BLOCK_BYTES = 2 * EPI_BUF_BYTES;  // a warp's 32 x 128 block of Y
-  static constexpr uint32_t EPI_WARP_BYTES = YS ? YB * Y_BLOCK_BYTES : EPI_BUF_BYTES;
+  // YB = 0 (staged Y): one 32 x 64 chunk of Y at a time per warp
+  static constexpr uint32_t EPI_WARP_BYTES = YS ? (YB == 0 ? EPI_BUF_BYTES : YB * Y_BLOCK_BYTES) : EPI_BUF_BYTES;
   static constexpr uint32_t RING_BUDGET = SMEM_LIMIT - 512 - 1024 - EPI_WARPS * EPI_WARP_BYTES;
   static constexpr int STAGES =
       RING_BUDGET / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : static_cast<int>(RING_BUDGET / STAGE_BYTES);
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(bar(BAR_ACC_EMPTY + b), (PAIR ? 2 : 1) * EPI_WARPS);
     }
     mbar_init(bar(BAR_MMA_DONE), 1);
-    for (int w = 0; w < YB * EPI_WARPS; ++w) mbar_init(bar(BAR_Y + w), 1);
+    for (int w = 0; w < (YB == 0 ? 1 : YB) * EPI_WARPS; ++w) mbar_init(bar(BAR_Y + w), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -387,10 +388,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     int it = 0;
     if constexpr (YS) {
-      // Gate with Y staged by TMA: the warp's 32 x 128 block of Y lands in one of its YB 8 KB
+      // Gate with Y staged by TMA: the warp's 32 x 128 block of Y lands in one of its NYB 8 KB
       // blocks (two 128-byte-swizzled 32 x 64 chunks) while earlier tiles are still computed; the
       // epilogue reads y from there, writes the result over it, and stores each chunk with one TMA
-      // store.  Work item number `it` of this CTA uses block it % YB.
+      // store.  Work item number `it` of this CTA uses block it % NYB.
+      // YB = 0 (long K loops): one 4 KB chunk buffer per warp; the tile's first chunk of Y is
+      // prefetched a work item ahead, the second is loaded once the first chunk's store has read
+      // the buffer (the epilogue has the whole next main loop to do it), which leaves the ring
+      // room for three two-row stages.
+      constexpr bool YHALF = YB == 0;
+      constexpr int NYB = YHALF ? 1 : YB;  // prefetched Y blocks per warp
       auto ybar = [&](int yb) { return bar(BAR_Y + yb * EPI_WARPS + ew); };
       uint32_t y_par = 0, y_issued = 0;  // bit yb: parity to wait for / a load is in flight
       auto issue_y = [&](int t, int yb) -> bool {  // warp-uniform result
@@ -401,6 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = cbeg; c < cbeg + BN / 2 && c < w.width; c += CH)
           if (w.col0 + c < p.N) ++nchunks;
         if (nchunks == 0) return false;
+        if (YHALF) nchunks = 1;
         if (lane == 0) {
           bulk_wait_read<0>();  // the stores that last read this region are done with it
           const uint32_t yblk = ebuf + static_cast<uint32_t>(yb) * C::Y_BLOCK_BYTES;
@@ -410,7 +418,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         return true;
       };
-      for (int j = 0; j < YB; ++j)
+      for (int j = 0; j < NYB; ++j)
         if (unit + j * units < p.num_items && issue_y(unit + j * units, j)) y_issued |= 1u << j;
       for (int t = unit; t < p.num_items; t += units, ++it) {
         const Work wk = work_of(p, t);
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
           break;
         tc_fence_after();
-        const int yb = YB == 1 ? 0 : (it & 1);
+        const int yb = NYB == 1 ? 0 : (it & 1);
         if ((y_issued >> yb) & 1u) {
           if (!mbar_wait(ybar(yb), (y_par >> yb) & 1u, abort_flag, tmo, p.err, SITE_EPI_Y)) break;
           y_par ^= 1u << yb;
@@ -434,10 +442,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
+        bool aborted = false;
 #pragma unroll 1
         for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
           const int col0 = n0 + c * CH;
           if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
+          if constexpr (YHALF) {
+            if (c != cbeg / CH) {  // later chunks: Y into the buffer the last store has read
+              if (lane == 0) {
+                bulk_wait_read<0>();
+                mbar_arrive_expect_tx(ybar(0), EPI_BUF_BYTES);
+                tma_load_2d(ebuf, &tmY, ybar(0), col0, row0, pol_out);
+              }
+              y_issued |= 1u;
+              if (!mbar_wait(ybar(0), y_par & 1u, abort_flag, tmo, p.err, SITE_EPI_Y)) {
+                aborted = true;
+                break;
+              }
+              y_par ^= 1u;
+              y_issued &= ~1u;
+            }
+          }
           uint32_t acc[CH];
           __syncwarp();  // tcgen05.ld is warp-collective
           {
@@ -447,8 +472,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld32(taddr, a1, c * CH + 32);
             tmem_ld_wait();
           }
-          const uint32_t sb = ebuf + static_cast<uint32_t>(yb) * C::Y_BLOCK_BYTES +
-                              static_cast<uint32_t>(c - cbeg / CH) * EPI_BUF_BYTES;
+          const uint32_t sb = YHALF ? ebuf
+                                    : ebuf + static_cast<uint32_t>(yb) * C::Y_BLOCK_BYTES +
+                                          static_cast<uint32_t>(c - cbeg / CH) * EPI_BUF_BYTES;
           // Y and out share the 16-bit operand type here: the chunk is compiled for fp16 and for
           // bf16 and one of the two is taken (a warp-uniform branch), so that no conversion
           // carries a run-time type test.
@@ -497,16 +523,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             chunk(std::false_type{});
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) tma_store_2d(&tmOut, sb, col0, row0, pol_out);
+          if (lane == 0) {
+            tma_store_2d(&tmOut, sb, col0, row0, pol_out);
+            if (YHALF) bulk_commit();  // the next chunk's Y load waits for this store's read
+          }
         }
+        if (aborted) break;
         if (lane == 0) bulk_commit();
         // This warp has finished reading accumulator b: release it to the MMA warp.
         release_acc(t + 2 * units, b);
-        // Prefetch into this block the Y of the work item YB items ahead (main loops run meanwhile).
-        if (t + YB * units < p.num_items && issue_y(t + YB * units, yb)) y_issued |= 1u << yb;
+        // Prefetch into this block the Y of the work item NYB items ahead (main loops run
+        // meanwhile).
+        if (t + NYB * units < p.num_items && issue_y(t + NYB * units, yb)) y_issued |= 1u << yb;
       }
       // After an abort a prefetched Y block may still be landing: wait for it (bounded).
-      for (int j = 0; j < YB; ++j)
+      for (int j = 0; j < NYB; ++j)
         if ((y_issued >> j) & 1u) drain_wait(ybar(j), (y_par >> j) & 1u, tmo, p.err);
     } else {
     for (int t = unit; t < p.num_items; t += units, ++it) {
@@ -774,6 +805,9 @@ cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const
                                cudaStream_t s) {
   if constexpr ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2 && !F8) {
     if (pair && p.y_blocks == 2) return launch_one<EPI, OUT_BYTES, true, false, 2>(a, b, o, y, p, grid, s);
+    if (pair && p.y_blocks == 0)  // one 4 KB chunk of Y per warp
+      return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, false, 0, 2>(a, b, o, y, p, grid, s)
+                           : launch_one<EPI, OUT_BYTES, true, false, 0, 1>(a, b, o, y, p, grid, s);
   }
   if (pair && p.k_rows == 2) return launch_one<EPI, OUT_BYTES, true, F8, 1, 2>(a, b, o, y, p, grid, s);
   return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, p, grid, s)

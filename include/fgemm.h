@@ -112,10 +112,12 @@ typedef struct {
                      Ignored by the other paths and by the plain GEMM. */
   int full_last_n; /* tensor-core path, diagnostic: 1 = run the last column of tiles at the full
                       256-column width instead of narrowing it to the columns left of N */
-  int y_blocks;   /* tensor-core path, gate and residual with 16-bit outputs on CTA pairs: blocks of
-                     the second M x N operand staged per epilogue warp; 0 = automatic (2 when
-                     K <= 256, else 1), 1 = one tile ahead (5-stage ring), 2 = two tiles ahead
-                     (3-stage ring).  Ignored elsewhere. */
+  int y_blocks;   /* tensor-core path, gate and residual with 16-bit outputs on CTA pairs: how
+                     each epilogue warp stages its share of the second M x N operand: 0 =
+                     automatic (3 when K > 1024, 2 when K <= 256, else 1), 1 = the tile's 32 x 128
+                     block, one work item ahead, 2 = two such blocks, two items ahead (3-stage
+                     ring), 3 = one 32 x 64 chunk at a time (4 KB; leaves room for two-row ring
+                     stages).  Ignored elsewhere. */
   int k_rows;     /* tensor-core path on CTA pairs: 128-byte K rows (64 16-bit or 128 fp8
                      elements) per stage of the operand ring; 0 = automatic (2, or 1 for the
                      gate and residual with 16-bit outputs), 1 = six stages of 32 KB per SM,
@@ -239,7 +241,7 @@ typedef struct {
   int last_tile_n;    /* tensor-core path: MMA width of the last column of tiles (the columns left
                          of N rounded up to what one CTA or pair stages and stores; 256 when N is a
                          multiple of 256); 0 on other paths */
-  int y_blocks;       /* tensor-core path: staged Y blocks per epilogue warp (see fgemm_opts) */
+  int y_blocks;       /* tensor-core path: staging of the second operand (see fgemm_opts) */
   int k_rows;         /* tensor-core path: 128-byte K rows per ring stage (see fgemm_opts) */
   int reserved;
 } fgemm_plan_info;

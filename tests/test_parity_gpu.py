@@ -383,10 +383,10 @@ Y_BLOCK_CASES = [  # M, N, K, max_ctas (0 = every SM)
 
 
 @pytest.mark.parametrize("M,N,K,max_ctas", Y_BLOCK_CASES)
-@pytest.mark.parametrize("y_blocks", [1, 2])
+@pytest.mark.parametrize("y_blocks", [1, 2, 3])
 def test_staged_y_blocks_integer_bit_exact(M, N, K, max_ctas, y_blocks):
-    # The gate's Y (and the residual's R) staged one or two tiles ahead per epilogue warp, on CTA
-    # pairs; tail pieces and the narrowed last tile included.
+    # The gate's Y (and the residual's R) staged one or two tiles ahead per epilogue warp, or one
+    # 32 x 64 chunk at a time (3), on CTA pairs; tail pieces and the narrowed last tile included.
     opts = {"path": fg.PATH_TC, "cta_pair": 2, "max_ctas": max_ctas, "y_blocks": y_blocks}
     p = gen.integer_problem(M, N, K, F16, F16, seed=M + K + y_blocks, gate=True)
     plan = fg.fgemm_plan(up(p.A, F16), up(p.B, F16), up(p.bias, F16), up(p.Y, F16),
@@ -396,7 +396,8 @@ def test_staged_y_blocks_integer_bit_exact(M, N, K, max_ctas, y_blocks):
     auto = fg.fgemm_plan(up(p.A, F16), up(p.B, F16), up(p.bias, F16), up(p.Y, F16),
                          torch.empty(M, N, dtype=torch.float16, device="cuda"), M, N, K, fg.F16,
                          gate=True, opts={"cta_pair": 2})
-    assert auto["y_blocks"] == (2 if K <= 256 else 1)
+    assert auto["y_blocks"] == (3 if K > 1024 else 2 if K <= 256 else 1)
+    assert auto["k_rows"] == (2 if K > 1024 else 1)
     out, path = run_fused(p, M, N, K, F16, F16, F16, gate=True, opts=opts)
     assert path == fg.PATH_TC
     assert np.array_equal(down(out, F16), oracle_run(p, M, N, K, F16, F16, F16, gate=True).out)
