@@ -127,6 +127,17 @@ def env_rank():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def slowest_rank(dist, value, device=None):
+    """Max over the ranks of a per-rank time: every rank times its own replica of the workload,
+    and the job takes as long as its slowest rank.  `dist` is torch.distributed (None: one rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------------------- our implementation
 
 class Problem:
@@ -375,15 +386,9 @@ def run_ours(args):
     unfused = args.variant == "unfused"
     ms, path = time_steps(prob, args.steps, args.warmup, stream, barrier=barrier, unfused=unfused)
     clocks = sampler.stop() if sampler else None
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank(dist, ms, dev)
     e2e_ms, h2d, d2h = e2e_steps(prob, max(3, min(args.steps, 20)), stream)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = slowest_rank(dist, e2e_ms, dev)
     assert fg.fgemm_device_status(stream) == 0
     if rank != 0:
         if dist:
