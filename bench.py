@@ -48,12 +48,39 @@ def tensor_peak(pk, w):
     return pk["bf16_tflops"] * (2.0 if w.ab_type == gen.E4M3 else 1.0)
 
 
+def strip_comments(src: str) -> str:
+    """C / C++ source without its comments (string literals kept), so that the hash below follows
+    the code only."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel and launch code (comments and layout excluded): recorded ncu traffic
+    counts only while this matches the hash stored with it."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "gemm_epilogue_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            code = " ".join(strip_comments(fh.read()).split())  # layout and comments excluded
+            h.update(f.encode() + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -4,27 +4,36 @@
 // in the CTA-pair form (PAIR), one 2-CTA cluster per SM pair walks 256 x 256 tiles: each CTA
 // stages its own 128 rows of A and half (128 columns) of B, the even CTA issues
 // tcgen05.mma.cta_group::2 (M = 256) for both, and each CTA's TMEM receives its 128 rows.  The pair
-// halves the B bytes each SM fetches per MMA and lets each SM keep 6 stages in flight.
-//   warp 0      TMA producer: A tile 128 x 64 (K-major) and B tile 64 x 256 (N-major, four
-//               64-column boxes) per stage into a STAGES-deep shared-memory ring, completion
-//               counted in bytes on full[s]; out-of-range rows / columns / K are zero-filled by
-//               TMA, which is the M/N/K tail mask of "I3. Fuse a GEMM epilogue and change tile
-//               scheduling" ("Tiles and grouped ownership": A's M/K edges, B's K/N edges).
-//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, fp32 accumulate in tensor memory,
-//               128 x 256 accumulator, double-buffered (2 x 256 of the 512 TMEM columns) so the
-//               epilogue of tile i overlaps the mainloop of tile i + 1.  tcgen05.commit releases
-//               each smem stage (empty[s]) and hands a finished accumulator over (acc_full[b]).
-//   warps 2-5   epilogue: each warp owns the 32 TMEM lanes (rows) its warp id allows, and per
-//               64-column chunk: tcgen05.ld -> + bias[j] -> ReLU (fmaxf) or the gate
-//               fma(x, y, x) -> one round-to-nearest conversion -> 128-byte-swizzled staging
-//               buffer -> one TMA store, which clips rows >= M and columns >= N (the store mask).
-//               The bias is read only here, after the reduction ("Triton: Fused Matmul + Bias +
-//               ReLU (Epilogue Fusion)", "Pitfalls": load the bias after the K loop; mask it with
-//               j < N).  For the gate (and the residual add, "Triton: Fused Matmul + Bias +
-//               ReLU (Epilogue Fusion)", "Variants") the second M x N operand is prefetched by TMA
-//               into the epilogue's own buffers while the next tile's main loop runs, and the
-//               result is written over it and stored from there; with fp32 outputs it is loaded
-//               straight into registers ahead of the TMEM read.
+// halves the B bytes each SM fetches per MMA.  fp16 / bf16 operands use kind::f16, fp8 e4m3
+// operands kind::f8f6f4; one "K row" of a stage is 128 bytes of K per operand row either way.
+//   warp 0      TMA producer: per stage, A as KSUB boxes of 128 rows x one K row (K-major) and
+//               B as 128-byte-wide boxes of KSUB K rows (N-major), into a shared-memory ring as
+//               deep as the epilogue's buffers allow (three 64 KB stages with two K rows on pairs,
+//               else up to six of 32 KB); completion counted in bytes on full[s]; out-of-range
+//               rows / columns / K are zero-filled by TMA, which is the M/N/K tail mask of
+//               "I3. Fuse a GEMM epilogue and change tile scheduling" ("Tiles and grouped
+//               ownership": A's M/K edges, B's K/N edges).
+//   warp 1      MMA issuer (one thread): fp32 accumulate in tensor memory, 128 x 256 accumulator
+//               per CTA, double-buffered (2 x 256 of the 512 TMEM columns) so the epilogue of tile
+//               i overlaps the main loop of tile i + 1.  The MMA's N is the work item's width: 256,
+//               or less for the pieces of the last partial round and for the last column of tiles
+//               (narrowed to the columns left of N).  tcgen05.commit releases each smem stage
+//               (empty[s]) and hands a finished accumulator over (acc_full[b]).
+//   warps 2-9   epilogue, two warpgroups splitting the tile's columns: each warp owns the 32 TMEM
+//               lanes (rows) its warp id allows, reads its 128 bias values with one coalesced load
+//               per work item (shuffled to the granules), and per 64-column chunk:
+//               tcgen05.ld -> + bias[j] -> ReLU (fmaxf), the gate fma(x, y, x), the residual, or
+//               the fp8 scale-and-clamp -> one round-to-nearest conversion -> 128-byte-swizzled
+//               staging buffer -> one TMA store, which clips rows >= M and columns >= N (the store
+//               mask).  The bias is added after the reduction ("Triton: Fused Matmul + Bias + ReLU
+//               (Epilogue Fusion)", "Pitfalls": after the K loop, masked with j < N), or, with the
+//               bias-initialised accumulator ("Optimizing GEMM + Activation on CDNA4 with TLX",
+//               V4; the default for short K loops), written into the free TMEM buffer before its
+//               tile's first MMA.  For the gate (and the residual add, "Variants") the second
+//               M x N operand is prefetched by TMA into the epilogue's own buffers while the main
+//               loop runs (a whole 8 KB block per warp a work item ahead, or one 4 KB chunk at a
+//               time on long K loops), and the result is written over it and stored from there;
+//               with fp32 outputs it is loaded straight into registers ahead of the TMEM read.
 // The accumulator goes from TMEM to registers to the single store; it never touches HBM.
 #include <type_traits>
 

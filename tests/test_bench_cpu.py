@@ -70,3 +70,12 @@ def test_tensor_peak_per_operand_type():
     pk = {"bf16_tflops": 1909.9}
     assert bench.tensor_peak(pk, gen.WORKLOADS["square_4096"]) == 1909.9
     assert bench.tensor_peak(pk, gen.WORKLOADS["square_fp8_4096"]) == 2 * 1909.9
+
+
+def test_source_hash_ignores_comments_and_layout_only():
+    src = 'int a; // note\n/* block\n comment */ const char* s = "// kept"; char c = \'/\';\nint  b;'
+    assert bench.strip_comments(src).split() == ["int", "a;", "const", "char*", "s", "=",
+                                                 '"//', 'kept";', "char", "c", "=", "'/';", "int",
+                                                 "b;"]
+    assert " ".join(bench.strip_comments(src).split()) != " ".join(
+        bench.strip_comments(src.replace("int  b", "int b2")).split())
