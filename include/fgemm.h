@@ -14,9 +14,15 @@
  *       the elementwise gate with a second tensor Y of the output's shape), evaluated as
  *       fma(X, Y, X) as in that page's "Version 4: Making the Epilogue Nearly Free".
  *
+ *   fgemm_bias_residual_relu  out = max(0, A @ B + bias + R)      ("Variants": residual add)
+ *   fgemm_bias_relu_quant     out = e4m3(clamp(scale * max(0, A @ B + bias), +-448))
+ *                                                        ("Variants": quantized output)
+ *
  * Rounding: products are accumulated in fp32; the epilogue runs in fp32; the result is rounded
  * once (round to nearest even) to the output type at the store ("I3. Fuse a GEMM epilogue and
- * change tile scheduling", opening paragraph and "Why the baseline uses FP32").
+ * change tile scheduling", opening paragraph and "Why the baseline uses FP32").  On the tensor-core
+ * path with K <= 1024 the fp32 sum starts at the bias instead of taking it last (the same value up
+ * to the rounding order; fgemm_opts.bias_init selects either order).
  *
  * K = 0 is valid: the zero accumulator still passes through the epilogue, so bias+ReLU gives
  * ReLU(bias) on every row ("I3 ...", "Implement in stages", stage 2); the gate gives
@@ -34,7 +40,9 @@
  *              The tensor-core path additionally needs 16-byte aligned base pointers and row
  *              strides (K and N multiples of 8); other shapes run on the generic CUDA-core path,
  *              which is not an error.
- *   Threading  no global mutable state apart from the per-device error word.
+ *   Threading  no per-call global state: per device, the library keeps the error word, cached
+ *              launch attributes (set once, idempotent) and, for fgemm_unfused_bias_relu_noalloc
+ *              only, its scratch array.
  */
 #ifndef FGEMM_H
 #define FGEMM_H
