@@ -37,10 +37,16 @@ def _cases(n=48, seed=2024):
         M = int(rng.integers(1, 700))
         N = int(rng.integers(1, 256)) * 8 if aligned else int(rng.integers(1, 2000))
         K = int(rng.integers(0, 80)) * 8 if aligned else int(rng.integers(0, 600))
-        epi = ["relu", "gate", "resid", "quant"][int(rng.integers(0, 4))]
-        ab = [F16, BF16][int(rng.integers(0, 2))]
-        bt = [ab, F32][int(rng.integers(0, 2))]
-        ot = [ab, F32][int(rng.integers(0, 2))] if epi != "quant" else E4M3
+        if rng.random() < 0.25:  # fp8 e4m3 operands: bias + ReLU or the quantized output
+            epi = ["relu", "quant"][int(rng.integers(0, 2))]
+            ab = E4M3
+            bt = [F32, BF16][int(rng.integers(0, 2))]
+            ot = [BF16, F32][int(rng.integers(0, 2))] if epi != "quant" else E4M3
+        else:
+            epi = ["relu", "gate", "resid", "quant"][int(rng.integers(0, 4))]
+            ab = [F16, BF16][int(rng.integers(0, 2))]
+            bt = [ab, F32][int(rng.integers(0, 2))]
+            ot = [ab, F32][int(rng.integers(0, 2))] if epi != "quant" else E4M3
         if epi == "quant" and N % 16:
             N += 16 - N % 16 if aligned else 0
         out.append((i, M, N, K, epi, ab, bt, ot))
@@ -57,8 +63,7 @@ def test_random_shapes_exact(case):
     Y = up(p.Y, ab) if epi in ("gate", "resid") else None
     if ot == E4M3:
         out = torch.empty(M, N, dtype=torch.uint8, device="cuda")
-        w = (fg.F16 if ab == F16 else fg.BF16) | (fg.BIAS_F32 if bt == F32 else 0) | fg.OUT_E4M3
-        fg.fgemm_bias_relu_quant(A, B, bias, out, M, N, K, w, 0.25)
+        fg.fgemm_bias_relu_quant(A, B, bias, out, M, N, K, dtype_word(ab, bt, E4M3), 0.25)
         torch.cuda.synchronize()
         ref = oracle.bias_relu_quant(p.A, p.B, p.bias, M, N, K, ab, bt, 0.25).out
         got = out.cpu().numpy()
