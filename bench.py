@@ -561,6 +561,10 @@ def run_sweep(args):
         assert fg.fgemm_device_status(stream) == 0
         del prob
         torch.cuda.empty_cache()
+        if args.sweep_cpu:  # the fp64 oracle on the host cores, a bounded row sample (~2 s)
+            r = dict(cpu_baseline(w, target_s=2.0), workload=name, variant="cpu_oracle")
+            results.append(r)
+            print(json.dumps(r), file=sys.stderr, flush=True)
     os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
     with open(os.path.join(ROOT, "gpurun_out", "sweep.json"), "w") as f:
         json.dump({"peaks": pk, "peak_source": pk_src, "results": results}, f, indent=1)
@@ -578,6 +582,8 @@ def main():
                     help="unfused: time the GEMM -> elementwise chain instead (traffic comparison)")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-workloads", default="")
+    ap.add_argument("--sweep-cpu", action="store_true",
+                    help="also time the fp64 oracle on a bounded sample of every swept workload")
     ap.add_argument("--sweep-variants", default="",
                     help='JSON list of fgemm_opts dicts (null = defaults) replacing the sweep\'s own')
     args = ap.parse_args()
