@@ -280,10 +280,6 @@ __device__ __forceinline__ float2 unpack2(uint32_t v, bool bf16) {
   __half2 h = *reinterpret_cast<__half2*>(&v);
   return __half22float2(h);
 }
-__device__ __forceinline__ float to_f32(uint16_t v, bool bf16) {
-  if (bf16) return __uint_as_float(static_cast<uint32_t>(v) << 16);
-  return __half2float(__ushort_as_half(v));
-}
 
 }  // namespace fgemm
 

@@ -3,7 +3,6 @@ skinny kernels is bounded.  A diagnostic option makes the first CTA announce a s
 it never issues (a barrier that nothing completes); the wait must expire after timeout_ms, the
 kernel must drain and exit, fgemm_device_status must report FGEMM_ERR_TIMEOUT, and the context
 must stay usable for the next call."""
-import numpy as np
 import pytest
 
 import oracle

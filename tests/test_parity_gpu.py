@@ -1,5 +1,4 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle on the same seeded inputs."""
-import itertools
 
 import numpy as np
 import pytest
