@@ -242,7 +242,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t pol = policy_evict_normal();
+      // L2 hints: A (a few MB, read by every column of tiles) is kept; B's boxes are read by the
+      // M-tiles of one band in quick succession and then not again, so they go first (measured:
+      // 4096^3 83.7 -> 82.4 us, GLU block K = 4096 120.1 -> 118.7 us).
+      const uint64_t pol_a = policy_evict_last();
+      const uint64_t pol_b = policy_evict_first();
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       bool ok = true;
@@ -272,15 +276,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t lfb = lead_bar(BAR_FULL + stage);
 #pragma unroll
             for (int r = 0; r < KSUB; ++r)
-              tma_load_2d_pair(a_dst + r * A_ROW_BYTES, &tmA, lfb, kb * KB_ELEMS + r * KROW, m0, pol);
+              tma_load_2d_pair(a_dst + r * A_ROW_BYTES, &tmA, lfb, kb * KB_ELEMS + r * KROW, m0, pol_a);
             for (int c = 0; c < boxes; ++c)
-              tma_load_2d_pair(b_dst + c * BBOX, &tmB, lfb, nb0 + BOXC * c, kb * KB_ELEMS, pol);
+              tma_load_2d_pair(b_dst + c * BBOX, &tmB, lfb, nb0 + BOXC * c, kb * KB_ELEMS, pol_b);
           } else {
 #pragma unroll
             for (int r = 0; r < KSUB; ++r)
-              tma_load_2d(a_dst + r * A_ROW_BYTES, &tmA, fb, kb * KB_ELEMS + r * KROW, m0, pol);
+              tma_load_2d(a_dst + r * A_ROW_BYTES, &tmA, fb, kb * KB_ELEMS + r * KROW, m0, pol_a);
             for (int c = 0; c < boxes; ++c)
-              tma_load_2d(b_dst + c * BBOX, &tmB, fb, nb0 + BOXC * c, kb * KB_ELEMS, pol);
+              tma_load_2d(b_dst + c * BBOX, &tmB, fb, nb0 + BOXC * c, kb * KB_ELEMS, pol_b);
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
