@@ -11,8 +11,8 @@
 //     through a TMA ring into tcgen05.mma (fp32 in TMEM);
 //   * reduces the S partial accumulators through distributed shared memory: rows
 //     [r*W/S, (r+1)*W/S) of the CTA's W = 128 * nt columns belong to CTA r; every CTA pushes its
-//     partial rows from TMEM straight into the owner's shared memory (remote vector stores), and
-//     after a cluster barrier each owner sums its rows locally;
+//     partial rows from TMEM straight into the owner's shared memory (remote vector stores; its
+//     own rows with local stores), and after a cluster barrier each owner sums its rows locally;
 //   * applies the epilogue once, on the complete sum ("Epilogue concept", "Why it cannot move
 //     earlier": ReLU of a partial sum is not ReLU of the sum, and a bias added per partial would be
 //     added S times): x = sum + bias[n], then ReLU or the gate, one rounding, coalesced store.
@@ -31,7 +31,10 @@ constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t B_BOX_BYTES = 64 * 64 * 2;         // 64 K-rows x 64 N-columns
 constexpr uint32_t B_TILE_BYTES = 2 * B_BOX_BYTES;    // 64 x 128: one MMA's worth of B
 constexpr int MAX_MPAD = 128;
-constexpr uint32_t BAR_BYTES = 256;
+// Area after the data: mbarriers, the TMEM address slot (byte 192), the abort flag (byte 200) and
+// the bias of the rows the CTA owns (at most 256 floats, from byte 256).
+constexpr uint32_t OFF_TMEM_SLOT = 192, OFF_ABORT = 200, OFF_BIAS = 256;
+constexpr uint32_t BAR_BYTES = OFF_BIAS + 4 * 256;
 constexpr uint32_t STAGE_AREA_MAX = 196608;           // bytes of stage ring at most
 
 enum { SITE_PROD_EMPTY = 16, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN };
@@ -98,9 +101,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   // barriers: full[0..7], empty[8..15], acc_full 16, mma_done 17
   constexpr int BAR_FULL = 0, BAR_EMPTY = MAX_STAGES, BAR_ACC_FULL = 2 * MAX_STAGES,
                 BAR_MMA_DONE = 2 * MAX_STAGES + 1;
+  static_assert(8 * (2 * MAX_STAGES + 2) <= OFF_TMEM_SLOT, "barrier area");
   uint8_t* bar_area = smem + dbytes;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + 200);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_area + OFF_TMEM_SLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bar_area + OFF_ABORT);
+  float* bias_s = reinterpret_cast<float*>(bar_area + OFF_BIAS);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t S = static_cast<uint32_t>(p.split);
@@ -112,6 +117,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int kb1 = static_cast<int>(static_cast<int64_t>(KB) * (rank + 1) / S);
   const int nkb = kb1 - kb0;
   const uint64_t tmo = p.timeout_ns;
+  const int maxslice = (W + static_cast<int>(S) - 1) / static_cast<int>(S);
+  auto first_row = [&](uint32_t r) { return static_cast<int>(static_cast<uint32_t>(W) * r / S); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -207,6 +214,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       volatile int never = 0;
       mbar_wait(bar(BAR_MMA_DONE), 0, &never, tmo, p.err, SITE_DRAIN);
     }
+  } else if constexpr (EPI != EPI_NONE) {
+    // Epilogue warps, while the main loop runs: the bias of the rows this CTA owns, so that the
+    // final epilogue reads it from shared memory (a global load there, after stores to out that
+    // may alias it, would go to L2 on every pass).
+    const int r0 = first_row(rank), nrows = first_row(rank + 1) - r0;
+    for (int i = static_cast<int>(threadIdx.x) - 64; i < nrows; i += 32 * EPI_WARPS) {
+      const int n = n0 + r0 + i;
+      bias_s[i] = n < p.N ? ld_any(p.bias, n, p.bias_type) : 0.0f;
+    }
   }
 
   // ------------------------------------------------------------ reduction across the cluster
@@ -222,9 +238,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   else
     __syncthreads();
 
-  const int maxslice = (W + static_cast<int>(S) - 1) / static_cast<int>(S);
   const int stride = p.mpad + 4;
-  auto first_row = [&](uint32_t r) { return static_cast<int>(static_cast<uint32_t>(W) * r / S); };
   if (warp >= 2) {
     const int q = warp & 3;
     const bool have = (nkb > 0) && mbar_wait(bar(BAR_ACC_FULL), 0, abort_flag, tmo, p.err,
@@ -238,7 +252,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t slot =
           sbase + 4u * static_cast<uint32_t>(
                            (static_cast<int>(rank) * maxslice + row - first_row(owner)) * stride);
-      const uint32_t dst = (S > 1) ? map_shared_rank(slot, owner) : slot;
+      const bool remote = owner != rank;  // own rows take the local store path
+      const uint32_t dst = remote ? map_shared_rank(slot, owner) : slot;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(t * p.mpad);
       for (int c = 0; c < p.mpad / 16; ++c) {
@@ -254,7 +269,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
           const uint32_t a = dst + 4u * static_cast<uint32_t>(16 * c + j);
-          if (S > 1)
+          if (remote)
             st_shared_cluster_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
                                  __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
           else
@@ -290,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int n = n0 + r0 + nl;
       if (n >= p.N) continue;
       float b = 0.f;
-      if constexpr (EPI != EPI_NONE) b = ld_any(p.bias, n, p.bias_type);  // once, on the full sum
+      if constexpr (EPI != EPI_NONE) b = bias_s[nl];  // once, on the full sum
       const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
