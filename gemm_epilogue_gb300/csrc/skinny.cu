@@ -50,10 +50,15 @@ __host__ __device__ inline int num_stages(int mpad, int nt, int want) {
   return s > cap ? cap : s;
 }
 // Receive area of the cluster reduction, overlaid on the stage ring.
+// Layout recv[src][m][row], rows of an owner's slice fastest, `pitch` floats per m: a warp's store
+// of one m for its 32 consecutive rows is one contiguous 128-byte run, which the cluster store
+// path moves far faster than 32 scattered 16-byte pieces.
+__host__ __device__ inline int recv_pitch(int nt, int split) {
+  const int maxslice = (BN * nt + split - 1) / split;
+  return (maxslice + 3) & ~3;
+}
 __host__ __device__ inline uint32_t recv_bytes(int mpad, int nt, int split) {
-  const int rows = BN * nt;
-  const int maxslice = (rows + split - 1) / split;
-  return static_cast<uint32_t>(split * maxslice * (mpad + 4)) * 4u;
+  return static_cast<uint32_t>(split * mpad * recv_pitch(nt, split)) * 4u;
 }
 // Shared memory before the barriers: the larger of the ring and the reduction's receive area.
 __host__ __device__ inline uint32_t data_bytes(int mpad, int nt, int split, int want) {
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int kb1 = static_cast<int>(static_cast<int64_t>(KB) * (rank + 1) / S);
   const int nkb = kb1 - kb0;
   const uint64_t tmo = p.timeout_ns;
-  const int maxslice = (W + static_cast<int>(S) - 1) / static_cast<int>(S);
+  const int pitch = recv_pitch(nt, static_cast<int>(S));
   auto first_row = [&](uint32_t r) { return static_cast<int>(static_cast<uint32_t>(W) * r / S); };
 
   if (threadIdx.x == 0) {
@@ -228,17 +233,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ------------------------------------------------------------ reduction across the cluster
   // Row n (0 <= n < W) of the CTA's columns is owned by CTA owner(n), the r with
   // W r / S <= n < W (r + 1) / S.  Each CTA pushes its partial row n into the owner's receive area
-  // recv[src][n - first_row(owner)][m] (row stride mpad + 4 floats), which overlays the owner's
-  // stage ring (or extends past it); so the first cluster barrier makes sure every CTA has
-  // finished its main loop
-  // before any push, and the second one that every push has landed before the owners read.
+  // recv[src][m][n - first_row(owner)] (see recv_pitch), which overlays the owner's stage ring
+  // (or extends past it); so the first cluster barrier makes sure every CTA has finished its main
+  // loop before any push, and the second one that every push has landed before the owners read.
   __syncwarp();
   if (S > 1)
     cluster_sync();
   else
     __syncthreads();
 
-  const int stride = p.mpad + 4;
   if (warp >= 2) {
     const int q = warp & 3;
     const bool have = (nkb > 0) && mbar_wait(bar(BAR_ACC_FULL), 0, abort_flag, tmo, p.err,
@@ -249,9 +252,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t owner = (static_cast<uint32_t>(row) * S) / static_cast<uint32_t>(W);
       while (owner + 1 < S && first_row(owner + 1) <= row) ++owner;
       while (owner > 0 && first_row(owner) > row) --owner;
-      const uint32_t slot =
-          sbase + 4u * static_cast<uint32_t>(
-                           (static_cast<int>(rank) * maxslice + row - first_row(owner)) * stride);
+      const uint32_t slot = sbase + 4u * static_cast<uint32_t>(static_cast<int>(rank) * p.mpad * pitch +
+                                                             row - first_row(owner));
       const bool remote = owner != rank;  // own rows take the local store path
       const uint32_t dst = remote ? map_shared_rank(slot, owner) : slot;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
@@ -267,14 +269,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int j = 0; j < 16; ++j) v[j] = 0u;
         }
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-          const uint32_t a = dst + 4u * static_cast<uint32_t>(16 * c + j);
+        for (int j = 0; j < 16; ++j) {  // m = 16 c + j; the warp's lanes write consecutive rows
+          const uint32_t a = dst + 4u * static_cast<uint32_t>((16 * c + j) * pitch);
           if (remote)
-            st_shared_cluster_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                 __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+            st_shared_cluster_f32(a, __uint_as_float(v[j]));
           else
-            st_shared_v4(a, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                         __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+            st_shared_f32(a, __uint_as_float(v[j]));
         }
       }
     }
@@ -296,17 +296,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int idx = t; idx < nrows * m4; idx += 32 * EPI_WARPS) {
       const int nl = idx % nrows;
       const int m = 4 * (idx / nrows);
-      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
       for (uint32_t src = 0; src < S; ++src) {
-        const float4 v = *reinterpret_cast<const float4*>(
-            recv + (static_cast<int>(src) * maxslice + nl) * stride + m);
-        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+        const float* col = recv + (static_cast<int>(src) * p.mpad + m) * pitch + nl;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s4[e] += col[e * pitch];
       }
       const int n = n0 + r0 + nl;
       if (n >= p.N) continue;
       float b = 0.f;
       if constexpr (EPI != EPI_NONE) b = bias_s[nl];  // once, on the full sum
-      const float s4[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         if (m + e >= p.M) break;
