@@ -26,8 +26,13 @@ namespace sk {
 constexpr int BN = 128;  // output columns per MMA (MMA M)
 constexpr int BK = 64;
 constexpr int MAX_STAGES = 8;
-constexpr int EPI_WARPS = 4;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+// Epilogue warps: one per TMEM lane quadrant (warp w reads lanes 32 (w % 4) ..), or two that split
+// the accumulator's 16-column chunks between them when the reduction and the final epilogue
+// carry enough work for the extra warps to pay (M padded to 64 or more); the launch picks the
+// block size and the kernel reads it back from blockDim.
+constexpr int MAX_EPI_WARPS = 8;
+constexpr int MAX_THREADS = 64 + 32 * MAX_EPI_WARPS;
+__host__ __device__ inline int epi_warps_for(int mpad) { return mpad >= 64 ? 8 : 4; }
 constexpr uint32_t B_BOX_BYTES = 64 * 64 * 2;         // 64 K-rows x 64 N-columns
 constexpr uint32_t B_TILE_BYTES = 2 * B_BOX_BYTES;    // 64 x 128: one MMA's worth of B
 constexpr int MAX_MPAD = 128;
@@ -90,7 +95,7 @@ __device__ __forceinline__ void st_any(void* p, int64_t i, int type, float v) {
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(MAX_THREADS, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
                   const SkParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -113,6 +118,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   float* bias_s = reinterpret_cast<float*>(bar_area + OFF_BIAS);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int epi_threads = static_cast<int>(blockDim.x) - 64;
   const uint32_t S = static_cast<uint32_t>(p.split);
   const uint32_t rank = (S > 1) ? cluster_ctarank() : 0u;
   const int W = BN * nt;  // output columns of this CTA
@@ -224,7 +230,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // final epilogue reads it from shared memory (a global load there, after stores to out that
     // may alias it, would go to L2 on every pass).
     const int r0 = first_row(rank), nrows = first_row(rank + 1) - r0;
-    for (int i = static_cast<int>(threadIdx.x) - 64; i < nrows; i += 32 * EPI_WARPS) {
+    for (int i = static_cast<int>(threadIdx.x) - 64; i < nrows; i += epi_threads) {
       const int n = n0 + r0 + i;
       bias_s[i] = n < p.N ? ld_any(p.bias, n, p.bias_type) : 0.0f;
     }
@@ -244,6 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp >= 2) {
     const int q = warp & 3;
+    const int half = (warp - 2) / 4, halves = epi_threads / 128;
     const bool have = (nkb > 0) && mbar_wait(bar(BAR_ACC_FULL), 0, abort_flag, tmo, p.err,
                                              SITE_EPI_ACC_FULL);
     tc_fence_after();
@@ -258,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t dst = remote ? map_shared_rank(slot, owner) : slot;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(t * p.mpad);
-      for (int c = 0; c < p.mpad / 16; ++c) {
+      for (int c = half; c < p.mpad / 16; c += halves) {
         uint32_t v[16];
         if (have) {
           __syncwarp();
@@ -293,7 +300,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r0 = first_row(rank), nrows = first_row(rank + 1) - r0;
     const int m4 = (p.M + 3) / 4;
     const float* recv = reinterpret_cast<const float*>(smem);
-    for (int idx = t; idx < nrows * m4; idx += 32 * EPI_WARPS) {
+    for (int idx = t; idx < nrows * m4; idx += epi_threads) {
       const int nl = idx % nrows;
       const int m = 4 * (idx / nrows);
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -344,7 +351,7 @@ cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkPar
   if (smem > 232448) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(ctas));
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(static_cast<unsigned>(64 + 32 * epi_warps_for(p.mpad)));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
