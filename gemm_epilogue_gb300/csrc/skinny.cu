@@ -295,34 +295,38 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
     __syncthreads();
 
   // ------------------------------------------------------------ epilogue on the full sums
+  // Lane l of every epilogue warp takes owned rows l, l + 32, ..; the warps take the groups of 4
+  // rows of out in turn.  Each thread sums the S partials of its element in source order and
+  // applies the epilogue once.
   if (warp >= 2) {
-    const int t = threadIdx.x - 64;
     const int r0 = first_row(rank), nrows = first_row(rank + 1) - r0;
     const int m4 = (p.M + 3) / 4;
+    const int ew = epi_threads / 32, wi = warp - 2;
     const float* recv = reinterpret_cast<const float*>(smem);
-    for (int idx = t; idx < nrows * m4; idx += epi_threads) {
-      const int nl = idx % nrows;
-      const int m = 4 * (idx / nrows);
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
-      for (uint32_t src = 0; src < S; ++src) {
-        const float* col = recv + (static_cast<int>(src) * p.mpad + m) * pitch + nl;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s4[e] += col[e * pitch];
-      }
+    for (int nl = lane; nl < nrows; nl += 32) {
       const int n = n0 + r0 + nl;
-      if (n >= p.N) continue;
+      if (n >= p.N) break;
       float b = 0.f;
       if constexpr (EPI != EPI_NONE) b = bias_s[nl];  // once, on the full sum
+      for (int g = wi; g < m4; g += ew) {
+        const int m = 4 * g;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (uint32_t src = 0; src < S; ++src) {
+          const float* col = recv + (static_cast<int>(src) * p.mpad + m) * pitch + nl;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (m + e >= p.M) break;
-        const int64_t o = static_cast<int64_t>(m + e) * p.N + n;
-        float v = s4[e] + b;
-        if constexpr (EPI == EPI_RELU) v = fmaxf(v, 0.0f);
-        if constexpr (EPI == EPI_QUANT) v = fminf(fmaxf(fmaxf(v, 0.0f) * p.out_scale, -448.0f), 448.0f);
-        if constexpr (EPI == EPI_GATE) v = fmaf(v, ld_any(p.Y, o, p.ab_type), v);
-        if constexpr (EPI == EPI_RESID) v = fmaxf(v + ld_any(p.Y, o, p.ab_type), 0.0f);
-        st_any(p.out, o, p.out_type, v);
+          for (int e = 0; e < 4; ++e) s4[e] += col[e * pitch];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (m + e >= p.M) break;
+          const int64_t o = static_cast<int64_t>(m + e) * p.N + n;
+          float v = s4[e] + b;
+          if constexpr (EPI == EPI_RELU) v = fmaxf(v, 0.0f);
+          if constexpr (EPI == EPI_QUANT) v = fminf(fmaxf(fmaxf(v, 0.0f) * p.out_scale, -448.0f), 448.0f);
+          if constexpr (EPI == EPI_GATE) v = fmaf(v, ld_any(p.Y, o, p.ab_type), v);
+          if constexpr (EPI == EPI_RESID) v = fmaxf(v + ld_any(p.Y, o, p.ab_type), 0.0f);
+          st_any(p.out, o, p.out_type, v);
+        }
       }
     }
   }
