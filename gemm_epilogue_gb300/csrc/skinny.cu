@@ -242,11 +242,13 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   // recv[src][m][n - first_row(owner)] (see recv_pitch), which overlays the owner's stage ring
   // (or extends past it); so the first cluster barrier makes sure every CTA has finished its main
   // loop before any push, and the second one that every push has landed before the owners read.
+  // With S = 1 only this CTA writes its ring, after its accumulator is complete (every load landed,
+  // every MMA done), and the epilogue warps synchronise among themselves (named barrier 1).  No
+  // CTA-wide barrier is used here: the producer and MMA issuer run in single lanes, and a CTA
+  // barrier reached by the other lanes of their warps was measured to complete while those lanes
+  // were still in their loops.
   __syncwarp();
-  if (S > 1)
-    cluster_sync();
-  else
-    __syncthreads();
+  if (S > 1) cluster_sync();
 
   if (warp >= 2) {
     const int q = warp & 3;
@@ -291,8 +293,8 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   __syncwarp();
   if (S > 1)
     cluster_sync();
-  else
-    __syncthreads();
+  else if (warp >= 2)
+    named_bar_sync(1, static_cast<uint32_t>(epi_threads));
 
   // ------------------------------------------------------------ epilogue on the full sums
   // Lane l of every epilogue warp takes owned rows l, l + 32, ..; the warps take the groups of 4

@@ -170,6 +170,20 @@ def test_skinny_integer_bit_exact(M, N, K, split, gate, tiles):
             pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
 
 
+@pytest.mark.parametrize("M,N,K,tiles", [(64, 520, 4096, 1), (128, 264, 2048, 1), (16, 1032, 8192, 2)])
+def test_skinny_single_cta_long_k_bit_exact(M, N, K, tiles):
+    # split 1 (no cluster) with long main loops: the epilogue warps synchronise among themselves
+    # while the producer and MMA lanes may still be in their loops
+    p = gen.integer_problem(M, N, K, BF16, BF16, seed=M + N + K)
+    out, path = run_fused(p, M, N, K, BF16, BF16, BF16, opts={"split_k": 1, "skinny_tiles": tiles})
+    assert path == fg.PATH_SKINNY
+    ref = oracle_run(p, M, N, K, BF16, BF16, BF16)
+    got = down(out, BF16)
+    if not np.array_equal(got, ref.out):
+        bad = np.argwhere(got != ref.out)
+        pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
+
+
 def test_skinny_auto_split_and_coverage():
     M, N, K = 16, 2056, 4096
     p = gen.random_problem(M, N, K, BF16, BF16, seed=12)
