@@ -198,6 +198,7 @@ struct TcPlan {
   int last_width, gran;  // width of the last column of tiles, and the width it is rounded up to
   int y_blocks;          // staged Y blocks per epilogue warp (gate / residual, 16-bit out)
   int k_rows;            // 128-byte K rows per ring stage
+  bool row_bars;         // a full barrier per K row of a stage
 };
 
 TcPlan plan_tc(const Call& c, DeviceInfo* d) {
@@ -278,6 +279,9 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
     t.k_rows = want ? want : ((staged_y && t.y_blocks > 0) ? 1 : 2);
     if (t.y_blocks == 2) t.k_rows = 1;
   }
+  // Each K row of a two-row stage on its own full barrier: measured faster with fp8 operands and
+  // with staged Y, slower on the plain 16-bit FFN shape, equal on 4096^3.
+  t.row_bars = t.k_rows > 1 && (c.t.ab == ELEM_E4M3 || staged_y);
   return t;
 }
 
@@ -329,7 +333,8 @@ int run_tc(const Call& c, DeviceInfo* d) {
   const uint32_t out_box_cols = 128u / static_cast<uint32_t>(elem_bytes(c.t.out));
   const uint32_t kb_elems = 128u / static_cast<uint32_t>(elem_bytes(c.t.ab));  // one 128-B row
   if (!encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, BM, kb_elems) ||
-      !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, kb_elems * static_cast<uint32_t>(t.k_rows), kb_elems) ||
+      !encode_2d(&tmB, c.t.ab, c.B, c.K, c.N,
+                 kb_elems * static_cast<uint32_t>(t.row_bars ? 1 : t.k_rows), kb_elems) ||
       !encode_2d(&tmO, c.t.out, c.out, c.M, c.N, 32, out_box_cols))
     return FGEMM_ERR_LAUNCH;
   if ((c.epi == EPI_GATE || c.epi == EPI_RESID) && c.t.out != ELEM_F32) {
@@ -357,6 +362,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.bias_init = (c.epi != EPI_NONE && (bi == 1 || (bi == 0 && c.K <= 1024))) ? 1 : 0;
   p.y_blocks = t.y_blocks;
   p.k_rows = t.k_rows;
+  p.row_bars = t.row_bars ? 1 : 0;
   // 16 M-tiles per band: measured best on the 8192-row FFN (577-583 vs 595-605 us for 8); the
   // square and GLU shapes have at most 16 tile rows, so every value from there up is the same order
   p.group = (c.opts && c.opts->group_m > 0) ? c.opts->group_m : 16;

@@ -29,6 +29,7 @@ struct TcParams {
   int bias_init;   // 1: the accumulator starts at the bias (written into TMEM before the K loop)
   int y_blocks;    // gate / residual with 16-bit out on CTA pairs: Y blocks per epilogue warp (1, 2)
   int k_rows;      // CTA pairs: 128-byte K rows per ring stage (1, 2)
+  int row_bars;    // k_rows 2: a full barrier per K row of a stage (B copied one K row at a time)
   int ab_bf16;     // operand (and Y) type: 0 = f16, 1 = bf16
   int ab_f8;       // 1: A and B are fp8 e4m3 (kind::f8f6f4 MMAs, 128-element K blocks)
   int bias_type;   // Elem of the bias

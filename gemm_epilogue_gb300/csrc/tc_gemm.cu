@@ -80,6 +80,7 @@ struct Cfg {
   static constexpr int STAGES =
       RING_BUDGET / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : static_cast<int>(RING_BUDGET / STAGE_BYTES);
   static_assert(STAGES >= 2, "at least two stages in the ring");
+  static_assert(STAGES * KSUB <= MAX_STAGES, "one full barrier per stage and K row");
   static constexpr uint32_t SMEM_A = 0;
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
   static constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
@@ -88,7 +89,8 @@ struct Cfg {
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
 };
 
-// barrier slots (uint64 each) inside the SMEM_BAR area
+// barrier slots (uint64 each) inside the SMEM_BAR area; full barriers BAR_FULL + stage * KSUB +
+// (row with per-row barriers, else 0), empty barriers per stage
 constexpr int BAR_FULL = 0;
 constexpr int BAR_EMPTY = MAX_STAGES;
 constexpr int BAR_ACC_FULL = 2 * MAX_STAGES;
@@ -179,6 +181,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int KB_ELEMS = KSUB * KROW;                   // K per stage
   constexpr int BOXC = 128 / EB;                          // B box columns
   constexpr uint32_t BBOX = static_cast<uint32_t>(KB_ELEMS * BOXC * EB);  // KSUB x 8 KB / 16 KB
+  // With p.row_bars (two K rows per stage) each K row of a stage completes on its own full barrier,
+  // so that the MMAs on the first row start while the second is still landing; B's column boxes
+  // are then copied one K row at a time (BBOX_ROW bytes each, stacked at the 1024-byte-aligned
+  // offsets one two-row box would fill: the same swizzled layout).  Measured on GB300: fp8
+  // operands 4096^3 49.3 -> 48.4 us, GLU block K = 4096 120.0 -> 118.4 us; on 16-bit operands
+  // without staged Y 4096^3 equal and FFN 8192 x 14336 x 4096 543 -> 548 us, so the host enables
+  // it for fp8 operands and staged Y only.
+  constexpr uint32_t BBOX_ROW = BBOX / KSUB;
+  const bool rowbar = KSUB > 1 && p.row_bars != 0;
+  const int nfb = rowbar ? KSUB : 1;  // full barriers per stage
   constexpr int KSTEP = F8 ? 32 : 16;                     // K per MMA instruction
   constexpr int KPR = KROW / KSTEP;                       // MMAs per K row (4)
   constexpr uint32_t B_KADV = static_cast<uint32_t>(KSTEP) * 128u;  // MN-major B bytes per MMA
@@ -208,7 +220,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(BAR_FULL + s), 1);
+      for (int r = 0; r < KSUB; ++r) mbar_init(bar(BAR_FULL + s * KSUB + r), 1);
       mbar_init(bar(BAR_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -257,34 +269,42 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int cols = PAIR ? wk.width / 2 : wk.width;
         const int nb0 = wk.col0 + static_cast<int>(rank) * cols;
         const int boxes = (cols + BOXC - 1) / BOXC;
-        const uint32_t tx = (PAIR ? 2u : 1u) * (A_STAGE_BYTES + static_cast<uint32_t>(boxes) * BBOX);
+        // bytes per full barrier: one K row, or the whole stage (both CTAs of a pair)
+        const uint32_t tx = (PAIR ? 2u : 1u) * (A_ROW_BYTES + static_cast<uint32_t>(boxes) * BBOX_ROW) *
+                            static_cast<uint32_t>(KSUB / nfb);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err,
                          SITE_PROD_EMPTY)) {
             ok = false;
             break;
           }
-          const uint32_t fb = bar(BAR_FULL + stage);
-          // the even CTA's full barrier counts both CTAs' bytes of the stage
-          if (leader) mbar_arrive_expect_tx(fb, tx);
           const uint32_t a_dst = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_dst = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
           // diagnostic stall: announce the stage's bytes but never load them
           const bool stall = p.inject_stall && blockIdx.x == 0 && t == unit && kb == 0;
-          if (stall) {
-          } else if constexpr (PAIR) {
-            const uint32_t lfb = lead_bar(BAR_FULL + stage);
+          // the even CTA's full barriers count both CTAs' bytes
+          if (leader)
+            for (int f = 0; f < nfb; ++f) mbar_arrive_expect_tx(bar(BAR_FULL + stage * KSUB + f), tx);
 #pragma unroll
-            for (int r = 0; r < KSUB; ++r)
-              tma_load_2d_pair(a_dst + r * A_ROW_BYTES, &tmA, lfb, kb * KB_ELEMS + r * KROW, m0, pol_a);
-            for (int c = 0; c < boxes; ++c)
-              tma_load_2d_pair(b_dst + c * BBOX, &tmB, lfb, nb0 + BOXC * c, kb * KB_ELEMS, pol_b);
-          } else {
-#pragma unroll
-            for (int r = 0; r < KSUB; ++r)
-              tma_load_2d(a_dst + r * A_ROW_BYTES, &tmA, fb, kb * KB_ELEMS + r * KROW, m0, pol_a);
-            for (int c = 0; c < boxes; ++c)
-              tma_load_2d(b_dst + c * BBOX, &tmB, fb, nb0 + BOXC * c, kb * KB_ELEMS, pol_b);
+          for (int r = 0; r < KSUB; ++r) {
+            const int fi = BAR_FULL + static_cast<int>(stage) * KSUB + (rowbar ? r : 0);
+            const int kx = kb * KB_ELEMS + r * KROW;
+            // B: per K row with row barriers, else the whole stage's rows with the first A row
+            const bool b_now = rowbar || r == 0;
+            const uint32_t b_off = rowbar ? r * BBOX_ROW : 0u;
+            if (stall) {
+            } else if constexpr (PAIR) {
+              const uint32_t lfb = lead_bar(fi);
+              tma_load_2d_pair(a_dst + r * A_ROW_BYTES, &tmA, lfb, kx, m0, pol_a);
+              if (b_now)
+                for (int c = 0; c < boxes; ++c)
+                  tma_load_2d_pair(b_dst + c * BBOX + b_off, &tmB, lfb, nb0 + BOXC * c, kx, pol_b);
+            } else {
+              tma_load_2d(a_dst + r * A_ROW_BYTES, &tmA, bar(fi), kx, m0, pol_a);
+              if (b_now)
+                for (int c = 0; c < boxes; ++c)
+                  tma_load_2d(b_dst + c * BBOX + b_off, &tmB, bar(fi), nb0 + BOXC * c, kx, pol_b);
+            }
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -299,7 +319,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       // peer resident until then.
       if (leader)
         for (int s = 0; s < STAGES; ++s)
-          if ((issued >> s) & 1u) drain_wait(bar(BAR_FULL + s), (issued_parity >> s) & 1u, tmo, p.err);
+          if ((issued >> s) & 1u)
+            for (int f = 0; f < nfb; ++f)
+              drain_wait(bar(BAR_FULL + s * KSUB + f), (issued_parity >> s) & 1u, tmo, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -322,24 +344,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(bar(BAR_FULL + stage), phase, abort_flag, tmo, p.err, SITE_MMA_FULL)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           const uint32_t a_addr = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_addr = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
 #pragma unroll
-          for (int k = 0; k < KB_ELEMS / KSTEP; ++k) {  // 32 bytes of K per MMA
-            const uint64_t ad =
-                sdesc_sw128(a_addr + (k / KPR) * A_ROW_BYTES + 32u * (k % KPR), 16u, 1024u);
-            const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, p.b_lbo, p.b_sbo);
-            const uint32_t acc = (p.bias_init | kb | k) != 0 ? 1u : 0u;
-            if constexpr (F8)
-              umma_f8_cg<CG>(d_tmem, ad, bd, idesc, acc);
-            else
-              umma_f16_cg<CG>(d_tmem, ad, bd, idesc, acc);
+          for (int r = 0; r < KSUB; ++r) {  // with row barriers each K row as soon as it has landed
+            if (r == 0 || rowbar) {
+              if (!mbar_wait(bar(BAR_FULL + static_cast<int>(stage) * KSUB + (rowbar ? r : 0)), phase,
+                             abort_flag, tmo, p.err, SITE_MMA_FULL)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int k = r * KPR; k < (r + 1) * KPR; ++k) {  // 32 bytes of K per MMA
+              const uint64_t ad =
+                  sdesc_sw128(a_addr + (k / KPR) * A_ROW_BYTES + 32u * (k % KPR), 16u, 1024u);
+              const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, p.b_lbo, p.b_sbo);
+              const uint32_t acc = (p.bias_init | kb | k) != 0 ? 1u : 0u;
+              if constexpr (F8)
+                umma_f8_cg<CG>(d_tmem, ad, bd, idesc, acc);
+              else
+                umma_f16_cg<CG>(d_tmem, ad, bd, idesc, acc);
+            }
           }
+          if (!ok) break;
           umma_commit_cg<CG>(bar(BAR_EMPTY + stage), kPair);  // stage free (both CTAs) once read
           if (++stage == STAGES) {
             stage = 0;
