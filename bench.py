@@ -260,6 +260,35 @@ def time_steps(prob, steps, warmup, stream, opts=None, unfused=False, barrier=No
     return start.elapsed_time(end) / steps, path
 
 
+def time_steps_graph(prob, steps, warmup, stream, barrier=None):
+    """The timed steps of the bench line: `warmup` untimed calls on the stream, then the next
+    `steps` calls (the same rotation of input sets as the stream loop) captured once in a CUDA
+    graph and replayed once between CUDA events on the launching stream, so that the host's and
+    the driver's per-launch gaps do not sit between the steps.  Every step runs in full."""
+    import torch
+    path = None
+    for i in range(warmup):
+        path = prob.call(i, stream.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(steps):
+            path = prob.call(warmup + i, stream.cuda_stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        start.record(stream)
+        g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end) / steps, path
+
+
 def time_graph(prob, steps, warmup, stream, opts=None, reps=5):
     """Device time per call with host launch overhead removed: `steps` calls captured once in a
     CUDA graph, the graph replayed `reps` times between CUDA events."""
@@ -411,9 +440,18 @@ def run_ours(args):
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     unfused = args.variant == "unfused"
-    ms, path = time_steps(prob, args.steps, args.warmup, stream, barrier=barrier, unfused=unfused)
+    if unfused:  # the library's comparison chain: launched from the stream loop
+        ms, path = time_steps(prob, args.steps, args.warmup, stream, barrier=barrier, unfused=True)
+        ms_loop = ms
+        launch = "stream loop"
+    else:
+        ms, path = time_steps_graph(prob, args.steps, args.warmup, stream, barrier=barrier)
+        # the same steps launched one by one from the host, for comparison
+        ms_loop, _ = time_steps(prob, args.steps, 0, stream, barrier=barrier)
+        launch = "CUDA graph of the timed steps, replayed once"
     clocks = sampler.stop() if sampler else None
     ms = slowest_rank(dist, ms, dev)
+    ms_loop = slowest_rank(dist, ms_loop, dev)
     e2e_ms, h2d, d2h = e2e_steps(prob, max(3, min(args.steps, 20)), stream)
     e2e_ms = slowest_rank(dist, e2e_ms, dev)
     assert fg.fgemm_device_status(stream) == 0
@@ -449,7 +487,8 @@ def run_ours(args):
                    "epilogue": w.epilogue,
                    "out": gen.TYPE_NAMES[w.out_type], "bias": gen.TYPE_NAMES[w.bias_type],
                    "path": fg.PATH_NAMES.get(path, str(path)), "plan": prob.plan(),
-                   "parallelism": f"replicas{world}",
+                   "parallelism": f"replicas{world}", "launch": launch,
+                   "stream_loop_ms_per_step": ms_loop,
                    "l2": f"inputs rotate over {len(prob.sets)} sets of {prob.set_bytes / 1e6:.1f} MB "
                          f"(> 2 x L2 {l2 / 1e6:.0f} MB)"},
         "pct_of_peak": 100.0 * tflops / pk["bf16_tflops"],
