@@ -604,9 +604,11 @@ def run_sweep(args):
             r = dict(cpu_baseline(w, target_s=2.0), workload=name, variant="cpu_oracle")
             results.append(r)
             print(json.dumps(r), file=sys.stderr, flush=True)
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    with open(os.path.join(ROOT, "gpurun_out", "sweep.json"), "w") as f:
-        json.dump({"peaks": pk, "peak_source": pk_src, "results": results}, f, indent=1)
+    if args.sweep_out:  # the whole sweep as one JSON document
+        d = os.path.dirname(os.path.abspath(args.sweep_out))
+        os.makedirs(d, exist_ok=True)
+        with open(args.sweep_out, "w") as f:
+            json.dump({"peaks": pk, "peak_source": pk_src, "results": results}, f, indent=1)
 
 
 def main():
@@ -621,6 +623,8 @@ def main():
                     help="unfused: time the GEMM -> elementwise chain instead (traffic comparison)")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-workloads", default="")
+    ap.add_argument("--sweep-out", default="",
+                    help="also write the sweep's results as one JSON file at this path")
     ap.add_argument("--sweep-cpu", action="store_true",
                     help="also time the fp64 oracle on a bounded sample of every swept workload")
     ap.add_argument("--sweep-variants", default="",
