@@ -11,8 +11,10 @@
 //     through a TMA ring into tcgen05.mma (fp32 in TMEM);
 //   * reduces the S partial accumulators through distributed shared memory: rows
 //     [r*W/S, (r+1)*W/S) of the CTA's W = 128 * nt columns belong to CTA r; every CTA pushes its
-//     partial rows from TMEM straight into the owner's shared memory (remote vector stores; its
-//     own rows with local stores), and after a cluster barrier each owner sums its rows locally;
+//     partial rows from TMEM straight into the owner's shared memory (remote stores laid out so
+//     that each warp store is one contiguous run; its own rows with local stores), and after a
+//     cluster barrier each owner sums its rows locally; four epilogue warps, or eight (two per
+//     TMEM lane quadrant) when M is padded to 64 or more;
 //   * applies the epilogue once, on the complete sum ("Epilogue concept", "Why it cannot move
 //     earlier": ReLU of a partial sum is not ReLU of the sum, and a bias added per partial would be
 //     added S times): x = sum + bias[n], then ReLU or the gate, one rounding, coalesced store.
