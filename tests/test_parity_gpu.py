@@ -212,6 +212,7 @@ def test_skinny_matches_square_tile_path():
 
 RESID_CASES = [  # M, N, K, opts, expected path
     (300, 520, 200, {"cta_pair": 2}, 1), (300, 520, 200, {"cta_pair": 1}, 1),
+    (300, 520, 2048, {"cta_pair": 2}, 1),  # long K on pairs: R staged a chunk at a time, row barriers
     (777, 1288, 328, None, 1), (16, 1032, 512, None, 2), (100, 264, 72, {"split_k": 3}, 2),
     (7, 9, 13, None, 3), (37, 70, 0, None, 4)]
 
