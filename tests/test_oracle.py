@@ -59,13 +59,15 @@ def test_encode_f16_matches_numpy_direct_rounding(oracle_mod):
         [65504.0, 65519.0, 65520.0, 65536.0, 1e9, -1e9, 2.0 ** -25, 3 * 2.0 ** -25, 0.0, -0.0],
     ])
     got = enc(oracle_mod, x, F16)
-    want = x.astype(np.float16).view(np.uint16)
+    with np.errstate(over="ignore"):  # 65520, 65536, 1e9 overflow to inf on purpose
+        want = x.astype(np.float16).view(np.uint16)
     assert np.array_equal(got, want)
 
 
 def test_encode_bf16_matches_torch_on_float32_values(oracle_mod):
     rng = np.random.default_rng(8)
-    x = (rng.standard_normal(20000) * np.exp2(rng.integers(-140, 128, 20000))).astype(np.float32)
+    with np.errstate(over="ignore"):  # the largest scales overflow float32; those are dropped
+        x = (rng.standard_normal(20000) * np.exp2(rng.integers(-140, 128, 20000))).astype(np.float32)
     x = x[np.isfinite(x)].astype(np.float64)
     got = enc(oracle_mod, x, BF16)
     assert np.array_equal(got, bits_of(x, BF16))
