@@ -260,7 +260,7 @@ def time_steps(prob, steps, warmup, stream, opts=None, unfused=False, barrier=No
     return start.elapsed_time(end) / steps, path
 
 
-def time_steps_graph(prob, steps, warmup, stream, barrier=None):
+def time_steps_graph(prob, steps, warmup, stream, barrier=None, opts=None):
     """The timed steps of the bench line: `warmup` untimed calls on the stream, then the next
     `steps` calls (the same rotation of input sets as the stream loop) captured once in a CUDA
     graph and replayed once between CUDA events on the launching stream, so that the host's and
@@ -268,12 +268,12 @@ def time_steps_graph(prob, steps, warmup, stream, barrier=None):
     import torch
     path = None
     for i in range(warmup):
-        path = prob.call(i, stream.cuda_stream)
+        path = prob.call(i, stream.cuda_stream, opts)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(steps):
-            path = prob.call(warmup + i, stream.cuda_stream)
+            path = prob.call(warmup + i, stream.cuda_stream, opts)
     torch.cuda.synchronize()
     if barrier:
         barrier()
@@ -440,14 +440,15 @@ def run_ours(args):
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     unfused = args.variant == "unfused"
+    opts = json.loads(args.opts) if args.opts else None
     if unfused:  # the library's comparison chain: launched from the stream loop
         ms, path = time_steps(prob, args.steps, args.warmup, stream, barrier=barrier, unfused=True)
         ms_loop = ms
         launch = "stream loop"
     else:
-        ms, path = time_steps_graph(prob, args.steps, args.warmup, stream, barrier=barrier)
+        ms, path = time_steps_graph(prob, args.steps, args.warmup, stream, barrier=barrier, opts=opts)
         # the same steps launched one by one from the host, for comparison
-        ms_loop, _ = time_steps(prob, args.steps, 0, stream, barrier=barrier)
+        ms_loop, _ = time_steps(prob, args.steps, 0, stream, opts=opts, barrier=barrier)
         launch = "CUDA graph of the timed steps, replayed once"
     clocks = sampler.stop() if sampler else None
     ms = slowest_rank(dist, ms, dev)
@@ -486,7 +487,8 @@ def run_ours(args):
         "config": {"workload": w.name, "variant": args.variant, "M": w.M, "N": w.N, "K": w.K,
                    "epilogue": w.epilogue,
                    "out": gen.TYPE_NAMES[w.out_type], "bias": gen.TYPE_NAMES[w.bias_type],
-                   "path": fg.PATH_NAMES.get(path, str(path)), "plan": prob.plan(),
+                   "path": fg.PATH_NAMES.get(path, str(path)), "plan": prob.plan(opts),
+                   "opts": opts,
                    "parallelism": f"replicas{world}", "launch": launch,
                    "stream_loop_ms_per_step": ms_loop,
                    "l2": f"inputs rotate over {len(prob.sets)} sets of {prob.set_bytes / 1e6:.1f} MB "
@@ -621,6 +623,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
                     help="unfused: time the GEMM -> elementwise chain instead (traffic comparison)")
+    ap.add_argument("--opts", default="",
+                    help="fgemm_opts for the timed calls, as JSON (e.g. '{\"group_m\": 8}')")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--sweep-workloads", default="")
     ap.add_argument("--sweep-out", default="",
