@@ -271,7 +271,8 @@ def time_steps_graph(prob, steps, warmup, stream, barrier=None, opts=None):
         path = prob.call(i, stream.cuda_stream, opts)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
+    # thread_local: CUDA calls of other threads (NCCL's watchdog under torchrun) do not void it
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
         for i in range(steps):
             path = prob.call(warmup + i, stream.cuda_stream, opts)
     torch.cuda.synchronize()
@@ -297,7 +298,7 @@ def time_graph(prob, steps, warmup, stream, opts=None, reps=5):
         prob.call(i, stream.cuda_stream, opts)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
         for i in range(steps):
             prob.call(i, stream.cuda_stream, opts)
     g.replay()
