@@ -55,7 +55,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("tiles", ctypes.c_int), ("work_items", ctypes.c_int), ("tail_split", ctypes.c_int),
                 ("resident_pairs", ctypes.c_int), ("last_tile_n", ctypes.c_int),
-                ("y_blocks", ctypes.c_int), ("k_rows", ctypes.c_int), ("reserved", ctypes.c_int)]
+                ("y_blocks", ctypes.c_int), ("k_rows", ctypes.c_int), ("row_barriers", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -86,6 +86,8 @@ _SIGS = {
     "fgemm_status_string": (ctypes.c_char_p, [_int]),
     "fgemm_plan": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int,
                           ctypes.POINTER(Opts), ctypes.POINTER(PlanInfo)]),
+    "fgemm_plan_on": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int,
+                             ctypes.POINTER(Opts), _int, _int, ctypes.POINTER(PlanInfo)]),
     "fgemm_tile_of": (_int, [_i64, _i64, _i64, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
 }
 
@@ -251,7 +253,21 @@ def fgemm_plan(A, B, bias, Y, out, M, N, K, dtype, gate=False, opts=None, epilog
     _check(lib().fgemm_plan(_ptr(A), _ptr(B), _ptr(bias), _ptr(Y), _ptr(out), M, N, K, dtype,
                             epi, ctypes.byref(o) if o else None, ctypes.byref(info)),
            "fgemm_plan")
-    return {name: getattr(info, name) for name, _ in PlanInfo._fields_ if name != "reserved"}
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
+
+
+def fgemm_plan_on(A, B, bias, Y, out, M, N, K, dtype, num_sms, resident_pairs, gate=False,
+                  opts=None, epilogue=None) -> dict:
+    """fgemm_plan for a device with `num_sms` SMs and `resident_pairs` resident CTA pairs,
+    computed on the host (no GPU needed); the buffers (ints are fine) are checked for alignment."""
+    info = PlanInfo()
+    o = _opts(opts)
+    epi = epilogue if epilogue is not None else (EPI_GATE if gate else EPI_RELU)
+    _check(lib().fgemm_plan_on(_ptr(A), _ptr(B), _ptr(bias), _ptr(Y), _ptr(out), M, N, K, dtype,
+                               epi, ctypes.byref(o) if o else None, num_sms, resident_pairs,
+                               ctypes.byref(info)),
+           "fgemm_plan_on")
+    return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
 
 
 def fgemm_tile_of(t, tiles_m, tiles_n, group) -> tuple[int, int]:

@@ -201,14 +201,22 @@ struct TcPlan {
   bool row_bars;         // a full barrier per K row of a stage
 };
 
-TcPlan plan_tc(const Call& c, DeviceInfo* d) {
+// What the planners need to know about the device: its SM count and how many CTA pairs of the
+// tensor-core kernel can be resident at once (< 0: ask the device when pairs are planned).
+struct DevShape {
+  int num_sms;
+  int resident_pairs;
+};
+DevShape shape_of(const DeviceInfo* d) { return DevShape{d->num_sms, -1}; }
+
+TcPlan plan_tc(const Call& c, const DevShape& d) {
   TcPlan t{};
   const int mode = c.opts ? c.opts->cta_pair : 0;
   // Pairs halve the B bytes each SM stages per MMA, which pays when the main loop is long; with
   // at most 8 K blocks per tile (K <= 512) the per-tile hand-offs dominate and single CTAs are as
   // fast or faster (measured on the GLU block, M = 1024, N = 21568: K = 256 29.9 vs 34.0 us,
   // K = 512 36.9 vs 37.2 us, K = 1024 54.4 vs 45.3 us).
-  t.pair = (mode == 2) || (mode == 0 && c.M > 128 && c.K > 512 && d->num_sms >= 2);
+  t.pair = (mode == 2) || (mode == 0 && c.M > 128 && c.K > 512 && d.num_sms >= 2);
   const int TILE_M = t.pair ? 2 * tc_block_m() : tc_block_m(), BN = tc_block_n();
   t.tiles_m = static_cast<int>((c.M + TILE_M - 1) / TILE_M);
   t.tiles_n = static_cast<int>((c.N + BN - 1) / BN);
@@ -218,9 +226,9 @@ TcPlan plan_tc(const Call& c, DeviceInfo* d) {
   // persistent grid: one CTA (or CTA pair) per SM (pair of SMs) that can be resident at once,
   // never more than the tiles
   const int per_unit = t.pair ? 2 : 1;
-  int units = d->num_sms / per_unit;
+  int units = d.num_sms / per_unit;
   if (t.pair) {
-    t.resident = tc_max_active_pairs(c.epi, c.t.out);
+    t.resident = d.resident_pairs >= 0 ? d.resident_pairs : tc_max_active_pairs(c.epi, c.t.out);
     if (t.resident > 0 && t.resident < units) units = t.resident;
   }
   if (c.opts && c.opts->max_ctas > 0 && c.opts->max_ctas / per_unit < units)
@@ -289,7 +297,7 @@ struct SkPlan {
   int mpad, nt, tmem_cols, tiles_n, groups, split, stages;
 };
 
-SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
+SkPlan plan_skinny(const Call& c, const DevShape& d) {
   // Default shape of the grid (measured on GB300 for N = K = 8192, M = 1 .. 128): every CTA must
   // be resident at once, two per SM, so the ring is at most 4 stages and small enough that two
   // CTAs fit on an SM, and K is split until the clusters cover 2 x SMs.  One 128-column tile per
@@ -305,7 +313,7 @@ SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
     s.groups = (s.tiles_n + nt - 1) / nt;
     int split = (c.opts && c.opts->split_k > 0) ? c.opts->split_k : 0;
     if (split == 0) {
-      split = (2 * d->num_sms) / (s.groups > 0 ? s.groups : 1);
+      split = (2 * d.num_sms) / (s.groups > 0 ? s.groups : 1);
       if (split > kb / 4) split = kb / 4;
       if (split > 8) split = 8;
       if (split < 1) split = 1;
@@ -325,7 +333,7 @@ SkPlan plan_skinny(const Call& c, DeviceInfo* d) {
 }
 
 int run_tc(const Call& c, DeviceInfo* d) {
-  const TcPlan t = plan_tc(c, d);
+  const TcPlan t = plan_tc(c, shape_of(d));
   if (t.num_tiles < 0) return FGEMM_ERR_INVALID_VALUE;
   const int BM = tc_block_m(), BN = tc_block_n();
   const int TILE_M = t.pair ? 2 * BM : BM;
@@ -388,7 +396,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
 }
 
 int run_skinny(const Call& c, DeviceInfo* d) {
-  const SkPlan s = plan_skinny(c, d);
+  const SkPlan s = plan_skinny(c, shape_of(d));
   CUtensorMap tmB, tmA;
   if (!encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
       !encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, static_cast<uint32_t>(s.mpad), 64))
@@ -644,9 +652,14 @@ const char* fgemm_status_string(int s) {
   }
 }
 
-int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
-               int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
-               fgemm_plan_info* info) {
+}  // extern "C"
+
+namespace {
+
+// fgemm_plan / fgemm_plan_on: the plan for the device `shape` (nullptr: the current device).
+int plan_info(const void* A, const void* B, const void* bias, const void* Y, const void* out,
+              int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
+              const DevShape* shape, fgemm_plan_info* info) {
   if (!info) return FGEMM_ERR_INVALID_VALUE;
   *info = fgemm_plan_info{};
   info->path = FGEMM_PATH_NONE;
@@ -661,8 +674,14 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
   bool nothing = false;
   st = validate(c, &nothing);
   if (st != FGEMM_OK || nothing) return st;
-  DeviceInfo* d = current_device();
-  if (!d) return FGEMM_ERR_NO_DEVICE;
+  DevShape dev{};
+  if (shape) {
+    dev = *shape;
+  } else {
+    DeviceInfo* d = current_device();
+    if (!d) return FGEMM_ERR_NO_DEVICE;
+    dev = shape_of(d);
+  }
   int path = 0;
   st = choose_path(c, &path);
   if (st != FGEMM_OK) return st;
@@ -670,7 +689,7 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
   info->cluster = 1;
   info->tail_split = 1;
   if (path == FGEMM_PATH_TC) {
-    const TcPlan t = plan_tc(c, d);
+    const TcPlan t = plan_tc(c, dev);
     if (t.num_tiles < 0) return FGEMM_ERR_INVALID_VALUE;
     info->cluster = t.pair ? 2 : 1;
     info->grid = t.units * info->cluster;
@@ -681,8 +700,9 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
     info->y_blocks = t.y_blocks == 0 ? 3 : t.y_blocks;
     info->k_rows = t.k_rows;
     info->resident_pairs = t.resident;
+    info->row_barriers = t.row_bars ? 1 : 0;
   } else if (path == FGEMM_PATH_SKINNY) {
-    const SkPlan s = plan_skinny(c, d);
+    const SkPlan s = plan_skinny(c, dev);
     info->cluster = s.split;
     info->grid = s.groups * s.split;
     info->tiles = s.tiles_n;
@@ -690,6 +710,30 @@ int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, co
     info->tail_split = s.nt;  // reused: 128-column tiles per CTA on the skinny path
   }
   return FGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
+               int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
+               fgemm_plan_info* info) {
+  return plan_info(A, B, bias, Y, out, M, N, K, dtype, epilogue, opts, nullptr, info);
+}
+
+int fgemm_plan_on(const void* A, const void* B, const void* bias, const void* Y, const void* out,
+                  int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
+                  int num_sms, int resident_pairs, fgemm_plan_info* info) {
+  if (num_sms < 1 || resident_pairs < 0) {
+    if (info) {
+      *info = fgemm_plan_info{};
+      info->path = FGEMM_PATH_NONE;
+    }
+    return FGEMM_ERR_INVALID_VALUE;
+  }
+  const DevShape shape{num_sms, resident_pairs};
+  return plan_info(A, B, bias, Y, out, M, N, K, dtype, epilogue, opts, &shape, info);
 }
 
 int fgemm_tile_of(int64_t t, int64_t tiles_m, int64_t tiles_n, int group, int64_t* m_tile,

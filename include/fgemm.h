@@ -251,11 +251,21 @@ typedef struct {
                          multiple of 256); 0 on other paths */
   int y_blocks;       /* tensor-core path: staging of the second operand (see fgemm_opts) */
   int k_rows;         /* tensor-core path: 128-byte K rows per ring stage (see fgemm_opts) */
-  int reserved;
+  int row_barriers;   /* tensor-core path, two K rows per stage: 1 = each K row of a stage lands on
+                         its own full barrier (fp8 operands and staged second operands) */
 } fgemm_plan_info;
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
                int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
                fgemm_plan_info* info);
+/*
+ * The same plan for a device described by its SM count and the number of CTA pairs of the
+ * tensor-core kernel that can be resident on it at once, computed on the host alone (no GPU is
+ * needed or touched; the buffers are inspected for alignment only).  num_sms >= 1 and
+ * resident_pairs >= 0 (0: no limit below num_sms / 2), else FGEMM_ERR_INVALID_VALUE.
+ */
+int fgemm_plan_on(const void* A, const void* B, const void* bias, const void* Y, const void* out,
+                  int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
+                  int num_sms, int resident_pairs, fgemm_plan_info* info);
 
 /*
  * The persistent kernels' tile order, exposed for host-side tests: linear tile t of a
