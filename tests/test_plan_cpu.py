@@ -132,3 +132,34 @@ def test_bad_device_shape_is_rejected():
     for sms, pairs in ((0, 76), (152, -1)):
         with pytest.raises(fg.FgemmError):
             plan(4096, 4096, 4096, fg.BF16, sms=sms, pairs=pairs)
+
+
+@pytest.mark.parametrize("M,N,K,tiles,split", [
+    (16, 2056, 4096, 17, 8),   # 17 column tiles; 2 x 152 / 17 = 17, at most 8
+    (100, 520, 1024, 5, 4),    # 5 tiles; 2 x 152 / 5 = 60, at most K blocks / 4 = 16 / 4 = 4
+    (16, 1032, 256, 9, 1),     # 4 K blocks: 4 / 4 = 1, no split
+    (64, 136, 8, 2, 1),        # one K block: no split
+])
+def test_skinny_split_caps(M, N, K, tiles, split):
+    p = plan(M, N, K, fg.BF16)
+    assert (p["path"], p["tiles"], p["cluster"], p["grid"]) == (fg.PATH_SKINNY, tiles, split,
+                                                                tiles * split)
+
+
+def test_skinny_two_tiles_per_cta():
+    # two 128-column tiles per CTA: 64 / 2 = 32 groups; 2 x 152 / 32 = 9, at most 8; 32 x 8 CTAs
+    p = plan(16, 8192, 8192, fg.BF16, opts={"skinny_tiles": 2})
+    assert (p["tail_split"], p["cluster"], p["grid"]) == (2, 8, 256)
+
+
+def test_residual_and_quantised_epilogues():
+    # the residual's R is staged like the gate's Y when the output is 16-bit ...
+    p = plan(1024, 21568, 4096, fg.F16, epilogue=fg.EPI_RESIDUAL_RELU)
+    assert (p["y_blocks"], p["k_rows"], p["row_barriers"]) == (3, 2, 1)
+    # ... and read into registers (no staging, no per-row barriers) with an fp32 output
+    p = plan(1024, 21568, 4096, fg.F16 | fg.OUT_F32, epilogue=fg.EPI_RESIDUAL_RELU)
+    assert (p["y_blocks"], p["k_rows"], p["row_barriers"]) == (1, 2, 0)
+    # fp8 output on pairs: 128-column staging rows keep pieces at 128 columns per pair, so the
+    # 4096^3 tail is still cut in two (284 items); 16-bit operands: one full barrier per stage
+    p = plan(4096, 4096, 4096, fg.BF16 | fg.BIAS_F32 | fg.OUT_E4M3, epilogue=fg.EPI_RELU_QUANT)
+    assert (p["path"], p["tail_split"], p["work_items"], p["row_barriers"]) == (fg.PATH_TC, 2, 284, 0)
