@@ -138,7 +138,10 @@ def _opts(opts) -> Opts | None:
     if opts is None or isinstance(opts, Opts):
         return opts
     o = Opts()
+    fields = {name for name, _ in Opts._fields_}
     for k, v in dict(opts).items():
+        if k not in fields:  # a misspelt key would otherwise be dropped without a word
+            raise ValueError(f"unknown fgemm_opts field {k!r}")
         setattr(o, k, int(v))
     return o
 

@@ -163,3 +163,8 @@ def test_residual_and_quantised_epilogues():
     # 4096^3 tail is still cut in two (284 items); 16-bit operands: one full barrier per stage
     p = plan(4096, 4096, 4096, fg.BF16 | fg.BIAS_F32 | fg.OUT_E4M3, epilogue=fg.EPI_RELU_QUANT)
     assert (p["path"], p["tail_split"], p["work_items"], p["row_barriers"]) == (fg.PATH_TC, 2, 284, 0)
+
+
+def test_unknown_option_names_are_refused():
+    with pytest.raises(ValueError):
+        plan(4096, 4096, 4096, fg.BF16, opts={"group": 8})  # the field is group_m
