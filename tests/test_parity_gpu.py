@@ -184,6 +184,35 @@ def test_skinny_single_cta_long_k_bit_exact(M, N, K, tiles):
         pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
 
 
+@pytest.mark.parametrize("M,N,K,opts,want_path", [
+    (300, 520, 200, None, 1),            # tensor cores, single CTAs, ragged last column
+    (700, 1800, 1104, None, 1),          # CTA pairs, last column narrowed to 128 of 256
+    (16, 1032, 512, None, 2),            # skinny, ragged last 128-column tile
+    (7, 9, 13, None, 3),                 # generic
+])
+@pytest.mark.parametrize("gate", [False, True])
+def test_bias_padded_with_nan_past_n(M, N, K, opts, want_path, gate):
+    # "Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "Pitfalls": the bias load must be
+    # masked with j < N.  The bias buffer runs on past N with NaNs; a read past the end that leaked
+    # into a stored column would show up as a NaN in out.
+    p = gen.integer_problem(M, N, K, BF16, BF16, seed=M + N + K, gate=gate)
+    A, B = up(p.A, BF16), up(p.B, BF16)
+    padded = torch.full((N + 512,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    padded[:N] = up(p.bias, BF16)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    w = dtype_word(BF16, BF16, BF16)
+    if gate:
+        path = fg.fgemm_addmm_gate_ex(A, B, padded, up(p.Y, BF16), out, M, N, K, w, opts=opts)
+    else:
+        path = fg.fgemm_bias_relu_ex(A, B, padded, out, M, N, K, w, opts=opts)
+    torch.cuda.synchronize()
+    assert path == want_path
+    assert not torch.isnan(out).any()
+    # by value: with the bias-initialised accumulator an exact zero may come out as -0
+    assert _same_values(down(out, BF16), oracle_run(p, M, N, K, BF16, BF16, BF16, gate=gate).out,
+                        BF16)
+
+
 def test_skinny_auto_split_and_coverage():
     M, N, K = 16, 2056, 4096
     p = gen.random_problem(M, N, K, BF16, BF16, seed=12)
