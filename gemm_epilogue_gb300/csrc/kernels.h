@@ -42,6 +42,11 @@ struct TcParams {
   uint64_t timeout_ns;
   int* err;        // device error word
   int inject_stall;  // diagnostic: CTA 0 skips the loads of its first stage (see fgemm_opts)
+  // Stream-K share-out of the last round (stream_k.h): the last sk_tiles tiles of the grouped
+  // order (full_tiles = num_tiles - sk_tiles, tail_split = 1); 0 = none.
+  int sk_tiles;
+  float* sk_part;     // per unit and CTA rank: 128 rows x 256 columns of fp32 partial sums
+  unsigned* sk_flag;  // per unit, CTA rank and epilogue warp: 1 = that warp's partial sums written
 };
 
 // Generic CUDA-core kernel and elementwise kernels: plain pointers.
