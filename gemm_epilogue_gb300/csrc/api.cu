@@ -173,7 +173,7 @@ int validate(const Call& c, bool* nothing) {
     if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
         o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
-        o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 2 ||
+        o.inject_stall < 0 || o.inject_stall > 2 || o.bias_init < 0 || o.bias_init > 2 ||
         o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 3 ||
         o.k_rows < 0 || o.k_rows > 2 || o.stream_k < 0 || o.stream_k > 2 ||
         (o.stream_k == 1 && o.bias_init == 1))
@@ -437,7 +437,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
+  p.inject_stall = c.opts ? c.opts->inject_stall : 0;
   return status_of(
       launch_tc(c.epi, tmA, tmB, tmO, tmY, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
 }
@@ -469,7 +469,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
+  p.inject_stall = (c.opts && c.opts->inject_stall == 1) ? 1 : 0;
   if (!skinny_fits(s.mpad, s.nt, s.split, s.stages)) return FGEMM_ERR_INVALID_VALUE;
   return status_of(launch_skinny(c.epi, tmB, tmA, p, s.groups * s.split, c.stream));
 }

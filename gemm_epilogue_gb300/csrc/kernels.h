@@ -41,7 +41,8 @@ struct TcParams {
   uint32_t b_lbo, b_sbo;  // B (MN-major) descriptor byte offsets
   uint64_t timeout_ns;
   int* err;        // device error word
-  int inject_stall;  // diagnostic: CTA 0 skips the loads of its first stage (see fgemm_opts)
+  int inject_stall;  // diagnostic (see fgemm_opts): 1 = CTA 0 skips the loads of its first stage,
+                     // 2 = stream-K runs that end a tile never raise their flags
   // Stream-K share-out of the last round (stream_k.h): the last sk_tiles tiles of the grouped
   // order (full_tiles = num_tiles - sk_tiles, tail_split = 1); 0 = none.
   int sk_tiles;

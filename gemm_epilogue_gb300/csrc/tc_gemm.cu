@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a_dst = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_dst = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
           // diagnostic stall: announce the stage's bytes but never load them
-          const bool stall = p.inject_stall && blockIdx.x == 0 && i == 0 && kb == wk.kb0;
+          const bool stall = p.inject_stall == 1 && blockIdx.x == 0 && i == 0 && kb == wk.kb0;
           // the even CTA's full barriers count both CTAs' bytes
           if (leader)
             for (int f = 0; f < nfb; ++f) mbar_arrive_expect_tx(bar(BAR_FULL + stage * KSUB + f), tx);
@@ -695,7 +695,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __threadfence();
         __syncwarp();  // every lane's stores come before lane 0's release
-        if (lane == 0) flag_raise(sk_flag_of(wk.part));
+        if (lane == 0 && p.inject_stall != 2) flag_raise(sk_flag_of(wk.part));  // 2: diagnostic
         release_acc(it + 2, b);
         continue;
       }

@@ -115,7 +115,10 @@ typedef struct {
                        announces its first stage but issues none of its loads, so the MMA's wait
                        on that stage can never complete; it expires after timeout_ms, the kernel
                        drains and exits, and fgemm_device_status reports FGEMM_ERR_TIMEOUT.
-                       The output of that call is undefined.  Tensor-core and skinny paths. */
+                       The output of that call is undefined.  Tensor-core and skinny paths.
+                       2 = (tensor-core path with stream-K) the runs that end a tile never
+                       raise their flags, so every head's wait for them expires the same way;
+                       the workspace's flags stay zero. */
   int bias_init;  /* tensor-core path: start each tile's accumulator at the bias (written into
                      tensor memory before the K loop) instead of adding it after the reduction;
                      same result up to the rounding order ("Optimizing GEMM + Activation on CDNA4
