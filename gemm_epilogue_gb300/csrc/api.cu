@@ -299,14 +299,13 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
   // Stream-K share-out of the last round (stream_k.h) instead of the column pieces: every unit
   // takes an equal run of the round's K blocks.  It needs a K loop long enough that a run's
   // partial-sum exchange is small next to it (>= 16 K blocks per tile), a run of at least one
-  // K block per unit, no staged second operand (the staged epilogue has no partial-sum step),
-  // the flags of every CTA in the workspace's flag area, and the caller's workspace.
+  // K block per unit, the flags of every CTA in the workspace's flag area, and the caller's
+  // workspace.
   {
     const int64_t kb_k = static_cast<int64_t>(128 / elem_bytes(c.t.ab)) * t.k_rows;  // K per stage
     const int64_t num_kb = (c.K + kb_k - 1) / kb_k;
     const int ctas = t.units * (t.pair ? 2 : 1);
-    // (the kernel stages the second operand for 16-bit outputs on single CTAs too)
-    const bool qualifies = rem > 0 && t.num_tiles > units && !staged_y && num_kb >= 16 &&
+    const bool qualifies = rem > 0 && t.num_tiles > units && num_kb >= 16 &&
                            num_kb <= 0x7fffffff && static_cast<int64_t>(rem) * num_kb >= units &&
                            static_cast<size_t>(ctas) * 8 * sizeof(unsigned) <= FGEMM_SK_FLAG_BYTES;
     t.sk_bytes = qualifies ? FGEMM_SK_FLAG_BYTES + static_cast<size_t>(ctas) * tc_block_m() *

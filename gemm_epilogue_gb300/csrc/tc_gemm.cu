@@ -466,6 +466,40 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto sk_add = [&](const Work& w, int col, auto& acc) {
       for (int s = 0; s < w.nsrc; ++s) sk_add_cols(sk_slot(w.src0 + s) + (32 * q + lane), col, acc);
     };
+    // Stream-K run that does not start its tile: the warp's 32 rows x (up to) 128 columns of fp32
+    // sums go to its slot (four columns of a row per 16-byte store; one warp store covers 32
+    // consecutive rows, 512 contiguous bytes), then the warp raises its flag.
+    auto sk_write = [&](const Work& w, uint32_t taddr) {
+      float4* dst = sk_slot(w.part) + (32 * q + lane);
+#pragma unroll 1
+      for (int c = cbeg; c < cbeg + BN / 2 && c < w.width; c += 32) {
+        uint32_t v[32];
+        __syncwarp();  // tcgen05.ld is warp-collective
+        tmem_ld32(taddr, v, c);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          __stcg(dst + ((c >> 2) + e) * BM,
+                 make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                             __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+      }
+      __threadfence();
+      __syncwarp();  // every lane's stores come before lane 0's release
+      if (lane == 0 && p.inject_stall != 2) flag_raise(sk_flag_of(w.part));  // 2: diagnostic
+    };
+    // Stream-K head: wait until the units that ran the tile's later K blocks have written this
+    // warp's rows and columns of their sums (false: the wait expired or the CTA aborts).
+    auto sk_wait = [&](const Work& w) {
+      bool ready = true;
+      for (int s = 0; s < w.nsrc && ready; ++s)
+        ready = flag_wait_warp(sk_flag_of(w.src0 + s), abort_flag, tmo, p.err, SITE_SK_FLAG);
+      return ready;
+    };
+    // The sums read, the head puts the flags back to zero for the next call (one reader each).
+    auto sk_clear = [&](const Work& w) {
+      if (lane == 0)
+        for (int s = 0; s < w.nsrc; ++s) flag_clear(sk_flag_of(w.src0 + s));
+    };
     // Bias-initialised accumulator ("Optimizing GEMM + Activation on CDNA4 with TLX", V4: the
     // accumulator starts at the bias instead of zero): this warp writes bias[col] into every lane
     // (row) of its quarter and every column of its half of buffer bb for work item t, then hands
@@ -519,6 +553,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto issue_y = [&](int i, int yb) -> bool {  // warp-uniform result
         Work w;
         if (!work_at(p, num_kb, unit, units, i, w)) return false;
+        if (w.part >= 0) return false;  // a stream-K run that only writes partial sums: no Y
         const int r0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + 32 * q;
         if (r0 >= p.M) return false;
         int nchunks = 0;
@@ -546,7 +581,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int row0 = m0 + 32 * q;
         const bool rows_live = row0 < p.M;  // warp-uniform
         float bq[4];
-        if (add_bias) load_bias_quad(p, n0 + cbeg, bq);
+        if (add_bias && wk.part < 0) load_bias_quad(p, n0 + cbeg, bq);
 
         if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
           break;
@@ -559,6 +594,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
+        if (wk.part >= 0) {  // stream-K run that does not start its tile: no Y, no store
+          sk_write(wk, taddr);
+          release_acc(it + 2, b);
+          if (issue_y(it + NYB, yb)) y_issued |= 1u << yb;
+          continue;
+        }
+        if (wk.nsrc > 0 && !sk_wait(wk)) break;  // stream-K head
         bool aborted = false;
 #pragma unroll 1
         for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
@@ -589,6 +631,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld32(taddr, a1, c * CH + 32);
             tmem_ld_wait();
           }
+          sk_add(wk, c * CH, acc);
           const uint32_t sb = YHALF ? ebuf
                                     : ebuf + static_cast<uint32_t>(yb) * C::Y_BLOCK_BYTES +
                                           static_cast<uint32_t>(c - cbeg / CH) * EPI_BUF_BYTES;
@@ -647,6 +690,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (aborted) break;
         if (lane == 0) bulk_commit();
+        sk_clear(wk);
         // This warp has finished reading accumulator b: release it to the MMA warp.
         release_acc(it + 2, b);
         // Prefetch into this block the Y of the work item NYB items ahead (main loops run
@@ -676,37 +720,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
 
-      if (wk.part >= 0) {
-        // Stream-K run that does not start its tile: the warp's 32 rows x (up to) 128 columns of
-        // fp32 sums go to its slot (four columns of a row per 16-byte store; one warp store
-        // covers 32 consecutive rows, 512 contiguous bytes), then the warp raises its flag.
-        float4* dst = sk_slot(wk.part) + (32 * q + lane);
-#pragma unroll 1
-        for (int c = cbeg; c < cbeg + BN / 2 && c < wk.width; c += 32) {
-          uint32_t v[32];
-          __syncwarp();  // tcgen05.ld is warp-collective
-          tmem_ld32(taddr, v, c);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            __stcg(dst + ((c >> 2) + e) * BM,
-                   make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                               __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
-        }
-        __threadfence();
-        __syncwarp();  // every lane's stores come before lane 0's release
-        if (lane == 0 && p.inject_stall != 2) flag_raise(sk_flag_of(wk.part));  // 2: diagnostic
+      if (wk.part >= 0) {  // stream-K run that does not start its tile
+        sk_write(wk, taddr);
         release_acc(it + 2, b);
         continue;
       }
-      if (wk.nsrc > 0) {
-        // Stream-K head: wait until the units that ran the tile's later K blocks have written
-        // this warp's rows and columns of their sums.
-        bool ready = true;
-        for (int s = 0; s < wk.nsrc && ready; ++s)
-          ready = flag_wait_warp(sk_flag_of(wk.src0 + s), abort_flag, tmo, p.err, SITE_SK_FLAG);
-        if (!ready) break;
-      }
+      if (wk.nsrc > 0 && !sk_wait(wk)) break;  // stream-K head
 
 #pragma unroll 1
       for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
@@ -869,9 +888,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         }  // OUT_BYTES != 1
       }
-      // The sums read, the flags go back to zero for the next call (each has this one reader).
-      if (wk.nsrc > 0 && lane == 0)
-        for (int s = 0; s < wk.nsrc; ++s) flag_clear(sk_flag_of(wk.src0 + s));
+      sk_clear(wk);
       // This warp has finished reading accumulator b: release it to the MMA warp.
       release_acc(it + 2, b);
     }
@@ -895,9 +912,6 @@ template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KS
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                        const CUtensorMap& y, const TcParams& p, int grid, cudaStream_t s) {
   auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB, KSUB>;
-  // the staged-Y epilogue has no stream-K step (the planner never asks for it there)
-  if ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2 && p.sk_tiles > 0)
-    return cudaErrorNotSupported;
   constexpr uint32_t smem =
       Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB, KSUB>::SMEM_BYTES;
   static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once

@@ -148,8 +148,7 @@ typedef struct {
                      adds them, in K order, to its own sum and runs the epilogue once on the
                      total.  The sum is deterministic for a given plan, but its rounding order
                      depends on the grid (max_ctas, the device) and on group_m, unlike the
-                     other tail cuts.  Qualifies: no staged second operand (the gate and the
-                     residual qualify with fp32 outputs only), at least 16 K blocks per tile, at least one
+                     other tail cuts.  Qualifies: at least 16 K blocks per tile, at least one
                      K block per CTA (pair); the bias is then added after the sum
                      (bias_init = 1 is refused). */
   /* Stream-K workspace (device memory, 256-byte aligned, caller-owned; fgemm_plan reports the

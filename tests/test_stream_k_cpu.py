@@ -171,11 +171,8 @@ def test_stream_k_switches():
 
 def test_shapes_that_do_not_qualify():
     ws = {"workspace": WS, "workspace_bytes": 1 << 30}
-    # the gate with a 16-bit output on pairs stages Y: no stream-K
-    p = plan(1024, 21568, 4096, fg.F16, gate=True, opts=ws)
-    assert (p["sk_tiles"], p["sk_workspace_bytes"]) == (0, 0)
     with pytest.raises(fg.FgemmError):
-        plan(1024, 21568, 4096, fg.F16, gate=True, opts=dict(ws, stream_k=1))
+        plan(4096, 4096, 1024, fg.BF16, opts=dict(ws, stream_k=1))
     # K = 1024 on pairs: 8 K blocks per tile, below 16
     assert plan(4096, 4096, 1024, fg.BF16, opts=ws)["sk_tiles"] == 0
     # a grid that divides the tiles has no partial round: 256 tiles on 64 pairs
@@ -190,6 +187,8 @@ def test_other_shapes_that_qualify():
     # FFN 8192 x 14336 x 4096: 32 x 56 = 1792 tiles = 23 x 76 + 44
     p = plan(8192, 14336, 4096, fg.BF16, opts=ws)
     assert (p["sk_tiles"], p["work_items"]) == (44, sk_items(1748, 76, 44, 32))
-    # the gate with an fp32 output reads Y into registers: it qualifies
-    p = plan(1024, 21568, 4096, fg.F16 | fg.OUT_F32, gate=True, opts=ws)
-    assert p["sk_tiles"] == 340 % 76
+    # the GLU block's gate: 4 x 85 = 340 tiles = 4 x 76 + 36, K = 4096 in 32 K blocks (two K rows
+    # per stage with Y staged one chunk at a time); with an fp32 output Y goes to registers
+    for w in (fg.F16, fg.F16 | fg.OUT_F32):
+        p = plan(1024, 21568, 4096, w, gate=True, opts=ws)
+        assert (p["sk_tiles"], p["work_items"]) == (36, sk_items(304, 76, 36, 32))

@@ -86,6 +86,33 @@ def test_stream_k_integer_bit_exact(ws, pair, max_ctas):
         assert flags_clear(ws)
 
 
+# The gate and the residual with 16-bit outputs stage Y (or R) through shared memory: on pairs one
+# 4 KB chunk at a time (K = 2048) or a whole block a work item ahead (K = 1024, one K row per
+# stage, 16 K blocks), on single CTAs a block ahead (K = 1096).
+STAGED = [(2, 10, 2048), (2, 14, 1024), (1, 10, 1096)]
+
+
+@pytest.mark.parametrize("pair,max_ctas,K", STAGED)
+def test_stream_k_staged_second_operand_bit_exact(ws, pair, max_ctas, K):
+    M, N = 700, 1800
+    opts = sk(ws, cta_pair=pair, max_ctas=max_ctas)
+    for ab in (F16, BF16):
+        p = gen.integer_problem(M, N, K, ab, ab, seed=K + max_ctas, gate=True)
+        out, plan = run(p, M, N, K, ab, ab, ab, opts, gate=True)
+        assert plan["sk_tiles"] > 0
+        ref = oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, ab, ab, ab)
+        assert np.array_equal(down(out, ab), ref.out)
+        # the residual add stages R the same way
+        out = torch.empty(M, N, dtype=TORCH_OF[ab], device="cuda")
+        path = fg.fgemm_bias_residual_relu_ex(up(p.A, ab), up(p.B, ab), up(p.bias, ab), up(p.Y, ab),
+                                              out, M, N, K, dtype_word(ab, ab, ab), opts=opts)
+        torch.cuda.synchronize()
+        assert path == fg.PATH_TC
+        ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, ab, ab, ab)
+        assert np.array_equal(down(out, ab), ref.out)
+        assert flags_clear(ws)
+
+
 def test_stream_k_quantized_output_bit_exact(ws):
     M, N, K = 700, 1808, 2048
     p = gen.integer_problem(M, N, K, BF16, F32, seed=3)
@@ -141,15 +168,22 @@ def test_stream_k_random_tolerance_deterministic_and_covering(ws, pair, max_ctas
     assert flags_clear(ws)
 
 
-def test_square_4096_stream_k_sampled_rows(ws):
-    w = gen.WORKLOADS["square_4096"]
+@pytest.mark.parametrize("name", ["square_4096", "glu_gate_1024x21568x4096"])
+def test_full_size_stream_k_sampled_rows(ws, name):
+    w = gen.WORKLOADS[name]
     x = gen.make(w)
     opts = {"workspace": ws.data_ptr(), "workspace_bytes": ws.numel()}  # automatic mode
-    out, plan = run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, opts)
+    gate = w.epilogue == "gate"
+    out, plan = run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, opts, gate=gate)
     assert plan["sk_tiles"] > 0
     rows = sample_rows(w.M)
-    ref = oracle.bias_relu(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type,
-                           rows=rows)
+    if gate:
+        ref = oracle.addmm_gate(x.A, x.B, x.bias, x.Y, w.M, w.N, w.K, w.ab_type, w.bias_type,
+                                w.out_type, rows=rows)
+    else:
+        ref = oracle.bias_relu(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type,
+                               w.out_type, rows=rows)
     check_close(down(out, w.out_type)[rows], ref, w.K, w.out_type,
-                bias64=oracle.decode(x.bias, w.bias_type), what="square_4096 stream-K")
+                Y64=oracle.decode(x.Y[rows], w.ab_type) if gate else None,
+                bias64=oracle.decode(x.bias, w.bias_type), what=name + " stream-K")
     assert flags_clear(ws)
