@@ -269,7 +269,10 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
       const uint32_t dst = remote ? map_shared_rank(slot, owner) : slot;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(t * p.mpad);
-      for (int c = half; c < p.mpad / 16; c += halves) {
+      // the owners read m < 4 ceil(M / 4) only: with M = 1 the MMA's 16 columns hold 15 padding
+      // rows, and pushing them would be three quarters of the exchange
+      const int mlim = 4 * ((p.M + 3) / 4);
+      for (int c = half; c < p.mpad / 16 && 16 * c < mlim; c += halves) {
         uint32_t v[16];
         if (have) {
           __syncwarp();
@@ -281,6 +284,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {  // m = 16 c + j; the warp's lanes write consecutive rows
+          if (16 * c + j >= mlim) break;
           const uint32_t a = dst + 4u * static_cast<uint32_t>((16 * c + j) * pitch);
           if (remote)
             st_shared_cluster_f32(a, __uint_as_float(v[j]));
