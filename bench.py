@@ -170,7 +170,7 @@ def slowest_rank(dist, value, device=None):
 class Problem:
     """Device-resident rotating input sets of one workload, and a call of the fused kernel."""
 
-    def __init__(self, w, dev, l2_bytes, max_sets=8, with_unfused=False, stream_k=True):
+    def __init__(self, w, dev, l2_bytes, max_sets=8, with_unfused=False, stream_k=True, pdl=False):
         import torch
         from gemm_epilogue_gb300 import inputs as gen
         import gemm_epilogue_gb300.binding as fg
@@ -221,12 +221,15 @@ class Problem:
         # caller's: with it the library deals the last round out stream-K where the shape
         # qualifies, and reports the workspace it needs either way.
         self.sk_ws = None
+        self.pdl = pdl
         if stream_k:
             need = self.plan()["sk_workspace_bytes"]
             if need:
                 self.sk_ws = torch.zeros(need, dtype=torch.uint8, device=dev)
 
     def with_ws(self, opts):
+        if self.pdl and not (opts and "pdl" in opts):
+            opts = dict(opts or {}, pdl=1)
         if self.sk_ws is None or (opts and "workspace" in opts):
             return opts
         return dict(opts or {}, workspace=self.sk_ws.data_ptr(), workspace_bytes=self.sk_ws.numel())
@@ -453,7 +456,7 @@ def run_ours(args):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_DEFAULT
     prob = Problem(w, dev, l2, with_unfused=args.variant == "unfused",
-                   stream_k=not args.no_stream_k)
+                   stream_k=not args.no_stream_k, pdl=args.pdl)
     stream = torch.cuda.Stream(device=dev)
     barrier = (lambda: dist.barrier()) if dist else None
     sampler = ClockSampler(local) if rank == 0 else None
@@ -507,7 +510,7 @@ def run_ours(args):
                    "epilogue": w.epilogue,
                    "out": gen.TYPE_NAMES[w.out_type], "bias": gen.TYPE_NAMES[w.bias_type],
                    "path": fg.PATH_NAMES.get(path, str(path)), "plan": prob.plan(opts),
-                   "opts": opts,
+                   "opts": opts, "pdl": bool(args.pdl),
                    "parallelism": f"replicas{world}", "launch": launch,
                    "stream_loop_ms_per_step": ms_loop,
                    "l2": f"inputs rotate over {len(prob.sets)} sets of {prob.set_bytes / 1e6:.1f} MB "
@@ -582,7 +585,7 @@ def run_sweep(args):
     for name in names:
         w = gen.WORKLOADS[name]
         unf = w.name in ("square_4096", "glu_gate_1024x21568x4096")
-        prob = Problem(w, dev, l2, with_unfused=unf, stream_k=not args.no_stream_k)
+        prob = Problem(w, dev, l2, with_unfused=unf, stream_k=not args.no_stream_k, pdl=args.pdl)
         steps = max(5, min(200, int(2e-1 / max(w.flops / 1.2e15, 1e-6))))
         if w.name.startswith("ffn"):
             variants = [{"group_m": g} for g in (1, 4, 8, 16)]
@@ -642,6 +645,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
                     help="unfused: time the GEMM -> elementwise chain instead (traffic comparison)")
+    ap.add_argument("--pdl", action="store_true",
+                    help="launch with programmatic dependent launch (fgemm_opts.pdl): a call's "
+                         "set-up overlaps the previous call's tail")
     ap.add_argument("--no-stream-k", action="store_true",
                     help="give the library no stream-K workspace (the last round is cut into "
                          "column pieces instead)")

@@ -175,7 +175,7 @@ int validate(const Call& c, bool* nothing) {
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
         o.inject_stall < 0 || o.inject_stall > 2 || o.bias_init < 0 || o.bias_init > 2 ||
         o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 3 ||
-        o.k_rows < 0 || o.k_rows > 2 || o.stream_k < 0 || o.stream_k > 2 ||
+        o.k_rows < 0 || o.k_rows > 2 || o.stream_k < 0 || o.stream_k > 2 || o.pdl < 0 || o.pdl > 1 ||
         (o.stream_k == 1 && o.bias_init == 1))
       return FGEMM_ERR_INVALID_VALUE;
     if (o.workspace && !aligned(o.workspace, 256)) return FGEMM_ERR_MISALIGNED;
@@ -437,6 +437,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
   p.inject_stall = c.opts ? c.opts->inject_stall : 0;
+  p.pdl = (c.opts && c.opts->pdl) ? 1 : 0;
   return status_of(
       launch_tc(c.epi, tmA, tmB, tmO, tmY, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
 }
@@ -469,6 +470,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
   p.inject_stall = (c.opts && c.opts->inject_stall == 1) ? 1 : 0;
+  p.pdl = (c.opts && c.opts->pdl) ? 1 : 0;
   if (!skinny_fits(s.mpad, s.nt, s.split, s.stages)) return FGEMM_ERR_INVALID_VALUE;
   return status_of(launch_skinny(c.epi, tmB, tmA, p, s.groups * s.split, c.stream));
 }

@@ -294,6 +294,17 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grids this one depends on have completed and their memory operations are
+// visible (returns at once for a launch without programmatic serialization), and let the grids
+// that depend on this one be scheduled before it ends.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- flags in global memory
 // A flag word that one warp raises after writing data to global memory and another warp (of
 // another CTA) waits for before reading it: release / acquire at GPU scope.

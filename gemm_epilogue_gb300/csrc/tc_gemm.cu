@@ -306,6 +306,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (PAIR) cluster_sync();  // the peer signals the even CTA's barriers: both must be initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Above, only this CTA's shared and tensor memory were touched: with programmatic dependent
+  // launch that part overlaps the previous kernel's tail.  Global memory only from here on.
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   const int num_kb = (p.K + KB_ELEMS - 1) / KB_ELEMS;
   const uint64_t tmo = p.timeout_ns;
@@ -927,13 +931,15 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k, a, b, o, y, p);
 }
 

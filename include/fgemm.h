@@ -151,6 +151,11 @@ typedef struct {
                      other tail cuts.  Qualifies: at least 16 K blocks per tile, at least one
                      K block per CTA (pair); the bias is then added after the sum
                      (bias_init = 1 is refused). */
+  int pdl;        /* tensor-core and skinny paths: 1 = launch with programmatic stream
+                     serialization, so that the kernel's set-up (barriers, tensor memory) runs
+                     while the previous kernel in the stream finishes; the kernel waits for that
+                     kernel's completion (griddepcontrol.wait) before its first access to global
+                     memory, so any dependency between the two stays safe.  0 = off. */
   /* Stream-K workspace (device memory, 256-byte aligned, caller-owned; fgemm_plan reports the
      bytes needed as sk_workspace_bytes).  Its first FGEMM_SK_FLAG_BYTES bytes hold flag words
      that must be zero before the first call; every call that completes leaves them zero again.  After a call that
