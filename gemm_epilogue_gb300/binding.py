@@ -44,7 +44,7 @@ class Opts(ctypes.Structure):
     """fgemm_opts: zero fields mean defaults."""
     _fields_ = [("group_m", ctypes.c_int), ("path", ctypes.c_int), ("split_k", ctypes.c_int),
                 ("max_ctas", ctypes.c_int), ("timeout_ms", ctypes.c_int),
-                ("b_desc_swap", ctypes.c_int), ("cta_pair", ctypes.c_int), ("tail_split", ctypes.c_int),
+                ("cta_pair", ctypes.c_int), ("tail_split", ctypes.c_int),
                 ("skinny_tiles", ctypes.c_int), ("stages", ctypes.c_int),
                 ("inject_stall", ctypes.c_int), ("bias_init", ctypes.c_int),
                 ("full_last_n", ctypes.c_int), ("y_blocks", ctypes.c_int),

@@ -428,11 +428,6 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.Y = c.Y;
   p.out_scale = c.out_scale;
   p.idesc = idesc_f16_f32acc(p.ab_bf16 != 0, TILE_M, BN, /*a_mn=*/false, /*b_mn=*/true);
-  const bool swap = c.opts && c.opts->b_desc_swap;
-  const uint32_t box_bytes = kb_elems * static_cast<uint32_t>(t.k_rows) * kb_elems *
-                             static_cast<uint32_t>(elem_bytes(c.t.ab));
-  p.b_lbo = swap ? 1024u : box_bytes;  // distance between the 128-byte-wide column boxes of B
-  p.b_sbo = swap ? box_bytes : 1024u;  // distance between 8-row groups along K
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;

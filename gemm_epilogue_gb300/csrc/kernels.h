@@ -38,7 +38,6 @@ struct TcParams {
   const void* Y;   // gate only, M x N operand type
   float out_scale; // quantized epilogue only
   uint32_t idesc;  // tcgen05 instruction descriptor
-  uint32_t b_lbo, b_sbo;  // B (MN-major) descriptor byte offsets
   uint64_t timeout_ns;
   int* err;        // device error word
   int inject_stall;  // diagnostic (see fgemm_opts): 1 = CTA 0 skips the loads of its first stage,

@@ -8,9 +8,9 @@
 //
 // Host code cannot use the array's name as a device address (on the host it names a shadow
 // variable, not device memory), so on the first call on each device, with that device current,
-// the address is looked up once with cudaGetSymbolAddress and cached; later calls on that device
+// the address is looked up with cudaGetSymbolAddress and cached; later calls on that device
 // reuse it.  That first call may load the library's device code; make it before any stream
-// capture.
+// capture.  A failed lookup is not cached: the next call on that device tries again.
 //
 // All calls share the one array and it keeps whatever the previous call left in it.  Nothing in
 // it has to start at zero: the GEMM step writes every intermediate element before the bias and
@@ -30,13 +30,15 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[FGEMM_NOALLOC_S
 constexpr int kMaxDevices = 64;
 
 struct ScratchSlot {
-  std::once_flag once;
-  void* ptr = nullptr;
-  int status = FGEMM_ERR_NO_DEVICE;
+  std::mutex mu;
+  void* ptr = nullptr;  // set once the lookup has succeeded; never changes afterwards
 };
 ScratchSlot g_scratch[kMaxDevices];
 
-// Device address of the array on the current device, resolved once per device.
+// Device address of the array on the current device.  Only a successful lookup is kept: if it
+// fails (for example when a first call is made while a stream is being captured, where loading
+// the library's device code is not allowed), the call reports FGEMM_ERR_NO_DEVICE and the next
+// call on that device tries again.
 int scratch_on_current_device(void** ptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -44,18 +46,17 @@ int scratch_on_current_device(void** ptr) {
     return FGEMM_ERR_NO_DEVICE;
   }
   ScratchSlot& s = g_scratch[dev];
-  std::call_once(s.once, [&s] {
+  std::lock_guard<std::mutex> lock(s.mu);
+  if (s.ptr == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
       cudaGetLastError();
-      s.status = FGEMM_ERR_NO_DEVICE;
-      return;
+      return FGEMM_ERR_NO_DEVICE;
     }
     s.ptr = p;
-    s.status = FGEMM_OK;
-  });
+  }
   *ptr = s.ptr;
-  return s.status;
+  return FGEMM_OK;
 }
 
 }  // namespace

@@ -19,6 +19,8 @@
 //     earlier": ReLU of a partial sum is not ReLU of the sum, and a bias added per partial would be
 //     added S times): x = sum + bias[n], then ReLU or the gate, one rounding, coalesced store.
 // No workspace in global memory: the reduction stays on chip.
+#include <atomic>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -356,13 +358,15 @@ cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkPar
                        cudaStream_t s) {
   auto k = skinny_kernel<EPI>;
   const uint32_t smem = smem_bytes(p.mpad, p.nt, p.split, p.stages);
-  static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
+  // Per device: the shared-memory opt-in is set once.  Host threads may race on a first call;
+  // setting the attribute twice is harmless, and the flag is atomic.
+  static std::atomic<bool> opted_in[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!opted_in[dev]) {
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
-    opted_in[dev] = true;
+    opted_in[dev].store(true, std::memory_order_release);
   }
   if (smem > 232448) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg{};

@@ -44,6 +44,7 @@
 // once, after the full reduction.
 // The accumulator goes from TMEM to registers to the single store; it never touches HBM (a
 // stream-K partial sum crosses it once, in the workspace).
+#include <atomic>
 #include <type_traits>
 
 #include "kernels.h"
@@ -423,7 +424,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int k = r * KPR; k < (r + 1) * KPR; ++k) {  // 32 bytes of K per MMA
               const uint64_t ad =
                   sdesc_sw128(a_addr + (k / KPR) * A_ROW_BYTES + 32u * (k % KPR), 16u, 1024u);
-              const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, p.b_lbo, p.b_sbo);
+              // MN-major B: one column box (BBOX bytes) apart along N, 1 KB per 8 K rows
+              const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, BBOX, 1024u);
               // the first MMA of a tile (or of a stream-K run) starts the sum
               const uint32_t acc = (p.bias_init | (kb - wk.kb0) | k) != 0 ? 1u : 0u;
               if constexpr (F8)
@@ -918,13 +920,15 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB, KSUB>;
   constexpr uint32_t smem =
       Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB, KSUB>::SMEM_BYTES;
-  static bool opted_in[64] = {};  // per device: the shared-memory opt-in is set once
+  // Per device: the shared-memory opt-in is set once.  Host threads may race on a first call;
+  // setting the attribute twice is harmless, and the flag is atomic.
+  static std::atomic<bool> opted_in[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!opted_in[dev]) {
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    opted_in[dev] = true;
+    opted_in[dev].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -947,10 +951,13 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
 // number of pairs that fit at once can be below SMs / 2.
 template <int EPI, int OUT_BYTES>
 int max_pairs() {
-  static int cached_dev[64] = {};  // per device
+  // Per device (0 = not yet known).  Host threads may race on a first call: each computes the
+  // same count, and the slot is atomic.
+  static std::atomic<int> cached_dev[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
-  int& cached = cached_dev[dev];
+  std::atomic<int>& slot = cached_dev[dev];
+  int cached = slot.load(std::memory_order_acquire);
   if (cached == 0) {
     auto k = tc_gemm_kernel<EPI, OUT_BYTES, true>;
     constexpr uint32_t smem =
@@ -972,6 +979,7 @@ int max_pairs() {
     }
     cudaGetLastError();
     cached = n > 0 ? n : -1;
+    slot.store(cached, std::memory_order_release);
   }
   return cached;
 }

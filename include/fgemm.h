@@ -103,7 +103,6 @@ typedef struct {
   int split_k;    /* skinny path: K splits (1..8, one CTA each in a cluster); 0 = automatic */
   int max_ctas;   /* persistent grid cap (default: one CTA per SM) */
   int timeout_ms; /* bound on every device-side barrier wait (default 1000 ms) */
-  int b_desc_swap; /* diagnostic: exchange the two byte offsets of B's shared-memory descriptor */
   int cta_pair;   /* tensor-core path: 0 = automatic, 1 = one CTA per 128 x 256 tile,
                      2 = CTA pairs (2-SM clusters, tcgen05 cta_group::2) on 256 x 256 tiles */
   int tail_split; /* tensor-core path: 0 = cut the tiles of the last partial round of the
@@ -243,7 +242,8 @@ int fgemm_unfused_addmm_gate(const void* A, const void* B, const void* bias, con
  * workspace.  Limit: fgemm_unfused_workspace_bytes(M, N, dtype, inter_f32) must not exceed
  * FGEMM_NOALLOC_SCRATCH_BYTES, else FGEMM_ERR_WORKSPACE is returned and nothing runs.
  * The first call on each device (with that device current) looks up the array's device address
- * once; make that first call before any stream capture.  All calls share the array and it keeps
+ * and keeps it; make that first call before any stream capture.  If the lookup fails the call
+ * returns FGEMM_ERR_NO_DEVICE and the next call on that device tries it again.  All calls share the array and it keeps
  * the previous call's contents (nothing in it needs to start at zero: each call writes every
  * intermediate element before reading it); calls whose work overlaps on the GPU race on it.
  */

@@ -1,8 +1,9 @@
 """fgemm_unfused_bias_relu_noalloc: the unfused bias + ReLU chain for callers that cannot
 allocate device memory (its intermediate lives in an array the library reserves on each device).
 
-Checked against the existing entry point fgemm_unfused_bias_relu (given a workspace from the
-caller) on two calls in a row, with the same tolerance as the other parity tests.  This file is
+Checked on two calls in a row against the existing entry point fgemm_unfused_bias_relu (given
+a workspace from the caller) and against the CPU oracle, with the same tolerance as the other
+parity tests.  This file is
 collected last so that a run stopping at its first failure has already run every other test; it
 also passes on its own in a fresh process.
 """
@@ -53,6 +54,10 @@ def test_noalloc_matches_the_workspace_entry_on_two_calls_in_a_row():
         g64, w64 = oracle.decode(got, t), oracle.decode(want, t)
         assert np.all(np.isfinite(g64))
         assert float(np.abs(g64 - w64).max()) <= tolerance(K, w64, t)
+        # and against the oracle (fp64 sum, bias and ReLU after it, one rounding), so that a fault
+        # shared by both CUDA chains cannot pass
+        ref = oracle.decode(oracle.bias_relu(p.A, p.B, p.bias, M, N, K, t, t, t).out, t)
+        assert float(np.abs(g64 - ref).max()) <= tolerance(K, ref, t)
     assert fg.fgemm_device_status() == 0
 
 
