@@ -170,7 +170,7 @@ def slowest_rank(dist, value, device=None):
 class Problem:
     """Device-resident rotating input sets of one workload, and a call of the fused kernel."""
 
-    def __init__(self, w, dev, l2_bytes, max_sets=8, with_unfused=False, stream_k=True, pdl=False):
+    def __init__(self, w, dev, l2_bytes, max_sets=8, with_unfused=False):
         import torch
         from gemm_epilogue_gb300 import inputs as gen
         import gemm_epilogue_gb300.binding as fg
@@ -217,33 +217,16 @@ class Problem:
             nb = fg.fgemm_unfused_workspace_bytes(w.M, w.N, self.word, 0)
             self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
             self.ws_bytes = nb
-        # The stream-K workspace (fgemm_opts.workspace), allocated and zeroed once like any
-        # caller's: with it the library deals the last round out stream-K where the shape
-        # qualifies, and reports the workspace it needs either way.
-        self.sk_ws = None
-        self.pdl = pdl
-        if stream_k:
-            need = self.plan()["sk_workspace_bytes"]
-            if need:
-                self.sk_ws = torch.zeros(need, dtype=torch.uint8, device=dev)
-
-    def with_ws(self, opts):
-        if self.pdl and not (opts and "pdl" in opts):
-            opts = dict(opts or {}, pdl=1)
-        if self.sk_ws is None or (opts and "workspace" in opts):
-            return opts
-        return dict(opts or {}, workspace=self.sk_ws.data_ptr(), workspace_bytes=self.sk_ws.numel())
 
     def plan(self, opts=None):
         a, b, bias, y, out = self.sets[0]
         w = self.w
         return self.fg.fgemm_plan(a, b, bias, y, out, w.M, w.N, w.K, self.word,
-                                  gate=y is not None, opts=self.with_ws(opts))
+                                  gate=y is not None, opts=opts)
 
     def call(self, i, stream, opts=None, unfused=False):
         a, b, bias, y, out = self.sets[i % len(self.sets)]
         w, fg = self.w, self.fg
-        opts = self.with_ws(opts)
         if unfused:
             if y is not None:
                 fg.fgemm_unfused_addmm_gate(a, b, bias, y, out, w.M, w.N, w.K, self.word, self.ws,
@@ -382,13 +365,10 @@ def e2e_steps(prob, steps, stream):
         stream.wait_event(e_a)
         stream.wait_event(e_b)
         stream.wait_event(read_back[j])
-        opts = prob.with_ws(None)  # the same call as the device-timed steps
         if y is not None:
-            fg.fgemm_addmm_gate_ex(a, b, bias, y, out, w.M, w.N, w.K, prob.word, stream.cuda_stream,
-                                   opts)
+            fg.fgemm_addmm_gate(a, b, bias, y, out, w.M, w.N, w.K, prob.word, stream.cuda_stream)
         else:
-            fg.fgemm_bias_relu_ex(a, b, bias, out, w.M, w.N, w.K, prob.word, stream.cuda_stream,
-                                  opts)
+            fg.fgemm_bias_relu(a, b, bias, out, w.M, w.N, w.K, prob.word, stream.cuda_stream)
         computed[j].record(stream)
         down.wait_event(computed[j])
         with torch.cuda.stream(down):
@@ -455,8 +435,7 @@ def run_ours(args):
     w = gen.WORKLOADS[args.workload]
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or L2_BYTES_DEFAULT
-    prob = Problem(w, dev, l2, with_unfused=args.variant == "unfused",
-                   stream_k=not args.no_stream_k, pdl=args.pdl)
+    prob = Problem(w, dev, l2, with_unfused=args.variant == "unfused")
     stream = torch.cuda.Stream(device=dev)
     barrier = (lambda: dist.barrier()) if dist else None
     sampler = ClockSampler(local) if rank == 0 else None
@@ -510,7 +489,7 @@ def run_ours(args):
                    "epilogue": w.epilogue,
                    "out": gen.TYPE_NAMES[w.out_type], "bias": gen.TYPE_NAMES[w.bias_type],
                    "path": fg.PATH_NAMES.get(path, str(path)), "plan": prob.plan(opts),
-                   "opts": opts, "pdl": bool(args.pdl),
+                   "opts": opts,
                    "parallelism": f"replicas{world}", "launch": launch,
                    "stream_loop_ms_per_step": ms_loop,
                    "l2": f"inputs rotate over {len(prob.sets)} sets of {prob.set_bytes / 1e6:.1f} MB "
@@ -585,7 +564,7 @@ def run_sweep(args):
     for name in names:
         w = gen.WORKLOADS[name]
         unf = w.name in ("square_4096", "glu_gate_1024x21568x4096")
-        prob = Problem(w, dev, l2, with_unfused=unf, stream_k=not args.no_stream_k, pdl=args.pdl)
+        prob = Problem(w, dev, l2, with_unfused=unf)
         steps = max(5, min(200, int(2e-1 / max(w.flops / 1.2e15, 1e-6))))
         if w.name.startswith("ffn"):
             variants = [{"group_m": g} for g in (1, 4, 8, 16)]
@@ -593,8 +572,8 @@ def run_sweep(args):
             variants = [None] + [{"split_k": s, "skinny_tiles": t, "stages": g}
                                  for t in (1, 2) for s in (2, 4, 8) for g in (3, 4, 6)]
         else:
-            variants = [None, {"stream_k": 2}, {"tail_split": 1, "stream_k": 2}, {"cta_pair": 1},
-                        {"cta_pair": 1, "stream_k": 2}, {"bias_init": 1}, {"bias_init": 2}]
+            variants = [None, {"tail_split": 1}, {"cta_pair": 1}, {"cta_pair": 1, "tail_split": 1},
+                        {"bias_init": 1}, {"bias_init": 2}]
         if args.sweep_variants:
             variants = json.loads(args.sweep_variants)
         for opts in variants:
@@ -645,12 +624,6 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--variant", default="fused", choices=["fused", "unfused"],
                     help="unfused: time the GEMM -> elementwise chain instead (traffic comparison)")
-    ap.add_argument("--pdl", action="store_true",
-                    help="launch with programmatic dependent launch (fgemm_opts.pdl): a call's "
-                         "set-up overlaps the previous call's tail")
-    ap.add_argument("--no-stream-k", action="store_true",
-                    help="give the library no stream-K workspace (the last round is cut into "
-                         "column pieces instead)")
     ap.add_argument("--opts", default="",
                     help="fgemm_opts for the timed calls, as JSON (e.g. '{\"group_m\": 8}')")
     ap.add_argument("--sweep", action="store_true")

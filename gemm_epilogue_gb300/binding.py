@@ -23,7 +23,6 @@ OUT_SAME, OUT_F32, OUT_E4M3, OUT_BF16 = 0x000, 0x100, 0x200, 0x300
 # status codes
 OK, ERR_INVALID_VALUE, ERR_UNSUPPORTED_DTYPE, ERR_MISALIGNED = 0, 1, 2, 3
 ERR_NO_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_WORKSPACE = 4, 5, 6, 7
-SK_FLAG_BYTES = 16384  # FGEMM_SK_FLAG_BYTES: leading flag words of a stream-K workspace
 
 # epilogue codes (fgemm_plan)
 EPI_RELU, EPI_GATE, EPI_RESIDUAL_RELU, EPI_RELU_QUANT = 0, 1, 2, 3
@@ -48,8 +47,7 @@ class Opts(ctypes.Structure):
                 ("skinny_tiles", ctypes.c_int), ("stages", ctypes.c_int),
                 ("inject_stall", ctypes.c_int), ("bias_init", ctypes.c_int),
                 ("full_last_n", ctypes.c_int), ("y_blocks", ctypes.c_int),
-                ("k_rows", ctypes.c_int), ("stream_k", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("k_rows", ctypes.c_int), ("reserved", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -57,8 +55,7 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("tiles", ctypes.c_int), ("work_items", ctypes.c_int), ("tail_split", ctypes.c_int),
                 ("resident_pairs", ctypes.c_int), ("last_tile_n", ctypes.c_int),
-                ("y_blocks", ctypes.c_int), ("k_rows", ctypes.c_int), ("row_barriers", ctypes.c_int),
-                ("sk_tiles", ctypes.c_int), ("sk_workspace_bytes", ctypes.c_size_t)]
+                ("y_blocks", ctypes.c_int), ("k_rows", ctypes.c_int), ("row_barriers", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -92,7 +89,6 @@ _SIGS = {
     "fgemm_plan_on": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int,
                              ctypes.POINTER(Opts), _int, _int, ctypes.POINTER(PlanInfo)]),
     "fgemm_tile_of": (_int, [_i64, _i64, _i64, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
-    "fgemm_stream_k_run": (_int, [_int] * 5 + [ctypes.POINTER(_int)] * 6),
 }
 
 
@@ -146,7 +142,7 @@ def _opts(opts) -> Opts | None:
     for k, v in dict(opts).items():
         if k not in fields:  # a misspelt key would otherwise be dropped without a word
             raise ValueError(f"unknown fgemm_opts field {k!r}")
-        setattr(o, k, _ptr(v) if k == "workspace" else int(v))
+        setattr(o, k, int(v))
     return o
 
 
@@ -275,14 +271,6 @@ def fgemm_plan_on(A, B, bias, Y, out, M, N, K, dtype, num_sms, resident_pairs, g
                                ctypes.byref(info)),
            "fgemm_plan_on")
     return {name: getattr(info, name) for name, _ in PlanInfo._fields_}
-
-
-def fgemm_stream_k_run(u, units, sk_tiles, num_kb, i) -> dict:
-    """Run i of unit u in the stream-K share-out (include/fgemm.h, fgemm_stream_k_run)."""
-    out = [ctypes.c_int() for _ in range(6)]
-    _check(lib().fgemm_stream_k_run(u, units, sk_tiles, num_kb, i, *(ctypes.byref(x) for x in out)),
-           "fgemm_stream_k_run")
-    return dict(zip(("tile", "kb0", "kb1", "part", "src0", "nsrc"), (x.value for x in out)))
 
 
 def fgemm_tile_of(t, tiles_m, tiles_n, group) -> tuple[int, int]:

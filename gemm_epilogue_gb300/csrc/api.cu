@@ -11,7 +11,6 @@
 #include "fgemm.h"
 #include "kernels.h"
 #include "ptx.cuh"
-#include "stream_k.h"
 #include "tile_order.h"
 
 namespace fgemm {
@@ -173,12 +172,10 @@ int validate(const Call& c, bool* nothing) {
     if (o.group_m < 0 || o.path < 0 || o.path > FGEMM_PATH_KZERO || o.split_k < 0 ||
         o.split_k > 8 || o.max_ctas < 0 || o.timeout_ms < 0 || o.cta_pair < 0 || o.cta_pair > 2 ||
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
-        o.inject_stall < 0 || o.inject_stall > 2 || o.bias_init < 0 || o.bias_init > 2 ||
+        o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 2 ||
         o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 3 ||
-        o.k_rows < 0 || o.k_rows > 2 || o.stream_k < 0 || o.stream_k > 2 || o.pdl < 0 || o.pdl > 1 ||
-        (o.stream_k == 1 && o.bias_init == 1))
+        o.k_rows < 0 || o.k_rows > 2)
       return FGEMM_ERR_INVALID_VALUE;
-    if (o.workspace && !aligned(o.workspace, 256)) return FGEMM_ERR_MISALIGNED;
   }
   return FGEMM_OK;
 }
@@ -202,9 +199,6 @@ struct TcPlan {
   int y_blocks;          // staged Y blocks per epilogue warp (gate / residual, 16-bit out)
   int k_rows;            // 128-byte K rows per ring stage
   bool row_bars;         // a full barrier per K row of a stage
-  int sk_tiles;          // tiles of the last round computed stream-K (0 = none)
-  size_t sk_bytes;       // workspace stream-K needs for this shape (0: the shape does not qualify)
-  int sk_status;         // FGEMM_OK, or why stream-K, asked for (stream_k = 1), cannot run
 };
 
 // What the planners need to know about the device: its SM count and how many CTA pairs of the
@@ -296,38 +290,6 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
   // Each K row of a two-row stage on its own full barrier: measured faster with fp8 operands and
   // with staged Y, slower on the plain 16-bit FFN shape, equal on 4096^3.
   t.row_bars = t.k_rows > 1 && (c.t.ab == ELEM_E4M3 || staged_y);
-  // Stream-K share-out of the last round (stream_k.h) instead of the column pieces: every unit
-  // takes an equal run of the round's K blocks.  It needs a K loop long enough that a run's
-  // partial-sum exchange is small next to it (>= 16 K blocks per tile), a run of at least one
-  // K block per unit, the flags of every CTA in the workspace's flag area, and the caller's
-  // workspace.
-  {
-    const int64_t kb_k = static_cast<int64_t>(128 / elem_bytes(c.t.ab)) * t.k_rows;  // K per stage
-    const int64_t num_kb = (c.K + kb_k - 1) / kb_k;
-    const int ctas = t.units * (t.pair ? 2 : 1);
-    const bool qualifies = rem > 0 && t.num_tiles > units && num_kb >= 16 &&
-                           num_kb <= 0x7fffffff && static_cast<int64_t>(rem) * num_kb >= units &&
-                           static_cast<size_t>(ctas) * 8 * sizeof(unsigned) <= FGEMM_SK_FLAG_BYTES;
-    t.sk_bytes = qualifies ? FGEMM_SK_FLAG_BYTES + static_cast<size_t>(ctas) * tc_block_m() *
-                                                       tc_block_n() * sizeof(float)
-                           : 0;
-    const int mode = c.opts ? c.opts->stream_k : 0;
-    const bool have_ws = c.opts && c.opts->workspace && c.opts->workspace_bytes >= t.sk_bytes;
-    t.sk_status = FGEMM_OK;
-    if (mode == 1 && !qualifies)
-      t.sk_status = FGEMM_ERR_INVALID_VALUE;
-    else if (mode == 1 && !have_ws)
-      t.sk_status = FGEMM_ERR_WORKSPACE;
-    const bool bias_init_forced = c.opts && c.opts->bias_init == 1;
-    if (qualifies && have_ws && (mode == 1 || (mode == 0 && !bias_init_forced))) {
-      t.sk_tiles = rem;
-      t.tail_split = 1;
-      t.full_tiles = t.num_tiles - rem;
-      t.num_items = t.full_tiles;
-      for (int u = 0; u < units; ++u)
-        t.num_items += sk_num_runs(u, units, rem, static_cast<int>(num_kb));
-    }
-  }
   return t;
 }
 
@@ -373,7 +335,6 @@ SkPlan plan_skinny(const Call& c, const DevShape& d) {
 int run_tc(const Call& c, DeviceInfo* d) {
   const TcPlan t = plan_tc(c, shape_of(d));
   if (t.num_tiles < 0) return FGEMM_ERR_INVALID_VALUE;
-  if (t.sk_status != FGEMM_OK) return t.sk_status;
   const int BM = tc_block_m(), BN = tc_block_n();
   const int TILE_M = t.pair ? 2 * BM : BM;
   CUtensorMap tmA, tmB, tmO, tmY;
@@ -407,13 +368,6 @@ int run_tc(const Call& c, DeviceInfo* d) {
   // accumulator hand-off instead (4096^3: 90.3 vs 88.1 us).
   const int bi = c.opts ? c.opts->bias_init : 0;
   p.bias_init = (c.epi != EPI_NONE && (bi == 1 || (bi == 0 && c.K <= 1024))) ? 1 : 0;
-  // Stream-K: partial sums must not hold the bias, which the head adds once after the total.
-  p.sk_tiles = t.sk_tiles;
-  if (t.sk_tiles > 0) {
-    p.bias_init = 0;
-    p.sk_flag = static_cast<unsigned*>(c.opts->workspace);
-    p.sk_part = reinterpret_cast<float*>(static_cast<char*>(c.opts->workspace) + FGEMM_SK_FLAG_BYTES);
-  }
   p.y_blocks = t.y_blocks;
   p.k_rows = t.k_rows;
   p.row_bars = t.row_bars ? 1 : 0;
@@ -431,8 +385,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  p.inject_stall = c.opts ? c.opts->inject_stall : 0;
-  p.pdl = (c.opts && c.opts->pdl) ? 1 : 0;
+  p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
   return status_of(
       launch_tc(c.epi, tmA, tmB, tmO, tmY, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
 }
@@ -464,8 +417,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   const int tmo_ms = (c.opts && c.opts->timeout_ms > 0) ? c.opts->timeout_ms : 1000;
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
-  p.inject_stall = (c.opts && c.opts->inject_stall == 1) ? 1 : 0;
-  p.pdl = (c.opts && c.opts->pdl) ? 1 : 0;
+  p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
   if (!skinny_fits(s.mpad, s.nt, s.split, s.stages)) return FGEMM_ERR_INVALID_VALUE;
   return status_of(launch_skinny(c.epi, tmB, tmA, p, s.groups * s.split, c.stream));
 }
@@ -744,9 +696,6 @@ int plan_info(const void* A, const void* B, const void* bias, const void* Y, con
     info->k_rows = t.k_rows;
     info->resident_pairs = t.resident;
     info->row_barriers = t.row_bars ? 1 : 0;
-    info->sk_tiles = t.sk_tiles;
-    info->sk_workspace_bytes = t.sk_bytes;
-    if (t.sk_status != FGEMM_OK) return t.sk_status;
   } else if (path == FGEMM_PATH_SKINNY) {
     const SkPlan s = plan_skinny(c, dev);
     info->cluster = s.split;
@@ -780,23 +729,6 @@ int fgemm_plan_on(const void* A, const void* B, const void* bias, const void* Y,
   }
   const DevShape shape{num_sms, resident_pairs};
   return plan_info(A, B, bias, Y, out, M, N, K, dtype, epilogue, opts, &shape, info);
-}
-
-int fgemm_stream_k_run(int u, int units, int sk_tiles, int num_kb, int i, int* tile, int* kb0,
-                       int* kb1, int* part, int* src0, int* nsrc) {
-  if (!tile || !kb0 || !kb1 || !part || !src0 || !nsrc || units < 1 || sk_tiles < 1 ||
-      sk_tiles >= units || num_kb < 1 || static_cast<int64_t>(sk_tiles) * num_kb < units ||
-      u < 0 || u >= units || i < 0 || i >= sk_num_runs(u, units, sk_tiles, num_kb))
-    return FGEMM_ERR_INVALID_VALUE;
-  SkRun r;
-  sk_run(u, units, sk_tiles, num_kb, 0, i, r);
-  *tile = r.tile;
-  *kb0 = r.kb0;
-  *kb1 = r.kb1;
-  *part = r.part;
-  *src0 = r.src0;
-  *nsrc = r.nsrc;
-  return FGEMM_OK;
 }
 
 int fgemm_tile_of(int64_t t, int64_t tiles_m, int64_t tiles_n, int group, int64_t* m_tile,

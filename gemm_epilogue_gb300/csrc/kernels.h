@@ -40,14 +40,7 @@ struct TcParams {
   uint32_t idesc;  // tcgen05 instruction descriptor
   uint64_t timeout_ns;
   int* err;        // device error word
-  int inject_stall;  // diagnostic (see fgemm_opts): 1 = CTA 0 skips the loads of its first stage,
-                     // 2 = stream-K runs that end a tile never raise their flags
-  // Stream-K share-out of the last round (stream_k.h): the last sk_tiles tiles of the grouped
-  // order (full_tiles = num_tiles - sk_tiles, tail_split = 1); 0 = none.
-  int pdl;          // launch with programmatic stream serialization (see fgemm_opts)
-  int sk_tiles;
-  float* sk_part;     // per unit and CTA rank: 128 rows x 256 columns of fp32 partial sums
-  unsigned* sk_flag;  // per unit, CTA rank and epilogue warp: 1 = that warp's partial sums written
+  int inject_stall;  // diagnostic: CTA 0 skips the loads of its first stage (see fgemm_opts)
 };
 
 // Generic CUDA-core kernel and elementwise kernels: plain pointers.
@@ -92,7 +85,6 @@ struct SkParams {
   uint64_t timeout_ns;
   int* err;
   int inject_stall;  // diagnostic: CTA 0 skips the loads of its first stage (see fgemm_opts)
-  int pdl;           // launch with programmatic stream serialization (see fgemm_opts)
 };
 cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           const SkParams& p, int ctas, cudaStream_t s);

@@ -294,60 +294,6 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-// ---------------------------------------------------------------- programmatic dependent launch
-// Wait until the grids this one depends on have completed and their memory operations are
-// visible (returns at once for a launch without programmatic serialization), and let the grids
-// that depend on this one be scheduled before it ends.
-__device__ __forceinline__ void grid_dependency_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependents_launch() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- flags in global memory
-// A flag word that one warp raises after writing data to global memory and another warp (of
-// another CTA) waits for before reading it: release / acquire at GPU scope.
-__device__ __forceinline__ void flag_raise(unsigned* f) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(1u) : "memory");
-}
-__device__ __forceinline__ void flag_clear(unsigned* f) {
-  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(0u) : "memory");
-}
-__device__ __forceinline__ unsigned flag_load_acquire(const unsigned* f) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
-  return v;
-}
-// Bounded wait, by a whole warp, until *f is raised: every lane acquires the raised flag itself.
-// Returns false (warp-uniform) if the CTA's abort flag is raised or the wait exceeds `timeout_ns`;
-// in the latter case it raises the abort flag and records `site` in the device error word.
-__device__ __forceinline__ bool flag_wait_warp(const unsigned* f, volatile int* abort_flag,
-                                               uint64_t timeout_ns, int* err, int site) {
-  uint64_t start = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (__all_sync(0xffffffffu, flag_load_acquire(f) != 0u)) return true;
-    if ((it & 63u) == 63u) {
-      int stop = 0;
-      if ((threadIdx.x & 31u) == 0) {
-        if (*abort_flag) {
-          stop = 1;
-        } else {
-          const uint64_t now = global_ns();
-          if (start == 0) {
-            start = now;
-          } else if (now - start > timeout_ns) {
-            *abort_flag = 1;
-            atomicCAS(err, 0, 6 /* FGEMM_ERR_TIMEOUT */ | (site << 8));
-            stop = 1;
-          }
-        }
-      }
-      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-    }
-  }
-}
-
 // Address of the same shared-memory location in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t local, uint32_t rank) {
   uint32_t r;

@@ -157,10 +157,6 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Global memory only from here on (programmatic dependent launch: the set-up above overlaps
-  // the previous kernel's tail).
-  grid_dependency_wait();
-  grid_dependents_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -275,10 +271,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
       const uint32_t dst = remote ? map_shared_rank(slot, owner) : slot;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(t * p.mpad);
-      // the owners read m < 4 ceil(M / 4) only: with M = 1 the MMA's 16 columns hold 15 padding
-      // rows, and pushing them would be three quarters of the exchange
-      const int mlim = 4 * ((p.M + 3) / 4);
-      for (int c = half; c < p.mpad / 16 && 16 * c < mlim; c += halves) {
+      for (int c = half; c < p.mpad / 16; c += halves) {
         uint32_t v[16];
         if (have) {
           __syncwarp();
@@ -290,7 +283,6 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {  // m = 16 c + j; the warp's lanes write consecutive rows
-          if (16 * c + j >= mlim) break;
           const uint32_t a = dst + 4u * static_cast<uint32_t>((16 * c + j) * pitch);
           if (remote)
             st_shared_cluster_f32(a, __uint_as_float(v[j]));
@@ -374,15 +366,13 @@ cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkPar
   cfg.blockDim = dim3(static_cast<unsigned>(64 + 32 * epi_warps_for(p.mpad)));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(p.split);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.pdl ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k, tb, ta, p);
 }
 

@@ -36,20 +36,12 @@
 //               loop runs (a whole 8 KB block per warp a work item ahead, or one 4 KB chunk at a
 //               time on long K loops), and the result is written over it and stored from there;
 //               with fp32 outputs it is loaded straight into registers ahead of the TMEM read.
-// Stream-K (with a caller's workspace): the tiles of the last, partial round are dealt to the
-// units as equal runs of K blocks (stream_k.h), done before the unit's whole tiles.  A run that
-// does not start its tile stores its fp32 sums to the workspace and raises a flag per epilogue
-// warp; the tile's head run waits for those flags (bounded), adds the sums in K order after its
-// TMEM read and runs the epilogue once on the total, so the bias and the activation still come
-// once, after the full reduction.
-// The accumulator goes from TMEM to registers to the single store; it never touches HBM (a
-// stream-K partial sum crosses it once, in the workspace).
+// The accumulator goes from TMEM to registers to the single store; it never touches HBM.
 #include <atomic>
 #include <type_traits>
 
 #include "kernels.h"
 #include "ptx.cuh"
-#include "stream_k.h"
 #include "tile_order.h"
 
 namespace fgemm {
@@ -113,7 +105,7 @@ constexpr uint32_t OFF_ABORT = 280;
 
 // wait sites recorded with a timeout
 enum { SITE_PROD_EMPTY = 1, SITE_MMA_ACC_EMPTY, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN,
-       SITE_EPI_Y, SITE_SK_FLAG };
+       SITE_EPI_Y };
 
 // Bounded wait that ignores the abort flag: used only to drain copies / MMAs already in flight.
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
@@ -122,17 +114,14 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64
   return mbar_wait(bar, parity, &never, timeout_ns, err, SITE_DRAIN);
 }
 
-// One unit of work of the persistent loop: a whole 256-column tile, a piece of a tail tile, or a
-// stream-K run over some of a tile's K blocks.
+// One unit of work of the persistent loop: a whole 256-column tile, or a piece of a tail tile.
 struct Work {
-  int tm, tn;     // tile coordinates
-  int col0;       // first output column of the piece
-  int width;      // columns in the piece (256, 128 or 64)
-  int kb0, kb1;   // K blocks [kb0, kb1): the whole K loop, or a stream-K run
-  int part;       // >= 0: a stream-K run that does not start its tile: its sums go to slot `part`
-  int src0, nsrc; // stream-K head: add the partial sums of slots src0 .. src0 + nsrc - 1
+  int tm, tn;   // tile coordinates
+  int col0;     // first output column of the piece
+  int width;    // columns in the piece (256, 128 or 64)
 };
-__device__ __forceinline__ void piece_of(const TcParams& p, int item, Work& w) {
+__device__ __forceinline__ Work work_of(const TcParams& p, int item) {
+  Work w;
   int tile = item, piece = 0, split = 1;
   if (item >= p.full_tiles) {
     const int j = item - p.full_tiles;
@@ -147,53 +136,7 @@ __device__ __forceinline__ void piece_of(const TcParams& p, int item, Work& w) {
     const int left = p.last_width - piece * w.width;
     if (left < w.width) w.width = left > 0 ? left : p.gran;
   }
-}
-
-// Work item i of persistent unit u (a CTA, or a CTA pair), false past its last.  Without
-// stream-K the unit takes items u, u + units, u + 2 units, ...; with it, first its stream-K runs
-// (stream_k.h), then the whole tiles u, u + units, ... below full_tiles.
-__device__ __forceinline__ bool work_at(const TcParams& p, int num_kb, int u, int units, int i,
-                                        Work& w) {
-  w.kb0 = 0;
-  w.kb1 = num_kb;
-  w.part = -1;
-  w.src0 = 0;
-  w.nsrc = 0;
-  int last = p.num_items;
-  if (p.sk_tiles > 0) {
-    const int runs = sk_num_runs(u, units, p.sk_tiles, num_kb);
-    if (i < runs) {
-      SkRun r;
-      sk_run(u, units, p.sk_tiles, num_kb, p.full_tiles, i, r);
-      piece_of(p, r.tile, w);
-      w.kb0 = r.kb0;
-      w.kb1 = r.kb1;
-      w.part = r.part;
-      w.src0 = r.src0;
-      w.nsrc = r.nsrc;
-      return true;
-    }
-    i -= runs;
-    last = p.full_tiles;
-  }
-  const int item = u + i * units;
-  if (item >= last) return false;
-  piece_of(p, item, w);
-  return true;
-}
-
-// Adds one stream-K slot's fp32 sums of this thread's row (`src` points at the row's first
-// float4) for the NC columns from `col` (a multiple of 4) to the accumulator words in `acc`.
-template <int NC>
-__device__ __forceinline__ void sk_add_cols(const float4* src, int col, uint32_t (&acc)[NC]) {
-#pragma unroll
-  for (int e = 0; e < NC / 4; ++e) {
-    const float4 f = __ldcg(src + ((col >> 2) + e) * BM);
-    acc[4 * e] = __float_as_uint(__uint_as_float(acc[4 * e]) + f.x);
-    acc[4 * e + 1] = __float_as_uint(__uint_as_float(acc[4 * e + 1]) + f.y);
-    acc[4 * e + 2] = __float_as_uint(__uint_as_float(acc[4 * e + 2]) + f.z);
-    acc[4 * e + 3] = __float_as_uint(__uint_as_float(acc[4 * e + 3]) + f.w);
-  }
+  return w;
 }
 
 // Bias of the 128 columns [col, col + 128) that one epilogue warpgroup owns: lane l holds columns
@@ -307,10 +250,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (PAIR) cluster_sync();  // the peer signals the even CTA's barriers: both must be initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // Above, only this CTA's shared and tensor memory were touched: with programmatic dependent
-  // launch that part overlaps the previous kernel's tail.  Global memory only from here on.
-  grid_dependency_wait();
-  grid_dependents_launch();
 
   const int num_kb = (p.K + KB_ELEMS - 1) / KB_ELEMS;
   const uint64_t tmo = p.timeout_ns;
@@ -326,8 +265,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       bool ok = true;
-      Work wk;
-      for (int i = 0; ok && work_at(p, num_kb, unit, units, i, wk); ++i) {
+      for (int t = unit; ok && t < p.num_items; t += units) {
+        const Work wk = work_of(p, t);
         const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM;
         // each CTA of a pair stages half of the piece's columns
         const int cols = PAIR ? wk.width / 2 : wk.width;
@@ -336,7 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // bytes per full barrier: one K row, or the whole stage (both CTAs of a pair)
         const uint32_t tx = (PAIR ? 2u : 1u) * (A_ROW_BYTES + static_cast<uint32_t>(boxes) * BBOX_ROW) *
                             static_cast<uint32_t>(KSUB / nfb);
-        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
+        for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err,
                          SITE_PROD_EMPTY)) {
             ok = false;
@@ -345,7 +284,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a_dst = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_dst = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
           // diagnostic stall: announce the stage's bytes but never load them
-          const bool stall = p.inject_stall == 1 && blockIdx.x == 0 && i == 0 && kb == wk.kb0;
+          const bool stall = p.inject_stall && blockIdx.x == 0 && t == unit && kb == 0;
           // the even CTA's full barriers count both CTAs' bytes
           if (leader)
             for (int f = 0; f < nfb; ++f) mbar_arrive_expect_tx(bar(BAR_FULL + stage * KSUB + f), tx);
@@ -393,10 +332,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint16_t kPair = 0x3;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      Work wk;
-      for (int it = 0; ok && work_at(p, num_kb, unit, units, it, wk); ++it) {
+      int it = 0;
+      for (int t = unit; ok && t < p.num_items; t += units, ++it) {
         // MMA N = the piece's width (all tiles but the tail pieces: 256)
-        const int width = wk.width;
+        const int width = work_of(p, t).width;
         const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(width >> 3) << 17);
         const int b = it & 1;
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
@@ -407,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
-        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
+        for (int kb = 0; kb < num_kb; ++kb) {
           const uint32_t a_addr = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_addr = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
 #pragma unroll
@@ -426,8 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                   sdesc_sw128(a_addr + (k / KPR) * A_ROW_BYTES + 32u * (k % KPR), 16u, 1024u);
               // MN-major B: one column box (BBOX bytes) apart along N, 1 KB per 8 K rows
               const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, BBOX, 1024u);
-              // the first MMA of a tile (or of a stream-K run) starts the sum
-              const uint32_t acc = (p.bias_init | (kb - wk.kb0) | k) != 0 ? 1u : 0u;
+              const uint32_t acc = (p.bias_init | kb | k) != 0 ? 1u : 0u;
               if constexpr (F8)
                 umma_f8_cg<CG>(d_tmem, ad, bd, idesc, acc);
               else
@@ -458,61 +396,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool y_bf = p.ab_bf16 != 0;
     const uint64_t pol_out = policy_evict_first();
     const bool add_bias = !p.bias_init;  // else the accumulator already holds the bias
-    // Stream-K slots: per unit and CTA rank, the CTA's 128 rows x 256 columns of fp32 sums as
-    // float4s [column / 4][row]; one flag per unit, CTA rank and epilogue warp.
-    auto sk_slot = [&](int s) {
-      return reinterpret_cast<float4*>(p.sk_part) +
-             static_cast<size_t>(s * CG + static_cast<int>(rank)) * (BM * BN / 4);
-    };
-    auto sk_flag_of = [&](int s) {
-      return p.sk_flag + (s * CG + static_cast<int>(rank)) * EPI_WARPS + ew;
-    };
-    // Stream-K head: add the sums of the tile's later K blocks, in K order, to this thread's row
-    // of the accumulator columns [col, col + NC).
-    auto sk_add = [&](const Work& w, int col, auto& acc) {
-      for (int s = 0; s < w.nsrc; ++s) sk_add_cols(sk_slot(w.src0 + s) + (32 * q + lane), col, acc);
-    };
-    // Stream-K run that does not start its tile: the warp's 32 rows x (up to) 128 columns of fp32
-    // sums go to its slot (four columns of a row per 16-byte store; one warp store covers 32
-    // consecutive rows, 512 contiguous bytes), then the warp raises its flag.
-    auto sk_write = [&](const Work& w, uint32_t taddr) {
-      float4* dst = sk_slot(w.part) + (32 * q + lane);
-#pragma unroll 1
-      for (int c = cbeg; c < cbeg + BN / 2 && c < w.width; c += 32) {
-        uint32_t v[32];
-        __syncwarp();  // tcgen05.ld is warp-collective
-        tmem_ld32(taddr, v, c);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          __stcg(dst + ((c >> 2) + e) * BM,
-                 make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                             __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
-      }
-      __threadfence();
-      __syncwarp();  // every lane's stores come before lane 0's release
-      if (lane == 0 && p.inject_stall != 2) flag_raise(sk_flag_of(w.part));  // 2: diagnostic
-    };
-    // Stream-K head: wait until the units that ran the tile's later K blocks have written this
-    // warp's rows and columns of their sums (false: the wait expired or the CTA aborts).
-    auto sk_wait = [&](const Work& w) {
-      bool ready = true;
-      for (int s = 0; s < w.nsrc && ready; ++s)
-        ready = flag_wait_warp(sk_flag_of(w.src0 + s), abort_flag, tmo, p.err, SITE_SK_FLAG);
-      return ready;
-    };
-    // The sums read, the head puts the flags back to zero for the next call (one reader each).
-    auto sk_clear = [&](const Work& w) {
-      if (lane == 0)
-        for (int s = 0; s < w.nsrc; ++s) flag_clear(sk_flag_of(w.src0 + s));
-    };
     // Bias-initialised accumulator ("Optimizing GEMM + Activation on CDNA4 with TLX", V4: the
     // accumulator starts at the bias instead of zero): this warp writes bias[col] into every lane
     // (row) of its quarter and every column of its half of buffer bb for work item t, then hands
     // the buffer to the MMA warp, whose first MMA of the tile accumulates onto it.
-    auto release_acc = [&](int inext, int bb) {
-      Work w;
-      if (p.bias_init && work_at(p, num_kb, unit, units, inext, w)) {
+    auto release_acc = [&](int t, int bb) {
+      if (p.bias_init && t < p.num_items) {
+        const Work w = work_of(p, t);
         const uint32_t ta =
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(bb * BN);
         float bq[4];
@@ -539,8 +429,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     };
     if (p.bias_init) {  // first use of both buffers
-      release_acc(0, 0);
-      release_acc(1, 1);
+      release_acc(unit, 0);
+      release_acc(unit + units, 1);
     }
     int it = 0;
     if constexpr (YS) {
@@ -556,10 +446,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr int NYB = YHALF ? 1 : YB;  // prefetched Y blocks per warp
       auto ybar = [&](int yb) { return bar(BAR_Y + yb * EPI_WARPS + ew); };
       uint32_t y_par = 0, y_issued = 0;  // bit yb: parity to wait for / a load is in flight
-      auto issue_y = [&](int i, int yb) -> bool {  // warp-uniform result
-        Work w;
-        if (!work_at(p, num_kb, unit, units, i, w)) return false;
-        if (w.part >= 0) return false;  // a stream-K run that only writes partial sums: no Y
+      auto issue_y = [&](int t, int yb) -> bool {  // warp-uniform result
+        const Work w = work_of(p, t);
         const int r0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + 32 * q;
         if (r0 >= p.M) return false;
         int nchunks = 0;
@@ -577,9 +465,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         return true;
       };
       for (int j = 0; j < NYB; ++j)
-        if (issue_y(j, j)) y_issued |= 1u << j;
-      Work wk;
-      for (; work_at(p, num_kb, unit, units, it, wk); ++it) {
+        if (unit + j * units < p.num_items && issue_y(unit + j * units, j)) y_issued |= 1u << j;
+      for (int t = unit; t < p.num_items; t += units, ++it) {
+        const Work wk = work_of(p, t);
         const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = wk.col0;
         const int nch = wk.width / CH;
         const int b = it & 1;
@@ -587,7 +475,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int row0 = m0 + 32 * q;
         const bool rows_live = row0 < p.M;  // warp-uniform
         float bq[4];
-        if (add_bias && wk.part < 0) load_bias_quad(p, n0 + cbeg, bq);
+        if (add_bias) load_bias_quad(p, n0 + cbeg, bq);
 
         if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
           break;
@@ -600,13 +488,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
-        if (wk.part >= 0) {  // stream-K run that does not start its tile: no Y, no store
-          sk_write(wk, taddr);
-          release_acc(it + 2, b);
-          if (issue_y(it + NYB, yb)) y_issued |= 1u << yb;
-          continue;
-        }
-        if (wk.nsrc > 0 && !sk_wait(wk)) break;  // stream-K head
         bool aborted = false;
 #pragma unroll 1
         for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
@@ -637,7 +518,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld32(taddr, a1, c * CH + 32);
             tmem_ld_wait();
           }
-          sk_add(wk, c * CH, acc);
           const uint32_t sb = YHALF ? ebuf
                                     : ebuf + static_cast<uint32_t>(yb) * C::Y_BLOCK_BYTES +
                                           static_cast<uint32_t>(c - cbeg / CH) * EPI_BUF_BYTES;
@@ -696,19 +576,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (aborted) break;
         if (lane == 0) bulk_commit();
-        sk_clear(wk);
         // This warp has finished reading accumulator b: release it to the MMA warp.
-        release_acc(it + 2, b);
+        release_acc(t + 2 * units, b);
         // Prefetch into this block the Y of the work item NYB items ahead (main loops run
         // meanwhile).
-        if (issue_y(it + NYB, yb)) y_issued |= 1u << yb;
+        if (t + NYB * units < p.num_items && issue_y(t + NYB * units, yb)) y_issued |= 1u << yb;
       }
       // After an abort a prefetched Y block may still be landing: wait for it (bounded).
       for (int j = 0; j < NYB; ++j)
         if ((y_issued >> j) & 1u) drain_wait(ybar(j), (y_par >> j) & 1u, tmo, p.err);
     } else {
-    Work wk;
-    for (; work_at(p, num_kb, unit, units, it, wk); ++it) {
+    for (int t = unit; t < p.num_items; t += units, ++it) {
+      const Work wk = work_of(p, t);
       const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM, n0 = wk.col0;
       const int nch = wk.width / CH;
       const int b = it & 1;
@@ -718,20 +597,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool rows_live = row0 < p.M;  // warp-uniform
       const bool use_bias = EPI != EPI_NONE && add_bias;
       float bq[4];
-      if (use_bias && wk.part < 0) load_bias_quad(p, n0 + cbeg, bq);
+      if (use_bias) load_bias_quad(p, n0 + cbeg, bq);
 
       if (!mbar_wait_sleepy(bar(BAR_ACC_FULL + b), acc_phase, abort_flag, tmo, p.err, SITE_EPI_ACC_FULL))
         break;
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
-
-      if (wk.part >= 0) {  // stream-K run that does not start its tile
-        sk_write(wk, taddr);
-        release_acc(it + 2, b);
-        continue;
-      }
-      if (wk.nsrc > 0 && !sk_wait(wk)) break;  // stream-K head
 
 #pragma unroll 1
       for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
@@ -754,7 +626,6 @@ __global__ void __launch_bounds__(THREADS, 1)
               tmem_ld32(taddr, a1, c * CH + 64 * h + 32);
               tmem_ld_wait();
             }
-            sk_add(wk, c * CH + 64 * h, acc);
 #pragma unroll
             for (int gi = 0; gi < 4; ++gi) {
               const int g = 4 * h + gi;  // 16-column granule within the 128-column row
@@ -819,7 +690,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tmem_ld_wait();
         }
-        sk_add(wk, c * CH, acc);
 
         // Staging buffer: wait until the store that last read it has finished reading.
         const uint32_t sb = ebuf;
@@ -894,9 +764,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         }  // OUT_BYTES != 1
       }
-      sk_clear(wk);
       // This warp has finished reading accumulator b: release it to the MMA warp.
-      release_acc(it + 2, b);
+      release_acc(t + 2 * units, b);
     }
     }
     if (lane == 0) bulk_wait<0>();
@@ -935,15 +804,13 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.pdl ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, k, a, b, o, y, p);
 }
 

@@ -93,9 +93,6 @@ typedef enum {
 #define FGEMM_PATH_KZERO 4   /* K == 0: epilogue over the zero accumulator, no MMA */
 #define FGEMM_PATH_NONE 5    /* M == 0 or N == 0: nothing launched */
 
-/* Leading bytes of a stream-K workspace that hold its flag words (see fgemm_opts.workspace). */
-#define FGEMM_SK_FLAG_BYTES 16384
-
 /* Per-call options of the _ex entry points.  Zero-initialised fields mean "default". */
 typedef struct {
   int group_m;    /* M-tiles per band of the grouped tile order (default 16; 1 = row-major) */
@@ -114,10 +111,7 @@ typedef struct {
                        announces its first stage but issues none of its loads, so the MMA's wait
                        on that stage can never complete; it expires after timeout_ms, the kernel
                        drains and exits, and fgemm_device_status reports FGEMM_ERR_TIMEOUT.
-                       The output of that call is undefined.  Tensor-core and skinny paths.
-                       2 = (tensor-core path with stream-K) the runs that end a tile never
-                       raise their flags, so every head's wait for them expires the same way;
-                       the workspace's flags stay zero. */
+                       The output of that call is undefined.  Tensor-core and skinny paths. */
   int bias_init;  /* tensor-core path: start each tile's accumulator at the bias (written into
                      tensor memory before the K loop) instead of adding it after the reduction;
                      same result up to the rounding order ("Optimizing GEMM + Activation on CDNA4
@@ -135,33 +129,7 @@ typedef struct {
                      elements) per stage of the operand ring; 0 = automatic (2, or 1 for the
                      gate and residual with 16-bit outputs), 1 = six stages of 32 KB per SM,
                      2 = three stages of 64 KB.  Ignored elsewhere. */
-  int stream_k;   /* tensor-core path: how the tiles of the persistent grid's last, partial round
-                     are shared out.  0 = automatic: stream-K when `workspace` is given and the
-                     shape qualifies (below), else the 128- / 64-column pieces of tail_split;
-                     1 = stream-K (FGEMM_ERR_WORKSPACE without a large enough workspace,
-                     FGEMM_ERR_INVALID_VALUE where the shape does not qualify); 2 = never.
-                     Stream-K: every CTA (pair) takes an equal share of the K blocks of those
-                     tiles, one contiguous run in (tile, K block) order, before its whole tiles.
-                     A run that does not start a tile ends it: its fp32 partial sums go to the
-                     workspace and a flag is raised; the CTA that holds the tile's first K block
-                     adds them, in K order, to its own sum and runs the epilogue once on the
-                     total.  The sum is deterministic for a given plan, but its rounding order
-                     depends on the grid (max_ctas, the device) and on group_m, unlike the
-                     other tail cuts.  Qualifies: at least 16 K blocks per tile, at least one
-                     K block per CTA (pair); the bias is then added after the sum
-                     (bias_init = 1 is refused). */
-  int pdl;        /* tensor-core and skinny paths: 1 = launch with programmatic stream
-                     serialization, so that the kernel's set-up (barriers, tensor memory) runs
-                     while the previous kernel in the stream finishes; the kernel waits for that
-                     kernel's completion (griddepcontrol.wait) before its first access to global
-                     memory, so any dependency between the two stays safe.  0 = off. */
-  /* Stream-K workspace (device memory, 256-byte aligned, caller-owned; fgemm_plan reports the
-     bytes needed as sk_workspace_bytes).  Its first FGEMM_SK_FLAG_BYTES bytes hold flag words
-     that must be zero before the first call; every call that completes leaves them zero again.  After a call that
-     reported an error through fgemm_device_status, zero them again before the next use.  Calls
-     whose work overlaps on the GPU must not share a workspace. */
-  void* workspace;
-  size_t workspace_bytes;
+  int reserved;
 } fgemm_opts;
 
 /*
@@ -285,9 +253,6 @@ typedef struct {
   int k_rows;         /* tensor-core path: 128-byte K rows per ring stage (see fgemm_opts) */
   int row_barriers;   /* tensor-core path, two K rows per stage: 1 = each K row of a stage lands on
                          its own full barrier (fp8 operands and staged second operands) */
-  int sk_tiles;       /* tensor-core path: tiles of the last round computed stream-K (0 = none) */
-  size_t sk_workspace_bytes; /* tensor-core path: workspace bytes stream-K needs for this call
-                                (0 where the shape does not qualify), whether or not one is given */
 } fgemm_plan_info;
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
                int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,
@@ -310,22 +275,6 @@ int fgemm_plan_on(const void* A, const void* B, const void* bias, const void* Y,
  */
 int fgemm_tile_of(int64_t t, int64_t tiles_m, int64_t tiles_n, int group, int64_t* m_tile,
                   int64_t* n_tile);
-
-/*
- * The stream-K share-out of the tensor-core path (fgemm_opts.stream_k), on the host, for tests
- * and tools.  `sk_tiles` tiles of `num_kb` K blocks each are dealt to `units` CTAs (or CTA pairs):
- * unit u takes the K blocks [u S / units, (u + 1) S / units) of the S = sk_tiles x num_kb, in
- * (tile, K block) order, as one or two runs split at a tile boundary.  Run `i` (0 or 1) of unit
- * `u`: *tile (0-based among the stream-K tiles), K blocks [*kb0, *kb1) of it, *part (>= 0: the
- * run does not start its tile and its partial sums go to slot *part = u; else -1), *src0 and
- * *nsrc (the run starts its tile but does not end it: it adds the sums of slots *src0 ..
- * *src0 + *nsrc - 1, in that order, which is K order; else 0 and 0).  Returns
- * FGEMM_ERR_INVALID_VALUE (and writes nothing) if a pointer is NULL, units < 1, sk_tiles < 1,
- * sk_tiles >= units, num_kb < 1, sk_tiles x num_kb < units, u is outside [0, units), or the unit
- * has no run i.
- */
-int fgemm_stream_k_run(int u, int units, int sk_tiles, int num_kb, int i, int* tile, int* kb0,
-                       int* kb1, int* part, int* src0, int* nsrc);
 
 #ifdef __cplusplus
 }

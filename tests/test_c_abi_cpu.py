@@ -41,20 +41,6 @@ int main(void) {
     return 12;
   printf("plan %d %d %d %d %d\n", info.path, info.grid, info.cluster, info.tiles, info.work_items);
   printf("unfused %lu\n", (unsigned long)fgemm_unfused_workspace_bytes(4096, 4096, FGEMM_BF16, 0));
-  /* the same plan with a stream-K workspace: the 28 tiles of the last round shared out */
-  opts.workspace = (void*)0x60000000;
-  opts.workspace_bytes = info.sk_workspace_bytes;
-  if (fgemm_plan_on((const void*)0x10000000, (const void*)0x20000000, (const void*)0x30000000,
-                    NULL, (const void*)0x50000000, 4096, 4096, 4096, FGEMM_BF16, FGEMM_EPI_RELU,
-                    &opts, 152, 76, &info) != FGEMM_OK)
-    return 15;
-  printf("stream-k %d %lu\n", info.sk_tiles, (unsigned long)info.sk_workspace_bytes);
-  {
-    int tile, kb0, kb1, part, src0, nsrc;
-    if (fgemm_stream_k_run(1, 76, 28, 32, 0, &tile, &kb0, &kb1, &part, &src0, &nsrc) != FGEMM_OK)
-      return 16;
-    printf("run %d %d %d %d %d %d\n", tile, kb0, kb1, part, src0, nsrc);
-  }
   /* validation happens before any device is looked for */
   if (fgemm_bias_relu(NULL, NULL, NULL, NULL, -1, 1, 1, FGEMM_BF16, NULL) != FGEMM_ERR_INVALID_VALUE)
     return 13;
@@ -106,7 +92,3 @@ def test_c_program_calls_the_host_entries(tmp_path, lib_path):
     # 128-column pieces: 228 + 56 work items
     assert "plan 1 152 2 256 284" in lines
     assert f"unfused {4096 * 4096 * 2}" in lines
-    # with a workspace: 28 stream-K tiles, the flag area and 152 CTA slots of 128 x 256 fp32
-    assert f"stream-k 28 {16384 + 152 * 128 * 256 * 4}" in lines
-    # unit 1 of 76 takes K blocks [11, 23) of the 28 x 32: tile 0, blocks 11..22, its own slot
-    assert "run 0 11 23 1 0 0" in lines

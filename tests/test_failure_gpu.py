@@ -50,27 +50,3 @@ def test_stalled_wait_times_out_and_the_context_survives(M, N, K, sel):
     ref = oracle.bias_relu(p.A, p.B, p.bias, M, N, K, BF16, BF16, BF16)
     check_close(down(out, BF16), ref, K, BF16, bias64=oracle.decode(p.bias, BF16), what="after stall")
     assert fg.fgemm_device_status() == 0
-
-
-def test_stream_k_flag_wait_times_out_and_the_context_survives():
-    # The stream-K heads wait for flags that other CTAs raise in global memory; the diagnostic
-    # inject_stall = 2 keeps those flags down, so the heads' bounded waits (site 7) must expire.
-    M, N, K = 700, 1800, 2048
-    ws = torch.zeros(64 << 20, dtype=torch.uint8, device="cuda")
-    sel = {"cta_pair": 2, "max_ctas": 10, "stream_k": 1, "workspace": ws.data_ptr(),
-           "workspace_bytes": ws.numel()}
-    p = gen.random_problem(M, N, K, BF16, BF16, seed=5)
-    A, B, bias = up(p.A, BF16), up(p.B, BF16), up(p.bias, BF16)
-    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    assert fg.fgemm_plan(A, B, bias, None, out, M, N, K, fg.BF16, opts=sel)["sk_tiles"] > 0
-    fg.fgemm_bias_relu_ex(A, B, bias, out, M, N, K, fg.BF16,
-                          opts=dict(sel, inject_stall=2, timeout_ms=50))
-    code = fg.fgemm_device_status()
-    assert code & 0xFF == fg.ERR_TIMEOUT and code >> 8 == 7, hex(code)
-    assert int(ws[:fg.SK_FLAG_BYTES].count_nonzero()) == 0
-    fg.fgemm_bias_relu_ex(A, B, bias, out, M, N, K, fg.BF16, opts=sel)
-    torch.cuda.synchronize()
-    ref = oracle.bias_relu(p.A, p.B, p.bias, M, N, K, BF16, BF16, BF16)
-    check_close(down(out, BF16), ref, K, BF16, bias64=oracle.decode(p.bias, BF16),
-                what="after stream-K stall")
-    assert fg.fgemm_device_status() == 0
