@@ -98,9 +98,11 @@ def recorded_traffic(workload: str, kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs.  Each sample
+    carries nvidia-smi's own timestamp (local wall clock), so that only the samples taken inside
+    the timed window count."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -115,7 +117,19 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _when(stamp: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp.strip(), fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, window=None):
+        """Summary of the samples taken inside `window` = (t0, t1) in time.time() seconds (all
+        samples when None)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -126,27 +140,34 @@ class ClockSampler:
             out, _ = self.proc.communicate()
         for line in out.splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                self.rows.append({"sm": float(parts[1]), "max": float(parts[2]),
-                                  "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else 0.0,
-                                  "hw_slow": parts[5], "hw_therm": parts[6], "sw_therm": parts[7],
-                                  "sw_power": parts[8]})
+                self.rows.append({"t": self._when(parts[0]), "sm": float(parts[2]),
+                                  "max": float(parts[3]),
+                                  "power": float(parts[4]) if parts[4] not in ("[N/A]", "") else 0.0,
+                                  "hw_slow": parts[6], "hw_therm": parts[7], "sw_therm": parts[8],
+                                  "sw_power": parts[9]})
             except ValueError:
                 continue
-        if not self.rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        loaded = [r for r in self.rows if r["power"] > 300.0] or self.rows
+        rows = self.rows
+        if window is not None:
+            t0, t1 = window
+            rows = [r for r in rows if r["t"] is not None and t0 <= r["t"] <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "samples_total": len(self.rows)}
         reasons = set()
-        for r in loaded:
+        for r in rows:
             for k, name in (("hw_slow", "hw_slowdown"), ("hw_therm", "hw_thermal_slowdown"),
                             ("sw_therm", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
                 if r[k] == "Active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
-                "sm_max_mhz": max(r["max"] for r in loaded), "reasons": sorted(reasons),
-                "samples": len(loaded)}
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "samples_total": len(self.rows),
+                "power_w_median": statistics.median(r["power"] for r in rows),
+                "window": "samples taken inside the timed replays"}
 
 
 def env_rank():
@@ -260,11 +281,14 @@ def time_steps(prob, steps, warmup, stream, opts=None, unfused=False, barrier=No
     return start.elapsed_time(end) / steps, path
 
 
-def time_steps_graph(prob, steps, warmup, stream, barrier=None, opts=None):
+def time_steps_graph(prob, steps, warmup, stream, barrier=None, opts=None, min_seconds=1.0):
     """The timed steps of the bench line: `warmup` untimed calls on the stream, then the next
     `steps` calls (the same rotation of input sets as the stream loop) captured once in a CUDA
-    graph and replayed once between CUDA events on the launching stream, so that the host's and
-    the driver's per-launch gaps do not sit between the steps.  Every step runs in full."""
+    graph, so that the host's and the driver's per-launch gaps do not sit between the steps.
+    The graph is replayed back to back, each replay between its own pair of CUDA events on the
+    launching stream, until the replays have kept the GPU busy for `min_seconds` (at least 5
+    replays); the time per step is the median replay time / `steps`.  Every step runs in full.
+    Returns (ms per step, path, replays, (t0, t1) wall-clock window of the replays)."""
     import torch
     path = None
     for i in range(warmup):
@@ -276,18 +300,32 @@ def time_steps_graph(prob, steps, warmup, stream, barrier=None, opts=None):
         for i in range(steps):
             path = prob.call(warmup + i, stream.cuda_stream, opts)
     torch.cuda.synchronize()
-    if barrier:
-        barrier()
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):  # replay() launches on the current stream
-        start.record(stream)
+    # one timed replay to size the run
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
         g.replay()
-        end.record(stream)
+        e1.record(stream)
     torch.cuda.synchronize()
+    one = max(e0.elapsed_time(e1) * 1e-3, 1e-6)
+    reps = max(5, min(20000, int(math.ceil(min_seconds / one))))
     if barrier:
         barrier()
-    return start.elapsed_time(end) / steps, path
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps)]
+    t0 = time.time()
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for a, b in ev:
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if barrier:
+        barrier()
+    per = sorted(a.elapsed_time(b) for a, b in ev)
+    return statistics.median(per) / steps, path, reps, (t0, t1)
 
 
 def time_graph(prob, steps, warmup, stream, opts=None, reps=5):
@@ -442,16 +480,22 @@ def run_ours(args):
     time.sleep(0.3 if sampler else 0)
     unfused = args.variant == "unfused"
     opts = json.loads(args.opts) if args.opts else None
+    window = None
     if unfused:  # the library's comparison chain: launched from the stream loop
+        t0 = time.time()
         ms, path = time_steps(prob, args.steps, args.warmup, stream, barrier=barrier, unfused=True)
+        window = (t0, time.time())
         ms_loop = ms
         launch = "stream loop"
     else:
-        ms, path = time_steps_graph(prob, args.steps, args.warmup, stream, barrier=barrier, opts=opts)
+        ms, path, reps, window = time_steps_graph(prob, args.steps, args.warmup, stream,
+                                                  barrier=barrier, opts=opts)
+        launch = (f"CUDA graph of the {args.steps} timed steps, replayed {reps} times back to back "
+                  f"(each replay between its own CUDA events; median replay / steps)")
+    clocks = sampler.stop(window) if sampler else None
+    if not unfused:
         # the same steps launched one by one from the host, for comparison
         ms_loop, _ = time_steps(prob, args.steps, 0, stream, opts=opts, barrier=barrier)
-        launch = "CUDA graph of the timed steps, replayed once"
-    clocks = sampler.stop() if sampler else None
     ms = slowest_rank(dist, ms, dev)
     ms_loop = slowest_rank(dist, ms_loop, dev)
     e2e_ms, h2d, d2h = e2e_steps(prob, max(3, min(args.steps, 20)), stream)
@@ -499,6 +543,8 @@ def run_ours(args):
         "e2e": {"value": w.flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * ((3 if w.epilogue != "gate" else 2) if unfused else 1),
+        "gpu_launches_note": ("launches of the library's kernels per timed pass of K steps "
+                              "(each graph replay repeats that pass)"),
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -518,7 +564,9 @@ def run_reference(args):
     w = gen.WORKLOADS[args.workload]
     x = gen.make(w)
     threads = oracle.default_threads()
-    rows = max(1, min(w.M, 2 * threads))
+    # 64 rows per thread per step: the oracle's per-call set-up (it decodes B once per call) is
+    # then a small part of a step, as in the cpu_baseline leg, which times one larger sample
+    rows = max(1, min(w.M, 64 * threads))
     sel = np.arange(rows, dtype=np.int64)
     epi = oracle.EPI_GATE if w.epilogue == "gate" else oracle.EPI_RELU
 

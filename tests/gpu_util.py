@@ -98,10 +98,45 @@ def check_close(got_bits, res, K, out_type, Y64=None, bias64=None, what=""):
 
 
 def sample_rows(M, BM=128, n_random=64, seed=0):
-    """Rows for full-size parity: first and last rows, every row of the last (ragged) M tile,
-    and a seeded random sample."""
+    """Rows for full-size parity, stratified over the tile grid: in every BM-row M tile one
+    seeded row from each 32-row quarter (each quarter is read out of tensor memory by its own
+    epilogue warp, so every warp of every M tile is sampled), every row of the last (ragged)
+    M tile, the first and last rows, and `n_random` more seeded rows anywhere."""
     rng = np.random.default_rng(seed)
     rows = {0, M - 1}
+    for t0 in range(0, M, BM):
+        for q0 in range(t0, min(t0 + BM, M), 32):
+            rows.add(int(rng.integers(q0, min(q0 + 32, M))))
     rows.update(range(max(0, (M - 1) // BM * BM), M))
     rows.update(int(r) for r in rng.integers(0, M, min(n_random, M)))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+NAN_BITS = {F16: 0x7FFF, BF16: 0x7FFF, F32: 0x7FFFFFFF, E4M3: 0x7F}
+GUARD = 4096
+
+
+def guarded_out(M, N, t, dev="cuda"):
+    """An M x N output tensor of type t inside a buffer of raw words pre-filled with a NaN bit
+    pattern, with GUARD elements of that pattern on both sides.  Returns (out, buf)."""
+    import torch
+    word = {F16: torch.int16, BF16: torch.int16, F32: torch.int32, E4M3: torch.uint8}[t]
+    buf = torch.full((GUARD + M * N + GUARD,), NAN_BITS[t], dtype=word, device=dev)
+    inner = buf[GUARD:GUARD + M * N]
+    out = inner if t == E4M3 else inner.view(torch_dtype(t))
+    return out.view(M, N), buf
+
+
+def check_guarded(buf, M, N, t, what=""):
+    """Every element of out written (no NaN pattern left: the outputs here are finite) and
+    nothing written outside it (the guard words keep their bits)."""
+    import torch
+    b = buf.cpu()
+    for g in (b[:GUARD], b[GUARD + M * N:]):
+        assert bool((g == NAN_BITS[t]).all()), f"{what}: a guard element was written"
+    inner = b[GUARD:GUARD + M * N]
+    if t == E4M3:
+        nan = (inner & 0x7F) == 0x7F
+    else:
+        nan = torch.isnan(inner.view(torch_dtype(t)))
+    assert not bool(nan.any()), f"{what}: {int(nan.sum())} output elements never written"

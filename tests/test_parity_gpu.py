@@ -6,7 +6,8 @@ import pytest
 import oracle
 from conftest import parse_matrix, read_golden
 from gemm_epilogue_gb300 import inputs as gen
-from gpu_util import (BF16, E4M3, F16, F32, check_close, down, dtype_word, sample_rows, up)
+from gpu_util import (BF16, E4M3, F16, F32, check_close, check_guarded, down, dtype_word,
+                      guarded_out, sample_rows, up)
 
 pytestmark = pytest.mark.gpu
 
@@ -684,27 +685,129 @@ def test_unfused_chain_matches_oracle(inter_f32, gate):
 FULL = ["square_4096", "glu_gate_1024x21568x4096", "ffn_up_8192x14336x4096", "ffn_up_fp8_8192x14336x4096",
         "square_fp8_4096", "skinny_M1_8192",
         "skinny_M16_8192", "skinny_M64_8192", "skinny_M128_8192", "glu_gate_1024x21568x256",
-        "glu_gate_1024x21568x512", "glu_gate_1024x21568x1024"]
+        "glu_gate_1024x21568x512", "glu_gate_1024x21568x1024", "ragged_200x136x72"]
+
+_made = {}
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_workloads_sampled_rows(name):
-    w = gen.WORKLOADS[name]
-    x = gen.make(w)
+def made(name):
+    """The workload's seeded inputs, drawn once per test session (the last one kept)."""
+    if name not in _made:
+        _made.clear()
+        _made[name] = gen.make(gen.WORKLOADS[name])
+    return _made[name]
+
+
+def launch_opts(dev_in, w, launch):
+    """Options of the launch under test: `bench` is the launch bench.py times (library defaults,
+    which cut the tiles of the persistent grid's last partial round into column pieces);
+    `whole_tiles` keeps those tiles whole.  None when `whole_tiles` is the same launch."""
+    if launch == "bench":
+        return {}
+    A, B, bias, Y, out = dev_in
+    plan = fg.fgemm_plan(A, B, bias, Y, out, w.M, w.N, w.K,
+                         dtype_word(w.ab_type, w.bias_type, w.out_type), gate=Y is not None)
+    if plan["path"] != fg.PATH_TC or plan["tail_split"] == 1:
+        return None
+    return {"tail_split": 1}
+
+
+_oracle_rows = {}
+
+
+def oracle_rows(name, x, w, rows):
+    key = (name, tuple(rows[:4]), len(rows))
+    if key not in _oracle_rows:
+        _oracle_rows.clear()
+        _oracle_rows[key] = oracle_run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type,
+                                       gate=w.epilogue == "gate", rows=rows)
+    return _oracle_rows[key]
+
+
+FULL_CASES = [(n, launch) for n in FULL for launch in ("bench", "whole_tiles")]
+
+
+def run_full(x, w, launch, what):
+    """One full-size launch into a NaN-prefilled output with guard bands; checks that every
+    element was written and nothing outside it.  Returns the output, or None when the launch is
+    the same as `bench`."""
     gate = w.epilogue == "gate"
-    out, path = run_fused(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, gate=gate)
+    out, buf = guarded_out(w.M, w.N, w.out_type)
+    dev_in = (up(x.A, w.ab_type), up(x.B, w.ab_type), up(x.bias, w.bias_type),
+              up(x.Y, w.ab_type) if gate else None, out)
+    opts = launch_opts(dev_in, w, launch)
+    if opts is None:
+        return None
+    A, B, bias, Y, _ = dev_in
+    word = dtype_word(w.ab_type, w.bias_type, w.out_type)
+    if gate:
+        fg.fgemm_addmm_gate_ex(A, B, bias, Y, out, w.M, w.N, w.K, word, opts=opts or None)
+    else:
+        fg.fgemm_bias_relu_ex(A, B, bias, out, w.M, w.N, w.K, word, opts=opts or None)
+    torch.cuda.synchronize()
+    check_guarded(buf, w.M, w.N, w.out_type, what=what)
+    return out
+
+
+@pytest.mark.parametrize("name,launch", FULL_CASES)
+def test_full_size_workloads(name, launch):
+    """Every configuration at its full size.  `bench`: the launch bench.py times; `whole_tiles`:
+    the tiles of the persistent grid's last partial round kept whole instead of cut into column
+    pieces (skipped where that is the same launch).  Every output element must be written and
+    nothing outside the output (NaN-prefilled buffer with guard bands), and a stratified row
+    sample (every epilogue warp's rows of every M tile, the ragged last tile) must match the
+    oracle within the stated tolerance and the per-element forward-error bound."""
+    w = gen.WORKLOADS[name]
+    x = made(name)
+    gate = w.epilogue == "gate"
+    out = run_full(x, w, launch, f"{name}/{launch}")
+    if out is None:
+        pytest.skip("the tail round is not cut on this shape: the same launch as `bench`")
     rows = sample_rows(w.M)
-    ref = oracle_run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, gate=gate, rows=rows)
+    ref = oracle_rows(name, x, w, rows)
     got = down(out, w.out_type)[rows]
     Y64 = oracle.decode(x.Y[rows], w.ab_type) if gate else None
     b64 = oracle.decode(x.bias, w.bias_type)
-    check_close(got, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what=name)
-    # negative control: an output that left out the GEMM term must fail the per-element bound
-    fake = oracle.gemm_epilogue(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type,
-                                w.out_type, oracle.EPI_GATE if gate else oracle.EPI_RELU,
-                                Y=x.Y, rows=rows, mutant=oracle.MUT_DROP_GEMM)
-    with pytest.raises(AssertionError):
-        check_close(fake.out, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what="bias-only control")
+    check_close(got, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what=f"{name}/{launch}")
+    if launch == "bench":
+        # negative control: an output that left out the GEMM term must fail the per-element bound
+        fake = oracle.gemm_epilogue(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type,
+                                    w.out_type, oracle.EPI_GATE if gate else oracle.EPI_RELU,
+                                    Y=x.Y, rows=rows, mutant=oracle.MUT_DROP_GEMM)
+        with pytest.raises(AssertionError):
+            check_close(fake.out, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what="bias-only control")
+
+
+@pytest.mark.parametrize("name,launch", [("square_4096", "bench"), ("square_4096", "whole_tiles"),
+                                         ("glu_gate_1024x21568x4096", "bench"),
+                                         ("glu_gate_1024x21568x4096", "whole_tiles")])
+def test_full_size_integer_every_element_bit_exact(name, launch):
+    """The two gated configurations at full size on small-integer inputs (every partial sum exact
+    in fp32, so the one rounding is the final one): every element of the output equals the oracle
+    bit for bit, which shows every output tile written exactly once with its own tile's value, in
+    the launch bench.py times and with whole tail tiles.  The gate takes values in [-1, 1] so
+    that X + X * Y stays finite in fp16."""
+    w = gen.WORKLOADS[name]
+    gate = w.epilogue == "gate"
+    lo, hi = (-1, 1) if gate else (-3, 3)
+    key = ("int", name)
+    if key not in _made:
+        _made.clear()
+        _made[key] = gen.integer_problem(w.M, w.N, w.K, w.ab_type, w.bias_type, seed=w.seed,
+                                         lo=lo, hi=hi, gate=gate)
+    x = _made[key]
+    out = run_full(x, w, launch, f"{name}/{launch}")
+    assert out is not None
+    rkey = ("int-oracle", name)
+    if rkey not in _oracle_rows:
+        _oracle_rows.clear()
+        _oracle_rows[rkey] = oracle_run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type,
+                                        gate=gate)
+    want = _oracle_rows[rkey].out
+    got = down(out, w.out_type)
+    if not np.array_equal(got, want):
+        bad = np.argwhere(got != want)
+        pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
 
 
 def test_plan_matches_the_path_that_runs():
