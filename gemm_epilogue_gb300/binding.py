@@ -47,7 +47,7 @@ class Opts(ctypes.Structure):
                 ("skinny_tiles", ctypes.c_int), ("stages", ctypes.c_int),
                 ("inject_stall", ctypes.c_int), ("bias_init", ctypes.c_int),
                 ("full_last_n", ctypes.c_int), ("y_blocks", ctypes.c_int),
-                ("k_rows", ctypes.c_int), ("reserved", ctypes.c_int)]
+                ("k_rows", ctypes.c_int), ("bias_mma", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -55,7 +55,8 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("grid", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("tiles", ctypes.c_int), ("work_items", ctypes.c_int), ("tail_split", ctypes.c_int),
                 ("resident_pairs", ctypes.c_int), ("last_tile_n", ctypes.c_int),
-                ("y_blocks", ctypes.c_int), ("k_rows", ctypes.c_int), ("row_barriers", ctypes.c_int)]
+                ("y_blocks", ctypes.c_int), ("k_rows", ctypes.c_int), ("row_barriers", ctypes.c_int),
+                ("bias_init", ctypes.c_int)]
 
 
 _lock = threading.Lock()

@@ -174,7 +174,7 @@ int validate(const Call& c, bool* nothing) {
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
         o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 2 ||
         o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 3 ||
-        o.k_rows < 0 || o.k_rows > 2)
+        o.k_rows < 0 || o.k_rows > 2 || o.bias_mma < 0 || o.bias_mma > 2)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -199,6 +199,8 @@ struct TcPlan {
   int y_blocks;          // staged Y blocks per epilogue warp (gate / residual, 16-bit out)
   int k_rows;            // 128-byte K rows per ring stage
   bool row_bars;         // a full barrier per K row of a stage
+  bool bias_init;        // the accumulator starts at the bias
+  bool bias_mma;         // ... set by an extra MMA from the staged bias row
 };
 
 // What the planners need to know about the device: its SM count and how many CTA pairs of the
@@ -290,6 +292,22 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
   // Each K row of a two-row stage on its own full barrier: measured faster with fp8 operands and
   // with staged Y, slower on the plain 16-bit FFN shape, equal on 4096^3.
   t.row_bars = t.k_rows > 1 && (c.t.ab == ELEM_E4M3 || staged_y);
+  // Bias-initialised accumulator: on by default for short K loops (K <= 1024), where the epilogue
+  // sets the pace and moving the bias out of it pays (GLU block, M = 1024, N = 21568: K = 256
+  // 27.2 vs 28.3 us, K = 1024 44.6 vs 45.1 us); with long K loops the bias write lengthens the
+  // accumulator hand-off instead (4096^3: 90.3 vs 88.1 us).
+  const int bi = c.opts ? c.opts->bias_init : 0;
+  t.bias_init = c.epi != EPI_NONE && (bi == 1 || (bi == 0 && c.K <= 1024));
+  // Set by one extra MMA (ones x the staged bias row) instead of by the epilogue warps, where the
+  // bias has the 16-bit operand type and the kernel instance has shared memory for the two small
+  // tiles it needs (staged second operand; single CTAs, or CTA pairs with one-row stages, where
+  // the tiles cost a ring stage).  Automatic for single CTAs with K <= 256 only: measured on the
+  // GLU block (M = 1024, N = 21568), alternating on one GB300, K = 256 26.3 vs 26.9 us; K = 512
+  // 37.8 vs 35.9 us; CTA pairs at K = 1024 48.9 vs 44.1 us.
+  const int bm = c.opts ? c.opts->bias_mma : 0;
+  t.bias_mma = t.bias_init && staged_y && c.t.bias == c.t.ab && c.t.ab != ELEM_F32 &&
+               (!t.pair || (t.y_blocks == 1 && t.k_rows == 1)) &&
+               (bm == 2 || (bm == 0 && !t.pair && c.K <= 256));
   return t;
 }
 
@@ -350,6 +368,8 @@ int run_tc(const Call& c, DeviceInfo* d) {
   } else {
     tmY = tmO;  // unused
   }
+  CUtensorMap tmBias = tmO;  // unused unless the bias MMA runs
+  if (t.bias_mma && !encode_2d(&tmBias, c.t.bias, c.bias, 1, c.N, 1, 64)) return FGEMM_ERR_LAUNCH;
   TcParams p{};
   p.M = static_cast<int>(c.M);
   p.N = static_cast<int>(c.N);
@@ -362,12 +382,8 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.num_items = t.num_items;
   p.last_width = t.last_width;
   p.gran = t.gran;
-  // Bias-initialised accumulator: on by default for short K loops (K <= 1024), where the epilogue
-  // sets the pace and moving the bias out of it pays (GLU block, M = 1024, N = 21568: K = 256
-  // 27.2 vs 28.3 us, K = 1024 44.6 vs 45.1 us); with long K loops the bias write lengthens the
-  // accumulator hand-off instead (4096^3: 90.3 vs 88.1 us).
-  const int bi = c.opts ? c.opts->bias_init : 0;
-  p.bias_init = (c.epi != EPI_NONE && (bi == 1 || (bi == 0 && c.K <= 1024))) ? 1 : 0;
+  p.bias_init = t.bias_init ? 1 : 0;
+  p.bias_mma = t.bias_mma ? 1 : 0;
   p.y_blocks = t.y_blocks;
   p.k_rows = t.k_rows;
   p.row_bars = t.row_bars ? 1 : 0;
@@ -387,7 +403,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.err = d->err;
   p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
   return status_of(
-      launch_tc(c.epi, tmA, tmB, tmO, tmY, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
+      launch_tc(c.epi, tmA, tmB, tmO, tmY, tmBias, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
 }
 
 int run_skinny(const Call& c, DeviceInfo* d) {
@@ -696,6 +712,7 @@ int plan_info(const void* A, const void* B, const void* bias, const void* Y, con
     info->k_rows = t.k_rows;
     info->resident_pairs = t.resident;
     info->row_barriers = t.row_bars ? 1 : 0;
+    info->bias_init = t.bias_init ? (t.bias_mma ? 2 : 1) : 0;
   } else if (path == FGEMM_PATH_SKINNY) {
     const SkPlan s = plan_skinny(c, dev);
     info->cluster = s.split;

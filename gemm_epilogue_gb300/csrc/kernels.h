@@ -26,7 +26,9 @@ struct TcParams {
   // to `gran`, the smallest width one CTA (pair) can stage and store); pieces of it that start at
   // or past that width are `gran` wide and store nothing.
   int last_width, gran;
-  int bias_init;   // 1: the accumulator starts at the bias (written into TMEM before the K loop)
+  int bias_init;   // 1: the accumulator starts at the bias
+  int bias_mma;    // with bias_init: 1 = set by an extra MMA from the staged bias row (16-bit bias of
+                   // the operand type, instances with room for it), 0 = written into TMEM
   int y_blocks;    // gate / residual with 16-bit out on CTA pairs: Y blocks per epilogue warp (1, 2)
   int k_rows;      // CTA pairs: 128-byte K rows per ring stage (1, 2)
   int row_bars;    // k_rows 2: a full barrier per K row of a stage (B copied one K row at a time)
@@ -59,9 +61,11 @@ struct SimtParams {
 
 // pair = true: 2-CTA clusters (grid even), 256 x 256 tiles, tiles_m counted in 256-row tiles.
 // tmY: the gate's Y (M x N, operand type, 32 x 64 boxes, 128-byte swizzle); any map otherwise.
+// tmBias: the bias as a 1 x N tensor (64-column boxes, 128-byte swizzle) for the bias MMA; any
+// map otherwise.
 cudaError_t launch_tc(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                      const CUtensorMap& tmOut, const CUtensorMap& tmY, const TcParams& p,
-                      int grid, bool pair, cudaStream_t s);
+                      const CUtensorMap& tmOut, const CUtensorMap& tmY, const CUtensorMap& tmBias,
+                      const TcParams& p, int grid, bool pair, cudaStream_t s);
 // How many CTA pairs of the pair-mode kernel can be resident at once (clusters need two free SMs
 // in one GPC); cached per process.
 int tc_max_active_pairs(int epi, int out_type);

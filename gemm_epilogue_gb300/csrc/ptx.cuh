@@ -242,6 +242,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// Shared-memory matrix descriptor for a tile without swizzle, made of 8-row x 16-byte core
+// matrices (each 128 contiguous bytes): lbo = byte distance between core matrices adjacent along
+// K, sbo = byte distance between core matrices adjacent along M / N (layout field 0).
+__device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
 // Instruction descriptor, kind::f16 (or kind::f8f6f4) with fp32 accumulator.
 //   bits 4-5 D type (1 = f32)   bits 7-9 A type, 10-12 B type (kind::f16: 0 = f16, 1 = bf16;
 //   kind::f8f6f4: 0 = e4m3, 1 = e5m2 -- so an e4m3 descriptor is the f16 one with bf16 = false)

@@ -67,7 +67,14 @@ constexpr int MAX_STAGES = 6;
 // so two K rows halve the number of stage hand-offs (TMA completion -> MMA -> release -> reload)
 // per byte, at the price of half as many, twice as large stages in the same shared memory.
 // The ring takes whatever the epilogue's buffers leave, up to MAX_STAGES stages.
-template <bool PAIR, bool YS = false, int YB = 1, int KSUB = 1>
+// MB: room for the bias-initialised accumulator set by one extra MMA ("Optimizing GEMM +
+// Activation on CDNA4 with TLX", V4: the accumulator starts at the bias): a 128 x 16 tile of ones
+// (A, K-major, no swizzle) and a 16-row tile of B whose first K row is the bias of the work item's
+// columns and whose other rows are zero (B's own MN-major, 128-byte-swizzled layout, 16 K rows per
+// 64-column box).  ones x that tile = the bias in every row, exactly (16-bit bias, products by 1).
+constexpr uint32_t ONES_BYTES = 4096;             // 128 rows x 16 K of 16-bit ones
+constexpr uint32_t BIAS_BOX_BYTES = 16 * 128;     // 16 K rows x 64 columns of 16-bit values
+template <bool PAIR, bool YS = false, int YB = 1, int KSUB = 1, bool MB = false>
 struct Cfg {
   static_assert(YB == 1 || ((YB == 2 || YB == 0) && PAIR && YS), "Y staging variants: staged Y on CTA pairs");
   static_assert(KSUB == 1 || KSUB == 2, "one or two K rows per stage");
@@ -79,7 +86,9 @@ struct Cfg {
   static constexpr uint32_t Y_BLOCK_BYTES = 2 * EPI_BUF_BYTES;  // a warp's 32 x 128 block of Y
   // YB = 0 (staged Y): one 32 x 64 chunk of Y at a time per warp
   static constexpr uint32_t EPI_WARP_BYTES = YS ? (YB == 0 ? EPI_BUF_BYTES : YB * Y_BLOCK_BYTES) : EPI_BUF_BYTES;
-  static constexpr uint32_t RING_BUDGET = SMEM_LIMIT - 512 - 1024 - EPI_WARPS * EPI_WARP_BYTES;
+  static constexpr uint32_t MB_BYTES = MB ? ONES_BYTES + (PAIR ? 2u : 4u) * BIAS_BOX_BYTES : 0u;
+  static constexpr uint32_t RING_BUDGET =
+      SMEM_LIMIT - 512 - 1024 - EPI_WARPS * EPI_WARP_BYTES - MB_BYTES;
   static constexpr int STAGES =
       RING_BUDGET / STAGE_BYTES > MAX_STAGES ? MAX_STAGES : static_cast<int>(RING_BUDGET / STAGE_BYTES);
   static_assert(STAGES >= 2, "at least two stages in the ring");
@@ -87,7 +96,8 @@ struct Cfg {
   static constexpr uint32_t SMEM_A = 0;
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE_BYTES;
   static constexpr uint32_t SMEM_EPI = SMEM_B + STAGES * B_STAGE_BYTES;
-  static constexpr uint32_t SMEM_BAR = SMEM_EPI + EPI_WARPS * EPI_WARP_BYTES;
+  static constexpr uint32_t SMEM_MB = SMEM_EPI + EPI_WARPS * EPI_WARP_BYTES;  // ones, then bias
+  static constexpr uint32_t SMEM_BAR = SMEM_MB + MB_BYTES;
   static constexpr uint32_t SMEM_BYTES = SMEM_BAR + 512 + 1024;  // + barriers + 1024-B alignment slack
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
 };
@@ -100,8 +110,11 @@ constexpr int BAR_ACC_FULL = 2 * MAX_STAGES;
 constexpr int BAR_ACC_EMPTY = 2 * MAX_STAGES + 2;
 constexpr int BAR_MMA_DONE = 2 * MAX_STAGES + 4;
 constexpr int BAR_Y = 2 * MAX_STAGES + 5;  // one per epilogue warp and Y block (staged Y)
-constexpr uint32_t OFF_TMEM_SLOT = 272;  // after the 33 barriers
-constexpr uint32_t OFF_ABORT = 280;
+constexpr int BAR_BIAS_FULL = 2 * MAX_STAGES + 5 + 2 * 8;  // the staged bias row landed (MB)
+constexpr int BAR_BIAS_EMPTY = BAR_BIAS_FULL + 1;          // the bias MMA has read it
+constexpr uint32_t OFF_TMEM_SLOT = 8 * (BAR_BIAS_EMPTY + 1);
+constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 8;
+static_assert(OFF_ABORT + 4 <= 512, "barrier area");
 
 // wait sites recorded with a timeout
 enum { SITE_PROD_EMPTY = 1, SITE_MMA_ACC_EMPTY, SITE_MMA_FULL, SITE_EPI_ACC_FULL, SITE_DRAIN,
@@ -165,17 +178,19 @@ __device__ __forceinline__ void bias_granule(const float (&b)[4], int j0, float 
   for (int e = 0; e < G; ++e) out[e] = __shfl_sync(0xffffffffu, b[e & 3], (j0 >> 2) + (e >> 2));
 }
 
-template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1>
+template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1,
+          bool MB = false>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmY,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmBias, const TcParams p) {
   constexpr int CH = 128 / OUT_BYTES;  // output columns per 128-byte staging row
   constexpr int G = 16 / OUT_BYTES;    // columns per 16-byte granule
   constexpr int NG = CH / G;           // granules per chunk (8)
   // the gate's Y and the residual R are staged the same way (16-bit outputs)
   constexpr bool YS = (EPI == EPI_GATE || EPI == EPI_RESID) && (OUT_BYTES == 2);
-  using C = Cfg<PAIR, YS, YB, KSUB>;
+  using C = Cfg<PAIR, YS, YB, KSUB, MB>;
+  static_assert(!MB || !F8, "the bias MMA is a kind::f16 MMA");
   // Operand element size: one K row of a stage is one 128-byte swizzle row per A row (64 16-bit or
   // 128 fp8 elements); A arrives as KSUB boxes of 128 rows x one K row, B as boxes of (128 bytes
   // of N) x (KSUB K rows); the stage byte counts and the ring are the same for both types.
@@ -202,6 +217,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int CG = PAIR ? 2 : 1;
   constexpr uint32_t SMEM_A = C::SMEM_A, SMEM_B = C::SMEM_B, SMEM_EPI = C::SMEM_EPI,
                      SMEM_BAR = C::SMEM_BAR;
+  constexpr uint32_t SMEM_ONES = C::SMEM_MB, SMEM_BIAS = C::SMEM_MB + ONES_BYTES;
+  // the bias-initialised accumulator: set by the extra MMA (MB) or written by the epilogue
+  const bool bias_mma = MB && p.bias_init;
+  const bool bias_tmem = p.bias_init && !bias_mma;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -232,6 +251,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(bar(BAR_MMA_DONE), 1);
     for (int w = 0; w < (YB == 0 ? 1 : YB) * EPI_WARPS; ++w) mbar_init(bar(BAR_Y + w), 1);
+    if (MB) {
+      mbar_init(bar(BAR_BIAS_FULL), 1);
+      mbar_init(bar(BAR_BIAS_EMPTY), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -244,6 +267,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 1) {
     tmem_alloc_cg<CG>(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish_cg<CG>();
+  }
+  if constexpr (MB) {
+    // the ones tile (every 16-bit element 1.0) and the bias tile's zero rows, written once; the
+    // bias row of each work item is then copied over the first K row of each box by TMA
+    if (warp >= 2) {
+      const uint32_t one = p.ab_bf16 ? 0x3F803F80u : 0x3C003C00u;
+      uint32_t* w = reinterpret_cast<uint32_t*>(smem + SMEM_ONES);
+      for (int i = static_cast<int>(threadIdx.x) - 64; i < static_cast<int>(C::MB_BYTES / 4);
+           i += 32 * EPI_WARPS)
+        w[i] = i < static_cast<int>(ONES_BYTES / 4) ? one : 0u;
+      fence_proxy_async_smem();  // generic-proxy writes, read by the MMA (async proxy)
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -264,6 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol_b = policy_evict_first();
       uint32_t stage = 0, phase = 0;
       uint32_t issued = 0, issued_parity = 0;
+      uint32_t bias_items = 0;  // bias rows copied (bias MMA)
       bool ok = true;
       for (int t = unit; ok && t < p.num_items; t += units) {
         const Work wk = work_of(p, t);
@@ -272,6 +308,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int cols = PAIR ? wk.width / 2 : wk.width;
         const int nb0 = wk.col0 + static_cast<int>(rank) * cols;
         const int boxes = (cols + BOXC - 1) / BOXC;
+        // This work item's bias row (bias MMA), once the previous item's bias MMA has read the
+        // tile: one 128-byte row per 64-column box, zero-filled past N (the bias mask).  Copied
+        // after the item's first stage: by then the MMA warp has begun the previous item (its
+        // stages are being consumed), so its bias MMA has been issued and the wait is short,
+        // while the producer itself never waits here ahead of the ring.
+        auto load_bias = [&]() -> bool {
+          if (!mbar_wait(bar(BAR_BIAS_EMPTY), (bias_items & 1u) ^ 1u, abort_flag, tmo, p.err,
+                         SITE_PROD_EMPTY))
+            return false;
+          const uint32_t bfull = lead_bar(BAR_BIAS_FULL);
+          if (leader)
+            mbar_arrive_expect_tx(bar(BAR_BIAS_FULL),
+                                  (PAIR ? 2u : 1u) * static_cast<uint32_t>(boxes) * 128u);
+          for (int c = 0; c < boxes; ++c) {
+            const uint32_t dst = sbase + SMEM_BIAS + static_cast<uint32_t>(c) * BIAS_BOX_BYTES;
+            if constexpr (PAIR)
+              tma_load_2d_pair(dst, &tmBias, bfull, nb0 + BOXC * c, 0, pol_a);
+            else
+              tma_load_2d(dst, &tmBias, bfull, nb0 + BOXC * c, 0, pol_a);
+          }
+          ++bias_items;
+          return true;
+        };
         // bytes per full barrier: one K row, or the whole stage (both CTAs of a pair)
         const uint32_t tx = (PAIR ? 2u : 1u) * (A_ROW_BYTES + static_cast<uint32_t>(boxes) * BBOX_ROW) *
                             static_cast<uint32_t>(KSUB / nfb);
@@ -315,16 +374,23 @@ __global__ void __launch_bounds__(THREADS, 1)
             stage = 0;
             phase ^= 1u;
           }
+          if (MB && bias_mma && kb == 0 && !load_bias()) {
+            ok = false;
+            break;
+          }
         }
+        if (MB && bias_mma && num_kb == 0 && ok && !load_bias()) ok = false;
       }
       // Every load issued must land before the CTA may exit (also after an abort).  In a pair the
       // even CTA's full barriers count the peer's bytes too; the closing cluster barrier keeps the
       // peer resident until then.
-      if (leader)
+      if (leader) {
         for (int s = 0; s < STAGES; ++s)
           if ((issued >> s) & 1u)
             for (int f = 0; f < nfb; ++f)
               drain_wait(bar(BAR_FULL + s * KSUB + f), (issued_parity >> s) & 1u, tmo, p.err);
+        if (MB && bias_items > 0) drain_wait(bar(BAR_BIAS_FULL), (bias_items - 1u) & 1u, tmo, p.err);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -339,13 +405,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(width >> 3) << 17);
         const int b = it & 1;
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
-        // Buffer b is free once the epilogue has read its previous tile; with the bias-initialised
-        // accumulator the epilogue has also written this tile's bias row into it (one more phase).
-        const uint32_t want = p.bias_init ? acc_phase : (acc_phase ^ 1u);
+        // Buffer b is free once the epilogue has read its previous tile; with the bias written by
+        // the epilogue, the epilogue has also written this tile's bias row into it (one more phase).
+        const uint32_t want = bias_tmem ? acc_phase : (acc_phase ^ 1u);
         if (!mbar_wait(bar(BAR_ACC_EMPTY + b), want, abort_flag, tmo, p.err, SITE_MMA_ACC_EMPTY))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * BN);
+        if (MB && bias_mma) {
+          // D = ones (128 x 16) x [bias row; 15 zero rows]: every row of the accumulator starts at
+          // the bias of its column; the K loop then accumulates onto it
+          if (!mbar_wait(bar(BAR_BIAS_FULL), static_cast<uint32_t>(it) & 1u, abort_flag, tmo, p.err,
+                         SITE_MMA_FULL))
+            break;
+          tc_fence_after();
+          // ones: K-major without swizzle, 8-row x 16-byte core matrices, 128 B apart along K and
+          // 256 B apart along M (the whole 4 KB tile is ones, so only the extent matters)
+          const uint64_t ad = sdesc_none(sbase + SMEM_ONES, 128u, 256u);
+          const uint64_t bd = sdesc_sw128(sbase + SMEM_BIAS, BIAS_BOX_BYTES, 1024u);
+          umma_f16_cg<CG>(d_tmem, ad, bd, idesc, 0u);
+          umma_commit_cg<CG>(bar(BAR_BIAS_EMPTY), kPair);  // bias tile free (both CTAs) once read
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           const uint32_t a_addr = sbase + SMEM_A + stage * A_STAGE_BYTES;
           const uint32_t b_addr = sbase + SMEM_B + stage * C::B_STAGE_BYTES;
@@ -365,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                   sdesc_sw128(a_addr + (k / KPR) * A_ROW_BYTES + 32u * (k % KPR), 16u, 1024u);
               // MN-major B: one column box (BBOX bytes) apart along N, 1 KB per 8 K rows
               const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, BBOX, 1024u);
-              const uint32_t acc = (p.bias_init | kb | k) != 0 ? 1u : 0u;
+              const uint32_t acc = (p.bias_init | kb | k) != 0 ? 1u : 0u;  // bias: already in D
               if constexpr (F8)
                 umma_f8_cg<CG>(d_tmem, ad, bd, idesc, acc);
               else
@@ -401,7 +481,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // (row) of its quarter and every column of its half of buffer bb for work item t, then hands
     // the buffer to the MMA warp, whose first MMA of the tile accumulates onto it.
     auto release_acc = [&](int t, int bb) {
-      if (p.bias_init && t < p.num_items) {
+      if (bias_tmem && t < p.num_items) {
         const Work w = work_of(p, t);
         const uint32_t ta =
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(bb * BN);
@@ -428,7 +508,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive(bar(BAR_ACC_EMPTY + bb));
       }
     };
-    if (p.bias_init) {  // first use of both buffers
+    if (bias_tmem) {  // first use of both buffers
       release_acc(unit, 0);
       release_acc(unit + units, 1);
     }
@@ -783,12 +863,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1>
+template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1,
+          bool MB = false>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                       const CUtensorMap& y, const TcParams& p, int grid, cudaStream_t s) {
-  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB, KSUB>;
+                       const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p, int grid,
+                       cudaStream_t s) {
+  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB, KSUB, MB>;
   constexpr uint32_t smem =
-      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB, KSUB>::SMEM_BYTES;
+      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB, KSUB, MB>::SMEM_BYTES;
   // Per device: the shared-memory opt-in is set once.  Host threads may race on a first call;
   // setting the attribute twice is harmless, and the flag is atomic.
   static std::atomic<bool> opted_in[64] = {};
@@ -811,7 +893,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, o, y, p);
+  return cudaLaunchKernelEx(&cfg, k, a, b, o, y, bm, p);
 }
 
 // A persistent grid must be co-resident: clusters of two need two free SMs in one GPC, so the
@@ -853,17 +935,21 @@ int max_pairs() {
 
 template <int EPI, int OUT_BYTES, bool F8 = false>
 cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                               const CUtensorMap& y, const TcParams& p, int grid, bool pair,
-                               cudaStream_t s) {
+                               const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p,
+                               int grid, bool pair, cudaStream_t s) {
   if constexpr ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2 && !F8) {
-    if (pair && p.y_blocks == 2) return launch_one<EPI, OUT_BYTES, true, false, 2>(a, b, o, y, p, grid, s);
+    if (pair && p.y_blocks == 2) return launch_one<EPI, OUT_BYTES, true, false, 2>(a, b, o, y, bm, p, grid, s);
     if (pair && p.y_blocks == 0)  // one 4 KB chunk of Y per warp
-      return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, false, 0, 2>(a, b, o, y, p, grid, s)
-                           : launch_one<EPI, OUT_BYTES, true, false, 0, 1>(a, b, o, y, p, grid, s);
+      return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, false, 0, 2>(a, b, o, y, bm, p, grid, s)
+                           : launch_one<EPI, OUT_BYTES, true, false, 0, 1>(a, b, o, y, bm, p, grid, s);
+    // the bias-initialised accumulator set by an extra MMA (room for its tiles in shared memory)
+    if (p.bias_init && p.bias_mma && p.k_rows != 2)
+      return pair ? launch_one<EPI, OUT_BYTES, true, false, 1, 1, true>(a, b, o, y, bm, p, grid, s)
+                  : launch_one<EPI, OUT_BYTES, false, false, 1, 1, true>(a, b, o, y, bm, p, grid, s);
   }
-  if (pair && p.k_rows == 2) return launch_one<EPI, OUT_BYTES, true, F8, 1, 2>(a, b, o, y, p, grid, s);
-  return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, p, grid, s)
-              : launch_one<EPI, OUT_BYTES, false, F8>(a, b, o, y, p, grid, s);
+  if (pair && p.k_rows == 2) return launch_one<EPI, OUT_BYTES, true, F8, 1, 2>(a, b, o, y, bm, p, grid, s);
+  return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, bm, p, grid, s)
+              : launch_one<EPI, OUT_BYTES, false, F8>(a, b, o, y, bm, p, grid, s);
 }
 
 }  // namespace tc
@@ -883,25 +969,25 @@ int tc_block_m() { return tc::BM; }
 int tc_block_n() { return tc::BN; }
 
 cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                      const CUtensorMap& y, const TcParams& p, int grid, bool pair,
-                      cudaStream_t s) {
+                      const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p, int grid,
+                      bool pair, cudaStream_t s) {
   const bool f32 = p.out_type == ELEM_F32;
   if (p.ab_f8) {  // fp8 operands: bias + ReLU (bf16 / fp32 out) and the quantized epilogue
-    if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1, true>(a, b, o, y, p, grid, pair, s);
+    if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1, true>(a, b, o, y, bm, p, grid, pair, s);
     if (epi != EPI_RELU) return cudaErrorNotSupported;
-    return f32 ? tc::launch_pair_or_not<EPI_RELU, 4, true>(a, b, o, y, p, grid, pair, s)
-               : tc::launch_pair_or_not<EPI_RELU, 2, true>(a, b, o, y, p, grid, pair, s);
+    return f32 ? tc::launch_pair_or_not<EPI_RELU, 4, true>(a, b, o, y, bm, p, grid, pair, s)
+               : tc::launch_pair_or_not<EPI_RELU, 2, true>(a, b, o, y, bm, p, grid, pair, s);
   }
-  if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1>(a, b, o, y, p, grid, pair, s);
+  if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1>(a, b, o, y, bm, p, grid, pair, s);
   switch (epi) {
-    case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, y, p, grid, pair, s)
-                              : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, y, p, grid, pair, s);
-    case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4>(a, b, o, y, p, grid, pair, s)
-                              : tc::launch_pair_or_not<EPI_GATE, 2>(a, b, o, y, p, grid, pair, s);
-    case EPI_RESID: return f32 ? tc::launch_pair_or_not<EPI_RESID, 4>(a, b, o, y, p, grid, pair, s)
-                               : tc::launch_pair_or_not<EPI_RESID, 2>(a, b, o, y, p, grid, pair, s);
-    default: return f32 ? tc::launch_pair_or_not<EPI_NONE, 4>(a, b, o, y, p, grid, pair, s)
-                        : tc::launch_pair_or_not<EPI_NONE, 2>(a, b, o, y, p, grid, pair, s);
+    case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, y, bm, p, grid, pair, s)
+                              : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, y, bm, p, grid, pair, s);
+    case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4>(a, b, o, y, bm, p, grid, pair, s)
+                              : tc::launch_pair_or_not<EPI_GATE, 2>(a, b, o, y, bm, p, grid, pair, s);
+    case EPI_RESID: return f32 ? tc::launch_pair_or_not<EPI_RESID, 4>(a, b, o, y, bm, p, grid, pair, s)
+                               : tc::launch_pair_or_not<EPI_RESID, 2>(a, b, o, y, bm, p, grid, pair, s);
+    default: return f32 ? tc::launch_pair_or_not<EPI_NONE, 4>(a, b, o, y, bm, p, grid, pair, s)
+                        : tc::launch_pair_or_not<EPI_NONE, 2>(a, b, o, y, bm, p, grid, pair, s);
   }
 }
 

@@ -129,7 +129,12 @@ typedef struct {
                      elements) per stage of the operand ring; 0 = automatic (2, or 1 for the
                      gate and residual with 16-bit outputs), 1 = six stages of 32 KB per SM,
                      2 = three stages of 64 KB.  Ignored elsewhere. */
-  int reserved;
+  int bias_mma;   /* tensor-core path, bias-initialised accumulator: how the bias gets into it.
+                     1 = written into tensor memory by the epilogue warps; 2 = set by one extra MMA
+                     (a tile of ones times the bias row staged by TMA), where the bias has the
+                     16-bit operand type and the kernel has room for the two small tiles (gate and
+                     residual with 16-bit outputs on single CTAs, or on CTA pairs with one-row
+                     stages), else as 1; 0 = automatic: 2 on single CTAs with K <= 256, else 1 */
 } fgemm_opts;
 
 /*
@@ -253,6 +258,9 @@ typedef struct {
   int k_rows;         /* tensor-core path: 128-byte K rows per ring stage (see fgemm_opts) */
   int row_barriers;   /* tensor-core path, two K rows per stage: 1 = each K row of a stage lands on
                          its own full barrier (fp8 operands and staged second operands) */
+  int bias_init;      /* tensor-core path: 0 = the bias is added after the reduction; 1 = the
+                         accumulator starts at the bias, written by the epilogue warps; 2 = set by
+                         the extra MMA (see fgemm_opts.bias_mma) */
 } fgemm_plan_info;
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
                int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,

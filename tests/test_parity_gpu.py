@@ -7,7 +7,7 @@ import oracle
 from conftest import parse_matrix, read_golden
 from gemm_epilogue_gb300 import inputs as gen
 from gpu_util import (BF16, E4M3, F16, F32, check_close, check_guarded, down, dtype_word,
-                      guarded_out, sample_rows, up)
+                      guarded_out, sample_rows, torch_dtype, up)
 
 pytestmark = pytest.mark.gpu
 
@@ -536,6 +536,44 @@ def test_bias_init_integer_exact(M, N, K, opts):
         torch.cuda.synchronize()
         assert _same_values(down(out, BF16),
                             oracle.bias_relu(p.A, p.B, p.bias, M, N, K, E4M3, F32, BF16).out, BF16)
+
+
+BIAS_MMA_CASES = [  # M, N, K, opts: single CTAs, CTA pairs with one Y block, tail pieces,
+    # the narrowed last tile (N = 1288 = 5 x 256 + 8), one-K-block tiles
+    (300, 520, 200, {"cta_pair": 1}), (700, 1800, 200, {"cta_pair": 1, "max_ctas": 44}),
+    (513, 1288, 328, {"cta_pair": 2, "y_blocks": 1}), (700, 1800, 600, {"cta_pair": 2, "max_ctas": 20}),
+    (129, 264, 8, {"cta_pair": 1}), (1000, 1288, 1024, None)]
+
+
+@pytest.mark.parametrize("M,N,K,opts", BIAS_MMA_CASES)
+def test_bias_mma_integer_exact(M, N, K, opts):
+    # The bias-initialised accumulator set by one extra MMA (ones x the staged bias row) must give
+    # the oracle's values exactly on integer inputs, as the form written by the epilogue does, for
+    # the gate and the residual add with 16-bit bias of the operand type.
+    o = dict(opts or {}, bias_init=1, bias_mma=2, path=fg.PATH_TC)
+    for ab in (F16, BF16):
+        for epi in ("gate", "residual"):
+            p = gen.integer_problem(M, N, K, ab, ab, seed=M + N + K + ab, gate=True)
+            A, B, bias, R = up(p.A, ab), up(p.B, ab), up(p.bias, ab), up(p.Y, ab)
+            word = dtype_word(ab, ab, ab)
+            plan = fg.fgemm_plan(A, B, bias, R, torch.empty(1, device="cuda"), M, N, K, word, opts=o,
+                                 epilogue=fg.EPI_GATE if epi == "gate" else fg.EPI_RESIDUAL_RELU)
+            assert plan["bias_init"] == 2, plan  # the MMA form runs
+            outs = []
+            for form in ({}, {"bias_mma": 1}, {"bias_mma": 0}):
+                out = torch.full((M, N), float("nan"), dtype=torch_dtype(ab), device="cuda")
+                if epi == "gate":
+                    fg.fgemm_addmm_gate_ex(A, B, bias, R, out, M, N, K, word, opts=dict(o, **form))
+                else:
+                    fg.fgemm_bias_residual_relu_ex(A, B, bias, R, out, M, N, K, word, opts=dict(o, **form))
+                torch.cuda.synchronize()
+                outs.append(down(out, ab))
+            if epi == "gate":
+                ref = oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, ab, ab, ab).out
+            else:
+                ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, ab, ab, ab).out
+            for got in outs:
+                assert _same_values(got, ref, ab), (epi, ab)
 
 
 def test_bias_init_default_on_short_k_only():

@@ -59,10 +59,18 @@ def test_gate_glu_block_short_k():
         (1, 152, 680, 2, 752)
     # single CTA: the last column narrowed to 64 (one 64-column box); one K row per stage
     assert (p["last_tile_n"], p["y_blocks"], p["k_rows"], p["row_barriers"]) == (64, 1, 1, 0)
+    # K <= 256 on single CTAs: the bias-initialised accumulator is set by the extra MMA (2)
+    assert p["bias_init"] == 2
+    assert plan(1024, 21568, 256, fg.F16, gate=True, opts={"bias_mma": 1})["bias_init"] == 1
+    assert plan(1024, 21568, 512, fg.F16, gate=True)["bias_init"] == 1
+    assert plan(1024, 21568, 512, fg.F16, gate=True, opts={"bias_mma": 2})["bias_init"] == 2
+    # an fp32 bias cannot be set by a 16-bit MMA: written by the epilogue
+    assert plan(1024, 21568, 256, fg.F16 | fg.BIAS_F32, gate=True, opts={"bias_mma": 2})["bias_init"] == 1
     p = plan(1024, 21568, 1024, fg.F16, gate=True)
     # K = 1024 > 512: pairs again; 256 < K <= 1024: one 8 KB Y block per warp, one K row
     assert (p["cluster"], p["work_items"], p["y_blocks"], p["k_rows"], p["row_barriers"]) == \
         (2, 376, 1, 1, 0)
+    assert p["bias_init"] == 1 and plan(1024, 21568, 4096, fg.F16, gate=True)["bias_init"] == 0
 
 
 def test_fp8_operands():
