@@ -174,7 +174,8 @@ int validate(const Call& c, bool* nothing) {
         o.tail_split < 0 || o.tail_split > 1 || o.skinny_tiles < 0 || o.skinny_tiles > 2 || o.stages < 0 || o.stages > 8 ||
         o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 2 ||
         o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 3 ||
-        o.k_rows < 0 || o.k_rows > 2 || o.bias_mma < 0 || o.bias_mma > 2)
+        o.k_rows < 0 || o.k_rows > 2 || o.bias_mma < 0 || o.bias_mma > 2 || o.pdl < 0 ||
+        o.pdl > 2)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -350,6 +351,18 @@ SkPlan plan_skinny(const Call& c, const DevShape& d) {
   return s;
 }
 
+// Programmatic dependent launch (fgemm_opts.pdl): automatic for the short kernels, where the
+// launch gap and set-up between consecutive kernels (about 1.5 us) is a visible share.  Measured
+// on one GB300, CUDA-graph replay of back-to-back calls: GLU block M = 1024, N = 21568, K = 256 /
+// 512 / 1024: 26.1 -> 25.4, 35.8 -> 34.8, 43.8 -> 41.8 us; skinny N = K = 8192, M = 1 / 128:
+// 24.5 -> 24.0, 29.4 -> 28.6 us.  With long K loops it measured slower (4096^3 80.4 -> 82-84.5 us,
+// GLU block K = 4096 124.5 -> 132 us), so it stays off there.
+int pdl_of(const Call& c, bool skinny) {
+  const int want = c.opts ? c.opts->pdl : 0;
+  if (want != 0) return want == 1 ? 1 : 0;
+  return (skinny || c.K <= 1024) ? 1 : 0;
+}
+
 int run_tc(const Call& c, DeviceInfo* d) {
   const TcPlan t = plan_tc(c, shape_of(d));
   if (t.num_tiles < 0) return FGEMM_ERR_INVALID_VALUE;
@@ -402,6 +415,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
   p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
+  p.pdl = pdl_of(c, false);
   return status_of(
       launch_tc(c.epi, tmA, tmB, tmO, tmY, tmBias, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
 }
@@ -434,6 +448,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
   p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
+  p.pdl = pdl_of(c, true);
   if (!skinny_fits(s.mpad, s.nt, s.split, s.stages)) return FGEMM_ERR_INVALID_VALUE;
   return status_of(launch_skinny(c.epi, tmB, tmA, p, s.groups * s.split, c.stream));
 }

@@ -43,6 +43,7 @@ struct TcParams {
   uint64_t timeout_ns;
   int* err;        // device error word
   int inject_stall;  // diagnostic: CTA 0 skips the loads of its first stage (see fgemm_opts)
+  int pdl;           // launched with programmatic stream serialization (see fgemm_opts)
 };
 
 // Generic CUDA-core kernel and elementwise kernels: plain pointers.
@@ -89,6 +90,7 @@ struct SkParams {
   uint64_t timeout_ns;
   int* err;
   int inject_stall;  // diagnostic: CTA 0 skips the loads of its first stage (see fgemm_opts)
+  int pdl;           // launched with programmatic stream serialization (see fgemm_opts)
 };
 cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA,
                           const SkParams& p, int ctas, cudaStream_t s);

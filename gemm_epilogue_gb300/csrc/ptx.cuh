@@ -306,6 +306,17 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grids this one depends on have completed and their memory operations are
+// visible (returns at once for a launch without programmatic stream serialization), and let the
+// grids launched after this one in the stream begin their set-up before it ends.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t local, uint32_t rank) {
   uint32_t r;

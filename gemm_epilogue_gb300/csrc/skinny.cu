@@ -157,6 +157,9 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Global memory only from here on (with programmatic dependent launch the set-up above
+  // overlaps the previous kernel in the stream).
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -337,6 +340,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
     }
   }
 
+  grid_dependents_launch();  // the next kernel in the stream may begin its set-up
   __syncthreads();
   tc_fence_after();
   if (warp == 1) {
@@ -366,13 +370,15 @@ cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkPar
   cfg.blockDim = dim3(static_cast<unsigned>(64 + 32 * epi_warps_for(p.mpad)));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(p.split);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k, tb, ta, p);
 }
 

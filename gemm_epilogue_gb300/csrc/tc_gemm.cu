@@ -285,6 +285,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (PAIR) cluster_sync();  // the peer signals the even CTA's barriers: both must be initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Up to here only this CTA's shared and tensor memory were touched; with programmatic
+  // dependent launch that set-up overlaps the previous kernel in the stream, and global memory is
+  // touched only after it has completed.
+  grid_dependency_wait();
 
   const int num_kb = (p.K + KB_ELEMS - 1) / KB_ELEMS;
   const uint64_t tmo = p.timeout_ns;
@@ -853,6 +857,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ------------------------------------------------------------ teardown
+  // The next kernel in the stream may begin its set-up (measured: letting it start as soon as
+  // this kernel has begun gains nothing on short K loops and slows the skinny kernel at M = 1).
+  grid_dependents_launch();
   tc_fence_before();
   __syncthreads();
   if (PAIR) cluster_sync();  // the even CTA's MMAs and both epilogues are done with TMEM
@@ -886,13 +893,15 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = PAIR ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = p.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k, a, b, o, y, bm, p);
 }
 

@@ -135,6 +135,12 @@ typedef struct {
                      16-bit operand type and the kernel has room for the two small tiles (gate and
                      residual with 16-bit outputs on single CTAs, or on CTA pairs with one-row
                      stages), else as 1; 0 = automatic: 2 on single CTAs with K <= 256, else 1 */
+  int pdl;        /* tensor-core and skinny paths: launch with programmatic stream serialization:
+                     the kernel's set-up (barriers, tensor memory) may run while the previous
+                     kernel in the stream is finishing, and the kernel waits for that kernel to
+                     complete (griddepcontrol.wait) before its first access to global memory, so a
+                     dependency between the two stays safe.  0 = automatic (on for the skinny path
+                     and for K <= 1024), 1 = on, 2 = off */
 } fgemm_opts;
 
 /*
