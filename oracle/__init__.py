@@ -67,7 +67,7 @@ def _load():
             lib.orc_gemm_epilogue.argtypes = (
                 [ctypes.c_void_p] * 7
                 + [ctypes.c_int64] * 3 + [ctypes.c_void_p, ctypes.c_int64]
-                + [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_int])
+                + [ctypes.c_int] * 6 + [ctypes.c_double, ctypes.c_int])
             lib.orc_encode.restype = None
             lib.orc_encode.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
             lib.orc_decode.restype = None
@@ -126,13 +126,16 @@ class Result:
 
 def gemm_epilogue(A, B, bias, M: int, N: int, K: int, ab_type: int, bias_type: int,
                   out_type: int, epi: int, Y=None, rows=None, threads: int | None = None,
-                  want_ref: bool = True, mutant: int = OK, scale: float = 1.0) -> Result:
-    """Run the oracle on all rows, or on the listed ``rows`` of the M x N output."""
+                  want_ref: bool = True, mutant: int = OK, scale: float = 1.0,
+                  y_type: int | None = None) -> Result:
+    """Run the oracle on all rows, or on the listed ``rows`` of the M x N output.  ``y_type`` is
+    the element type of the gate's Y (or the residual R); by default the operand type."""
+    y_type = ab_type if y_type is None else y_type
     A = _bits(A, ab_type) if K > 0 else (None if A is None else _bits(A, ab_type))
     B = _bits(B, ab_type) if K > 0 else (None if B is None else _bits(B, ab_type))
     bias = _bits(bias, bias_type)
     if epi in (EPI_GATE, EPI_RESIDUAL):
-        Y = _bits(Y, ab_type)
+        Y = _bits(Y, y_type)
     if rows is None:
         nrows, rows_arr = M, None
     else:
@@ -147,7 +150,7 @@ def gemm_epilogue(A, B, bias, M: int, N: int, K: int, ab_type: int, bias_type: i
     used = _load().orc_gemm_epilogue(
         _ptr(A), _ptr(B), _ptr(bias), _ptr(Y if epi in (EPI_GATE, EPI_RESIDUAL) else None),
         _ptr(out), _ptr(ref), _ptr(absdot), M, N, K, _ptr(rows_arr), nrows,
-        ab_type, bias_type, out_type, epi, mutant, float(scale), th)
+        ab_type, bias_type, out_type, y_type, epi, mutant, float(scale), th)
     if used < 0:
         raise ValueError("oracle rejected its arguments")
     return Result(out, ref, absdot, used)

@@ -292,7 +292,7 @@ typedef struct {
     double *absdot;          /* nrows x N, sum_k |A[i,k] B[k,j]|, or NULL */
     const int64_t *rows;     /* row indices into A / Y, or NULL = 0..nrows-1 */
     int64_t N, K;
-    int ab_type, bias_type, out_type, epi, mutant;
+    int ab_type, bias_type, out_type, y_type, epi, mutant;
     double scale;            /* quantized epilogue only */
     int64_t r_begin, r_end;  /* this worker's slice of the row list */
 } work_t;
@@ -326,7 +326,7 @@ static void *row_worker(void *arg)
         for (int64_t j = 0; j < N; ++j) {
             const double b = decode(w->bias, (mut == ORC_MUT_BIAS_ROW) ? i % N : j, w->bias_type);
             const double y = (w->epi == ORC_EPI_GATE || w->epi == ORC_EPI_RESIDUAL)
-                                 ? decode(w->Y, i * N + j, w->ab_type) : 0.0;
+                                 ? decode(w->Y, i * N + j, w->y_type) : 0.0;
             const double v = epilogue(w->epi, (mut == ORC_MUT_BIAS_IN_SUM) ? s[j] - b : s[j], b, y,
                                       mut, w->scale);
             store(w->out, r * N + j, w->out_type, v);
@@ -346,7 +346,7 @@ static void *row_worker(void *arg)
  *   A      M x K row-major (ab_type), may be NULL when K == 0
  *   B      K x N row-major (ab_type), may be NULL when K == 0
  *   bias   N (bias_type)
- *   Y      M x N row-major (ab_type): the gate's Y, or the residual R
+ *   Y      M x N row-major (y_type): the gate's Y, or the residual R
  *   rows   nrows row indices, or NULL for rows 0..nrows-1
  *   out    nrows x N (out_type): the rounded result for each listed row
  *   ref    nrows x N fp64: the value before the final rounding (may be NULL)
@@ -358,8 +358,8 @@ static void *row_worker(void *arg)
 int orc_gemm_epilogue(const void *A, const void *B, const void *bias, const void *Y,
                       void *out, double *ref, double *absdot,
                       int64_t M, int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
-                      int ab_type, int bias_type, int out_type, int epi, int mutant,
-                      double scale, int nthreads)
+                      int ab_type, int bias_type, int out_type, int y_type, int epi,
+                      int mutant, double scale, int nthreads)
 {
     if (M < 0 || N < 0 || K < 0 || nrows < 0 || nthreads < 1)
         return -1;
@@ -377,7 +377,7 @@ int orc_gemm_epilogue(const void *A, const void *B, const void *bias, const void
     work_t *w = (work_t *)malloc(sizeof(work_t) * (size_t)nthreads);
     for (int t = 0; t < nthreads; ++t) {
         w[t] = (work_t){A, bias, Y, Bd, out, ref, absdot, rows, N, K,
-                        ab_type, bias_type, out_type, epi, mutant, scale,
+                        ab_type, bias_type, out_type, y_type, epi, mutant, scale,
                         nrows * t / nthreads, nrows * (t + 1) / nthreads};
         pthread_create(&th[t], NULL, row_worker, &w[t]);
     }

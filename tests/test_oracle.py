@@ -425,6 +425,57 @@ def test_e4m3_operands_transposed_b_is_caught(oracle_mod):
     assert not np.array_equal(r.ref, dec(A) @ dec(B).T)
 
 
+@pytest.mark.parametrize("K", [1, 13, 64])
+@pytest.mark.parametrize("yt", [F16, BF16])
+def test_e4m3_gate_with_16_bit_y(oracle_mod, K, yt):
+    # "Optimizing GEMM + Activation on CDNA4 with TLX", "Future Work" (FP8 precision): the
+    # projection A @ B in fp8 while the gate's Y stays 16-bit.  Y is decoded by its own type: the
+    # result equals torch's float8 decode of A and B, an fp64 matmul (exact here), the bias, and
+    # X + X * Y with Y decoded by numpy / torch; reading Y as the other 16-bit type must differ.
+    M, N = 6, 10
+    rng = np.random.default_rng(500 + K + yt)
+    finite = np.array([p for p in range(256) if p & 0x7F != 0x7F], dtype=np.uint8)
+    A, B = rng.choice(finite, (M, K)), rng.choice(finite, (K, N))
+    bias = rng.standard_normal(N).astype(np.float32)
+    Yf = rng.standard_normal((M, N)).astype(np.float32)
+    if yt == F16:
+        Y = Yf.astype(np.float16).view(np.uint16)
+        Y64 = Y.view(np.float16).astype(np.float64)
+    else:
+        Y = torch.from_numpy(Yf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+        Y64 = torch.from_numpy(Y.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    r = oracle_mod.addmm_gate(A, B, bias, Y, M, N, K, E4M3, F32, F32, y_type=yt)
+    dec = lambda x: torch.from_numpy(x.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    X = dec(A) @ dec(B) + bias.astype(np.float64)[None, :]
+    assert np.array_equal(r.ref, X + X * Y64)
+    other = oracle_mod.addmm_gate(A, B, bias, Y, M, N, K, E4M3, F32, F32,
+                                  y_type=BF16 if yt == F16 else F16)
+    assert not np.array_equal(other.ref, r.ref)
+    # residual with a 16-bit R beside fp8 operands
+    rr = oracle_mod.bias_residual_relu(A, B, bias, Y, M, N, K, E4M3, F32, F32, y_type=yt)
+    assert np.array_equal(rr.ref, np.maximum(X + Y64, 0.0))
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (3, 5, 2), (5, 3, 7), (4, 9, 16)])
+def test_e4m3_gate_brute_force_exact(oracle_mod, M, N, K):
+    # exact rational arithmetic on the decoded values (fp8 operands, 16-bit Y, fp32 bias)
+    rng = np.random.default_rng(600 + M * N * K)
+    finite = np.array([p for p in range(256) if p & 0x7F != 0x7F], dtype=np.uint8)
+    A, B = rng.choice(finite, (M, K)), rng.choice(finite, (K, N))
+    bias = rng.standard_normal(N).astype(np.float32)
+    Y = rng.standard_normal((M, N)).astype(np.float16).view(np.uint16)
+    r = oracle_mod.addmm_gate(A, B, bias, Y, M, N, K, E4M3, F32, F32, y_type=F16)
+    A64, B64 = oracle_mod.decode(A, E4M3), oracle_mod.decode(B, E4M3)
+    b64, Y64 = oracle_mod.decode(bias, F32), oracle_mod.decode(Y, F16)
+    for i, j in itertools.product(range(M), range(N)):
+        e = _exact(A64, B64, b64, i, j, K, "gate", Y64)
+        x = _exact(A64, B64, b64, i, j, K, "linear")
+        # three fp64 roundings at most (the bias add, X * Y, the final add; the products and
+        # their sum are exact): bounded by the magnitudes they act on
+        bound = 4 * 2.0 ** -53 * abs(float(x)) * (1 + abs(Y64[i, j])) + 1e-300
+        assert abs(Fraction(r.ref[i, j]) - e) <= Fraction(bound), (i, j)
+
+
 # --------------------------------------------------------- negative controls --
 
 def _pins_pass(oracle_mod, mutant):
