@@ -216,7 +216,7 @@ class Problem:
             return torch.from_numpy(a.view(np.int16)).view(tdt[t]).to(dev)
 
         A, B = up(x.A, w.ab_type), up(x.B, w.ab_type)
-        bias, Y = up(x.bias, w.bias_type), up(x.Y, w.ab_type)
+        bias, Y = up(x.bias, w.bias_type), up(x.Y, w.y_type)
         set_bytes = A.numel() * A.element_size() + B.numel() * B.element_size()
         set_bytes += w.M * w.N * gen.ELEM_BYTES[w.out_type] * (2 if Y is not None else 1)
         n = max(1, min(max_sets, math.ceil(2 * l2_bytes / max(set_bytes, 1)) + 1))
@@ -239,6 +239,10 @@ class Problem:
             self.word |= fg.OUT_F32
         elif w.out_type == gen.BF16 and w.ab_type != gen.BF16:
             self.word |= fg.OUT_BF16
+        elif w.out_type == gen.F16 and w.ab_type != gen.F16:
+            self.word |= fg.OUT_F16
+        if w.epilogue == "gate" and w.y_type != w.ab_type:
+            self.word |= {gen.F16: fg.Y_F16, gen.BF16: fg.Y_BF16}[w.y_type]
         self.ws = None
         if with_unfused:
             nb = fg.fgemm_unfused_workspace_bytes(w.M, w.N, self.word, 0)
@@ -448,7 +452,7 @@ def cpu_baseline(w, target_s=12.0):
         t0 = time.perf_counter()
         oracle.gemm_epilogue(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type,
                              oracle.EPI_GATE if w.epilogue == "gate" else oracle.EPI_RELU,
-                             Y=x.Y, rows=sel, threads=threads, want_ref=False)
+                             Y=x.Y, rows=sel, threads=threads, want_ref=False, y_type=w.y_type)
         dt = time.perf_counter() - t0
         if dt >= target_s / 4 or rows >= w.M:
             break
@@ -583,7 +587,8 @@ def run_reference(args):
 
     def step():
         oracle.gemm_epilogue(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type,
-                             w.out_type, epi, Y=x.Y, rows=sel, threads=threads, want_ref=False)
+                             w.out_type, epi, Y=x.Y, rows=sel, threads=threads, want_ref=False,
+                             y_type=w.y_type)
 
     for _ in range(args.warmup):
         step()

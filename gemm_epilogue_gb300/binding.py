@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "libfgemm.so")
 # dtype word (include/fgemm.h)
 F16, BF16, E4M3 = 0x1, 0x2, 0x3
 BIAS_SAME, BIAS_F32, BIAS_BF16 = 0x00, 0x10, 0x20
-OUT_SAME, OUT_F32, OUT_E4M3, OUT_BF16 = 0x000, 0x100, 0x200, 0x300
+OUT_SAME, OUT_F32, OUT_E4M3, OUT_BF16, OUT_F16 = 0x000, 0x100, 0x200, 0x300, 0x400
+Y_SAME, Y_F16, Y_BF16 = 0x0000, 0x1000, 0x2000
 
 # status codes
 OK, ERR_INVALID_VALUE, ERR_UNSUPPORTED_DTYPE, ERR_MISALIGNED = 0, 1, 2, 3

@@ -81,18 +81,24 @@ DeviceInfo* current_device() {
 
 struct Types {
   int ab, bias, out;  // Elem codes
+  int y;              // Elem code of the gate's Y / the residual R (the operand type by default)
 };
 
 // fp8_out: the entry produces fp8 e4m3 (FGEMM_OUT_E4M3 required); otherwise it is refused.
 // fp8 operands (FGEMM_E4M3) take an explicit bias type (fp32 / bf16) and output type.
-int parse_dtype(int dtype, Types* t, bool fp8_out = false) {
-  const int ab = dtype & 0xF, bias = dtype & 0xF0, out = dtype & 0xF00;
-  if ((dtype & ~0xFFF) != 0) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+// second: the entry takes a second M x N operand (the gate's Y, the residual's R), whose type
+// may be given (FGEMM_Y_*); other entries refuse those bits.
+int parse_dtype(int dtype, Types* t, bool fp8_out = false, bool second = false) {
+  const int ab = dtype & 0xF, bias = dtype & 0xF0, out = dtype & 0xF00, y = dtype & 0xF000;
+  if ((dtype & ~0xFFFF) != 0) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (y != FGEMM_Y_SAME && y != FGEMM_Y_F16 && y != FGEMM_Y_BF16) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (y != FGEMM_Y_SAME && !second) return FGEMM_ERR_UNSUPPORTED_DTYPE;
   if (ab != FGEMM_F16 && ab != FGEMM_BF16 && ab != FGEMM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;
   if (bias != FGEMM_BIAS_SAME && bias != FGEMM_BIAS_F32 && bias != FGEMM_BIAS_BF16)
     return FGEMM_ERR_UNSUPPORTED_DTYPE;
   if (fp8_out ? (out != FGEMM_OUT_E4M3)
-              : (out != FGEMM_OUT_SAME && out != FGEMM_OUT_F32 && out != FGEMM_OUT_BF16))
+              : (out != FGEMM_OUT_SAME && out != FGEMM_OUT_F32 && out != FGEMM_OUT_BF16 &&
+                 out != FGEMM_OUT_F16))
     return FGEMM_ERR_UNSUPPORTED_DTYPE;
   const bool f8 = ab == FGEMM_E4M3;
   if (f8 && (bias == FGEMM_BIAS_SAME || out == FGEMM_OUT_SAME)) return FGEMM_ERR_UNSUPPORTED_DTYPE;
@@ -101,7 +107,18 @@ int parse_dtype(int dtype, Types* t, bool fp8_out = false) {
   t->out = (out == FGEMM_OUT_F32)    ? ELEM_F32
            : (out == FGEMM_OUT_E4M3) ? ELEM_E4M3
            : (out == FGEMM_OUT_BF16) ? ELEM_BF16
+           : (out == FGEMM_OUT_F16)  ? ELEM_F16
                                      : t->ab;
+  t->y = (y == FGEMM_Y_F16) ? ELEM_F16 : (y == FGEMM_Y_BF16) ? ELEM_BF16 : t->ab;
+  return FGEMM_OK;
+}
+
+// The gate's Y / the residual's R: a 16-bit type (explicit with fp8 operands), and with a 16-bit
+// output the output has Y's type (the tensor-core epilogue writes the result over the staged Y).
+int check_second_operand(const Types& t) {
+  if (t.y != ELEM_F16 && t.y != ELEM_BF16) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if ((t.out == ELEM_F16 || t.out == ELEM_BF16) && t.out != t.y) return FGEMM_ERR_UNSUPPORTED_DTYPE;
+  if (t.out == ELEM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;
   return FGEMM_OK;
 }
 
@@ -271,8 +288,7 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
   // (the epilogue has a whole main loop of slack); K <= 256: two blocks (Y two tiles ahead);
   // else one block.
   t.y_blocks = 1;
-  const bool staged_y = (c.epi == EPI_GATE || c.epi == EPI_RESID) && elem_bytes(c.t.out) == 2 &&
-                        c.t.ab != ELEM_E4M3;
+  const bool staged_y = (c.epi == EPI_GATE || c.epi == EPI_RESID) && elem_bytes(c.t.out) == 2;
   if (t.pair && staged_y) {
     const int want = c.opts ? c.opts->y_blocks : 0;
     if (want == 3)
@@ -377,7 +393,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
       !encode_2d(&tmO, c.t.out, c.out, c.M, c.N, 32, out_box_cols))
     return FGEMM_ERR_LAUNCH;
   if ((c.epi == EPI_GATE || c.epi == EPI_RESID) && c.t.out != ELEM_F32) {
-    if (!encode_2d(&tmY, c.t.ab, c.Y, c.M, c.N, 32, 64)) return FGEMM_ERR_LAUNCH;
+    if (!encode_2d(&tmY, c.t.y, c.Y, c.M, c.N, 32, 64)) return FGEMM_ERR_LAUNCH;
   } else {
     tmY = tmO;  // unused
   }
@@ -405,6 +421,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.group = (c.opts && c.opts->group_m > 0) ? c.opts->group_m : 16;
   p.ab_bf16 = c.t.ab == ELEM_BF16;
   p.ab_f8 = c.t.ab == ELEM_E4M3;
+  p.y_bf16 = c.t.y == ELEM_BF16;
   p.bias_type = c.t.bias;
   p.out_type = c.t.out;
   p.bias = c.bias;
@@ -436,6 +453,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   p.split = s.split;
   p.stages = s.stages;
   p.ab_type = c.t.ab;
+  p.y_type = c.t.y;
   p.bias_type = c.t.bias;
   p.out_type = c.t.out;
   p.bias = c.bias;
@@ -464,6 +482,7 @@ SimtParams simt_params(const Call& c) {
   p.N = static_cast<int>(c.N);
   p.K = static_cast<int>(c.K);
   p.ab_type = c.t.ab;
+  p.y_type = c.t.y;
   p.bias_type = c.t.bias;
   p.out_type = c.t.out;
   p.out_scale = c.out_scale;
@@ -539,9 +558,9 @@ int fgemm_addmm_gate_ex(const void* A, const void* B, const void* bias, const vo
                         int64_t M, int64_t N, int64_t K, int dtype, void* stream,
                         const fgemm_opts* opts, int* path_taken) {
   Call c{A, B, bias, Y, out, M, N, K, {}, EPI_GATE, static_cast<cudaStream_t>(stream), opts};
-  const int st = parse_dtype(dtype, &c.t);
+  int st = parse_dtype(dtype, &c.t, false, true);
+  if (st == FGEMM_OK) st = check_second_operand(c.t);
   if (st != FGEMM_OK) return st;
-  if (c.t.ab == ELEM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;  // Y has the operand type
   return fused(c, path_taken);
 }
 
@@ -549,9 +568,9 @@ int fgemm_bias_residual_relu_ex(const void* A, const void* B, const void* bias, 
                                 void* out, int64_t M, int64_t N, int64_t K, int dtype,
                                 void* stream, const fgemm_opts* opts, int* path_taken) {
   Call c{A, B, bias, R, out, M, N, K, {}, EPI_RESID, static_cast<cudaStream_t>(stream), opts};
-  const int st = parse_dtype(dtype, &c.t);
+  int st = parse_dtype(dtype, &c.t, false, true);
+  if (st == FGEMM_OK) st = check_second_operand(c.t);
   if (st != FGEMM_OK) return st;
-  if (c.t.ab == ELEM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;  // R has the operand type
   return fused(c, path_taken);
 }
 
@@ -588,7 +607,7 @@ int fgemm_addmm_gate(const void* A, const void* B, const void* bias, const void*
 
 size_t fgemm_unfused_workspace_bytes(int64_t M, int64_t N, int dtype, int inter_f32) {
   Types t{};
-  if (parse_dtype(dtype, &t) != FGEMM_OK || M < 0 || N < 0) return 0;
+  if (parse_dtype(dtype, &t, false, true) != FGEMM_OK || M < 0 || N < 0) return 0;
   const size_t e = inter_f32 ? 4 : static_cast<size_t>(elem_bytes(t.out));
   return round_up(static_cast<size_t>(M) * static_cast<size_t>(N) * e, 256);
 }
@@ -597,7 +616,8 @@ static int unfused(const void* A, const void* B, const void* bias, const void* Y
                    int64_t M, int64_t N, int64_t K, int dtype, void* workspace,
                    size_t workspace_bytes, int inter_f32, void* stream, int epi) {
   Call fin{A, B, bias, Y, out, M, N, K, {}, epi, static_cast<cudaStream_t>(stream), nullptr};
-  int st = parse_dtype(dtype, &fin.t);
+  int st = parse_dtype(dtype, &fin.t, false, epi == EPI_GATE);
+  if (st == FGEMM_OK && epi == EPI_GATE) st = check_second_operand(fin.t);
   if (st != FGEMM_OK) return st;
   if (fin.t.ab == ELEM_E4M3) return FGEMM_ERR_UNSUPPORTED_DTYPE;
   bool nothing = false;
@@ -626,7 +646,7 @@ static int unfused(const void* A, const void* B, const void* bias, const void* Y
     return status_of(launch_ew_relu(workspace, inter, out, fin.t.out, m, n, d->num_sms, s));
   }
   // step 2: out = (I + bias) + (I + bias) * Y
-  return status_of(launch_ew_bias_gate(workspace, inter, bias, fin.t.bias, Y, fin.t.ab, out,
+  return status_of(launch_ew_bias_gate(workspace, inter, bias, fin.t.bias, Y, fin.t.y, out,
                                        fin.t.out, m, n, d->num_sms, s));
 }
 
@@ -695,7 +715,9 @@ int plan_info(const void* A, const void* B, const void* bias, const void* Y, con
                 : epilogue == FGEMM_EPI_RELU_QUANT ? EPI_QUANT : EPI_RELU;
   Call c{A, B, bias, (epi == EPI_GATE || epi == EPI_RESID) ? Y : nullptr, const_cast<void*>(out),
          M, N, K, {}, epi, nullptr, opts};
-  int st = parse_dtype(dtype, &c.t, epi == EPI_QUANT);
+  const bool second = epi == EPI_GATE || epi == EPI_RESID;
+  int st = parse_dtype(dtype, &c.t, epi == EPI_QUANT, second);
+  if (st == FGEMM_OK && second) st = check_second_operand(c.t);
   if (st != FGEMM_OK) return st;
   bool nothing = false;
   st = validate(c, &nothing);

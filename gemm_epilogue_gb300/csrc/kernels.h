@@ -34,6 +34,7 @@ struct TcParams {
   int row_bars;    // k_rows 2: a full barrier per K row of a stage (B copied one K row at a time)
   int ab_bf16;     // operand (and Y) type: 0 = f16, 1 = bf16
   int ab_f8;       // 1: A and B are fp8 e4m3 (kind::f8f6f4 MMAs, 128-element K blocks)
+  int y_bf16;      // the gate's Y / the residual's R: 0 = f16, 1 = bf16
   int bias_type;   // Elem of the bias
   int out_type;    // Elem of out
   const void* bias;
@@ -55,6 +56,7 @@ struct SimtParams {
   void* out;
   int M, N, K;
   int ab_type;    // Elem
+  int y_type;     // Elem of Y / R
   int bias_type;  // Elem
   int out_type;   // Elem
   float out_scale;  // quantized epilogue only
@@ -82,6 +84,7 @@ struct SkParams {
   int split;      // CTAs per cluster splitting K (1..8)
   int stages;     // ring depth requested (0 = default)
   int ab_type, bias_type, out_type;  // Elem
+  int y_type;     // Elem of Y / R
   const void* bias;
   const void* Y;
   void* out;

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(gen::THREADS) generic_kernel(const SimtParams 
       const int gm = m0 + ty * 4 + i;
       if (gm >= p.M) continue;
       const int64_t idx = static_cast<int64_t>(gm) * p.N + gn;
-      const float y = (EPI == EPI_GATE || EPI == EPI_RESID) ? ld_elem(p.Y, idx, p.ab_type) : 0.f;
+      const float y = (EPI == EPI_GATE || EPI == EPI_RESID) ? ld_elem(p.Y, idx, p.y_type) : 0.f;
       st_elem(p.out, idx, p.out_type, epilogue<EPI>(acc[i][j], bj, y, p.out_scale));
     }
   }
@@ -258,7 +258,7 @@ static cudaError_t launch_ew(const EwParams& p, int num_sms, cudaStream_t s) {
 }
 
 cudaError_t launch_kzero(int epi, const SimtParams& sp, int num_sms, cudaStream_t s) {
-  EwParams p{sp.out_scale, nullptr, 0, sp.bias, sp.bias_type, sp.Y, sp.ab_type, sp.out, sp.out_type,
+  EwParams p{sp.out_scale, nullptr, 0, sp.bias, sp.bias_type, sp.Y, sp.y_type, sp.out, sp.out_type,
              sp.M, sp.N};
   if (epi == EPI_QUANT) return launch_ew<EW_KZERO_QUANT>(p, num_sms, s);
   if (epi == EPI_GATE) return launch_ew<EW_KZERO_GATE>(p, num_sms, s);

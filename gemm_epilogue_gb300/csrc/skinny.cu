@@ -332,8 +332,8 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
           float v = s4[e] + b;
           if constexpr (EPI == EPI_RELU) v = fmaxf(v, 0.0f);
           if constexpr (EPI == EPI_QUANT) v = fminf(fmaxf(fmaxf(v, 0.0f) * p.out_scale, -448.0f), 448.0f);
-          if constexpr (EPI == EPI_GATE) v = fmaf(v, ld_any(p.Y, o, p.ab_type), v);
-          if constexpr (EPI == EPI_RESID) v = fmaxf(v + ld_any(p.Y, o, p.ab_type), 0.0f);
+          if constexpr (EPI == EPI_GATE) v = fmaf(v, ld_any(p.Y, o, p.y_type), v);
+          if constexpr (EPI == EPI_RESID) v = fmaxf(v + ld_any(p.Y, o, p.y_type), 0.0f);
           st_any(p.out, o, p.out_type, v);
         }
       }

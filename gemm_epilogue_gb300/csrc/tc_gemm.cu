@@ -477,7 +477,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int cbeg = (ew >> 2) * (BN / 2);  // first column (within the tile) of this warpgroup
     const uint32_t ebuf = sbase + SMEM_EPI + static_cast<uint32_t>(ew) * C::EPI_WARP_BYTES;
     const bool out_bf = p.out_type == ELEM_BF16;
-    const bool y_bf = p.ab_bf16 != 0;
+    const bool y_bf = p.y_bf16 != 0;  // the gate's Y / the residual's R
     const uint64_t pol_out = policy_evict_first();
     const bool add_bias = !p.bias_init;  // else the accumulator already holds the bias
     // Bias-initialised accumulator ("Optimizing GEMM + Activation on CDNA4 with TLX", V4: the
@@ -946,15 +946,16 @@ template <int EPI, int OUT_BYTES, bool F8 = false>
 cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                                const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p,
                                int grid, bool pair, cudaStream_t s) {
-  if constexpr ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2 && !F8) {
-    if (pair && p.y_blocks == 2) return launch_one<EPI, OUT_BYTES, true, false, 2>(a, b, o, y, bm, p, grid, s);
+  if constexpr ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2) {
+    if (pair && p.y_blocks == 2) return launch_one<EPI, OUT_BYTES, true, F8, 2>(a, b, o, y, bm, p, grid, s);
     if (pair && p.y_blocks == 0)  // one 4 KB chunk of Y per warp
-      return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, false, 0, 2>(a, b, o, y, bm, p, grid, s)
-                           : launch_one<EPI, OUT_BYTES, true, false, 0, 1>(a, b, o, y, bm, p, grid, s);
+      return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, F8, 0, 2>(a, b, o, y, bm, p, grid, s)
+                           : launch_one<EPI, OUT_BYTES, true, F8, 0, 1>(a, b, o, y, bm, p, grid, s);
     // the bias-initialised accumulator set by an extra MMA (room for its tiles in shared memory)
-    if (p.bias_init && p.bias_mma && p.k_rows != 2)
-      return pair ? launch_one<EPI, OUT_BYTES, true, false, 1, 1, true>(a, b, o, y, bm, p, grid, s)
-                  : launch_one<EPI, OUT_BYTES, false, false, 1, 1, true>(a, b, o, y, bm, p, grid, s);
+    if constexpr (!F8)
+      if (p.bias_init && p.bias_mma && p.k_rows != 2)
+        return pair ? launch_one<EPI, OUT_BYTES, true, false, 1, 1, true>(a, b, o, y, bm, p, grid, s)
+                    : launch_one<EPI, OUT_BYTES, false, false, 1, 1, true>(a, b, o, y, bm, p, grid, s);
   }
   if (pair && p.k_rows == 2) return launch_one<EPI, OUT_BYTES, true, F8, 1, 2>(a, b, o, y, bm, p, grid, s);
   return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, bm, p, grid, s)
@@ -981,11 +982,18 @@ cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const
                       const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p, int grid,
                       bool pair, cudaStream_t s) {
   const bool f32 = p.out_type == ELEM_F32;
-  if (p.ab_f8) {  // fp8 operands: bias + ReLU (bf16 / fp32 out) and the quantized epilogue
+  if (p.ab_f8) {  // fp8 operands: bias + ReLU, the gate and the residual (16-bit / fp32 out),
+                  // and the quantized epilogue
     if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1, true>(a, b, o, y, bm, p, grid, pair, s);
-    if (epi != EPI_RELU) return cudaErrorNotSupported;
-    return f32 ? tc::launch_pair_or_not<EPI_RELU, 4, true>(a, b, o, y, bm, p, grid, pair, s)
-               : tc::launch_pair_or_not<EPI_RELU, 2, true>(a, b, o, y, bm, p, grid, pair, s);
+    switch (epi) {
+      case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4, true>(a, b, o, y, bm, p, grid, pair, s)
+                                : tc::launch_pair_or_not<EPI_RELU, 2, true>(a, b, o, y, bm, p, grid, pair, s);
+      case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4, true>(a, b, o, y, bm, p, grid, pair, s)
+                                : tc::launch_pair_or_not<EPI_GATE, 2, true>(a, b, o, y, bm, p, grid, pair, s);
+      case EPI_RESID: return f32 ? tc::launch_pair_or_not<EPI_RESID, 4, true>(a, b, o, y, bm, p, grid, pair, s)
+                                 : tc::launch_pair_or_not<EPI_RESID, 2, true>(a, b, o, y, bm, p, grid, pair, s);
+      default: return cudaErrorNotSupported;
+    }
   }
   if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1>(a, b, o, y, bm, p, grid, pair, s);
   switch (epi) {

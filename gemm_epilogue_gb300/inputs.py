@@ -42,6 +42,11 @@ class Workload:
     scale: float             # A and B are N(0,1) * scale
     bias_dist: str           # "normal" or "uniform"  (uniform is U(-1, 1))
     seed: int
+    y_dtype: int | None = None  # the gate's Y type when it differs from the operand type
+
+    @property
+    def y_type(self) -> int:
+        return self.ab_type if self.y_dtype is None else self.y_dtype
 
     @property
     def flops(self) -> int:
@@ -53,7 +58,7 @@ class Workload:
         b = self.M * self.K * es[self.ab_type] + self.K * self.N * es[self.ab_type]
         b += self.N * es[self.bias_type] + self.M * self.N * es[self.out_type]
         if self.epilogue == "gate":
-            b += self.M * self.N * es[self.ab_type]
+            b += self.M * self.N * es[self.y_type]
         return b
 
 
@@ -79,6 +84,11 @@ WORKLOADS["ffn_up_fp8_8192x14336x4096"] = Workload("ffn_up_fp8_8192x14336x4096",
                                                    "uniform", 6)
 WORKLOADS["square_fp8_4096"] = Workload("square_fp8_4096", 4096, 4096, 4096, E4M3, F32, BF16,
                                         "bias_relu", 1.0 / 8.0, "normal", 7)
+# the GLU block with the projection in fp8 and Y, out in fp16 ("Optimizing GEMM + Activation on
+# CDNA4 with TLX", "Future Work": FP8 precision); fp32 bias
+WORKLOADS["glu_gate_fp8_1024x21568x4096"] = Workload("glu_gate_fp8_1024x21568x4096", 1024, 21568,
+                                                     4096, E4M3, F32, F16, "gate", 1.0 / 8.0,
+                                                     "normal", 8, y_dtype=F16)
 for _m in (1, 16, 64, 128):
     WORKLOADS[f"skinny_M{_m}_8192"] = Workload(f"skinny_M{_m}_8192", _m, 8192, 8192, BF16, BF16,
                                                BF16, "bias_relu", 1.0 / 90.0, "normal", 4)
@@ -124,28 +134,34 @@ def make(w: Workload, seed: int | None = None) -> Inputs:
     bias = quantize(b, w.bias_type)
     Y = None
     if w.epilogue == "gate":
-        Y = quantize(rng.standard_normal((w.M, w.N), dtype=np.float32), w.ab_type)
+        Y = quantize(rng.standard_normal((w.M, w.N), dtype=np.float32), w.y_type)
     return Inputs(A, B, bias, Y)
 
 
 def random_problem(M: int, N: int, K: int, ab_type: int, bias_type: int, seed: int,
-                   scale: float | None = None, gate: bool = False) -> Inputs:
-    """Small seeded problem of any shape: A, B ~ N(0,1)/sqrt(K) (or ``scale``)."""
+                   scale: float | None = None, gate: bool = False,
+                   y_type: int | None = None) -> Inputs:
+    """Small seeded problem of any shape: A, B ~ N(0,1)/sqrt(K) (or ``scale``); Y (gate) of
+    ``y_type``, by default the operand type."""
     rng = np.random.default_rng(seed)
     s = np.float32(scale if scale is not None else 1.0 / math.sqrt(max(K, 1)))
     A = quantize(rng.standard_normal((M, K), dtype=np.float32) * s, ab_type)
     B = quantize(rng.standard_normal((K, N), dtype=np.float32) * s, ab_type)
     bias = quantize(rng.standard_normal(N, dtype=np.float32), bias_type)
-    Y = quantize(rng.standard_normal((M, N), dtype=np.float32), ab_type) if gate else None
+    yt = ab_type if y_type is None else y_type
+    Y = quantize(rng.standard_normal((M, N), dtype=np.float32), yt) if gate else None
     return Inputs(A, B, bias, Y)
 
 
 def integer_problem(M: int, N: int, K: int, ab_type: int, bias_type: int, seed: int,
-                    lo: int = -3, hi: int = 3, gate: bool = False) -> Inputs:
-    """Small-integer inputs in [lo, hi] (exact in every type, exact sums for small K)."""
+                    lo: int = -3, hi: int = 3, gate: bool = False,
+                    y_type: int | None = None) -> Inputs:
+    """Small-integer inputs in [lo, hi] (exact in every type, exact sums for small K); Y (gate)
+    of ``y_type``, by default the operand type."""
     rng = np.random.default_rng(seed)
     A = quantize(rng.integers(lo, hi + 1, (M, K)).astype(np.float32), ab_type)
     B = quantize(rng.integers(lo, hi + 1, (K, N)).astype(np.float32), ab_type)
     bias = quantize(rng.integers(2 * lo, 2 * hi + 1, N).astype(np.float32), bias_type)
-    Y = quantize(rng.integers(-2, 3, (M, N)).astype(np.float32), ab_type) if gate else None
+    yt = ab_type if y_type is None else y_type
+    Y = quantize(rng.integers(-2, 3, (M, N)).astype(np.float32), yt) if gate else None
     return Inputs(A, B, bias, Y)

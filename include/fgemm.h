@@ -65,12 +65,14 @@ typedef enum {
   FGEMM_ERR_WORKSPACE = 7          /* workspace NULL or smaller than required */
 } fgemm_status;
 
-/* dtype word = operand type | bias type | output type.  Y has the operand type. */
+/* dtype word = operand type | bias type | output type [| Y type].  The gate's Y (and the residual's
+   R) has the operand type unless a Y type is given. */
 #define FGEMM_F16 0x1        /* A, B (and Y) are IEEE binary16 */
 #define FGEMM_BF16 0x2       /* A, B (and Y) are bfloat16 */
-#define FGEMM_E4M3 0x3       /* A, B are fp8 e4m3 (bias+ReLU and the quantized entry only; the
-                                bias and output types must then be given explicitly; tensor-core
-                                path for K, N multiples of 16, CUDA-core path otherwise) */
+#define FGEMM_E4M3 0x3       /* A, B are fp8 e4m3 (the bias and output types must then be given
+                                explicitly, and for the gate and the residual the Y type as well;
+                                tensor-core path for K, N multiples of 16, CUDA-core path
+                                otherwise) */
 #define FGEMM_BIAS_SAME 0x00 /* bias has the operand type (16-bit operands) */
 #define FGEMM_BIAS_F32 0x10  /* bias is fp32 */
 #define FGEMM_BIAS_BF16 0x20 /* bias is bfloat16 */
@@ -78,6 +80,10 @@ typedef enum {
 #define FGEMM_OUT_F32 0x100  /* out is fp32 */
 #define FGEMM_OUT_E4M3 0x200 /* out is fp8 e4m3 (fgemm_bias_relu_quant only) */
 #define FGEMM_OUT_BF16 0x300 /* out is bfloat16 */
+#define FGEMM_OUT_F16 0x400  /* out is IEEE binary16 */
+#define FGEMM_Y_SAME 0x0000  /* Y (or R) has the operand type (16-bit operands) */
+#define FGEMM_Y_F16 0x1000   /* Y (or R) is IEEE binary16 (fgemm_addmm_gate, fgemm_bias_residual_relu) */
+#define FGEMM_Y_BF16 0x2000  /* Y (or R) is bfloat16 (fgemm_addmm_gate, fgemm_bias_residual_relu) */
 
 /* Epilogue codes (fgemm_plan). */
 #define FGEMM_EPI_RELU 0          /* fgemm_bias_relu */
@@ -150,13 +156,19 @@ typedef struct {
 int fgemm_bias_relu(const void* A, const void* B, const void* bias, void* out, int64_t M,
                     int64_t N, int64_t K, int dtype, void* stream);
 
-/* X = A @ B + bias; out = X + X * Y (Y: M x N, operand type).  Returns an fgemm_status. */
+/*
+ * X = A @ B + bias; out = X + X * Y (Y: M x N, 16-bit: the operand type, or the FGEMM_Y_* type).
+ * With fp8 e4m3 operands the projection A @ B runs on fp8 while Y stays 16-bit ("Optimizing GEMM +
+ * Activation on CDNA4 with TLX", "Future Work": FP8 precision); e.g. dtype = FGEMM_E4M3 |
+ * FGEMM_BIAS_F32 | FGEMM_OUT_F16 | FGEMM_Y_F16.  A 16-bit output has Y's type (else
+ * FGEMM_ERR_UNSUPPORTED_DTYPE); an fp32 output takes any 16-bit Y.  Returns an fgemm_status.
+ */
 int fgemm_addmm_gate(const void* A, const void* B, const void* bias, const void* Y, void* out,
                      int64_t M, int64_t N, int64_t K, int dtype, void* stream);
 
 /*
- * out = ReLU(A @ B + bias + R), R: M x N of the operand type, added after the K loop and before
- * the activation ("Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "Variants": matmul +
+ * out = ReLU(A @ B + bias + R), R: M x N, 16-bit (the operand type, or the FGEMM_Y_* type, with
+ * the same rules as the gate's Y), added after the K loop and before the activation ("Triton: Fused Matmul + Bias + ReLU (Epilogue Fusion)", "Variants": matmul +
  * residual add).  Same conventions as fgemm_bias_relu.  Returns an fgemm_status.
  */
 int fgemm_bias_residual_relu(const void* A, const void* B, const void* bias, const void* R,

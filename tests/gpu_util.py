@@ -36,9 +36,12 @@ def down(x, t):
     return x.view(torch.int16).numpy().view(np.uint16)
 
 
-def dtype_word(ab, bias, out):
+def dtype_word(ab, bias, out, y=None):
+    """The library's dtype word; `y` is the gate's Y type when it is not the operand type."""
     import gemm_epilogue_gb300.binding as fg
     w = {F16: fg.F16, BF16: fg.BF16, E4M3: fg.E4M3}[ab]
+    if y is not None and y != ab:
+        w |= {F16: fg.Y_F16, BF16: fg.Y_BF16}[y]
     if bias == F32:
         w |= fg.BIAS_F32
     elif bias == BF16 and ab != BF16:
@@ -51,6 +54,8 @@ def dtype_word(ab, bias, out):
         w |= fg.OUT_E4M3
     elif out == BF16 and ab != BF16:
         w |= fg.OUT_BF16
+    elif out == F16 and ab != F16:
+        w |= fg.OUT_F16
     elif out != ab:
         raise ValueError("unsupported out type")
     return w

@@ -139,3 +139,23 @@ def test_no_device_is_reported_without_a_gpu(lib):
     # all arguments valid; the call reaches the device check and stops there
     st = fg.call_status("fgemm_bias_relu", 4096, 4096, 4096, 4096, 4, 4, 4, fg.F16, None)
     assert st == fg.ERR_NO_DEVICE
+
+
+def test_second_operand_type_rules(lib):
+    # the gate / residual's Y type: 16-bit, and a 16-bit output has Y's type; other entries refuse
+    # the Y bits.  Refused before any device is touched.
+    bad = [("fgemm_addmm_gate", fg.E4M3 | fg.BIAS_F32 | fg.OUT_F16),                 # Y would be fp8
+           ("fgemm_addmm_gate", fg.E4M3 | fg.BIAS_F32 | fg.OUT_BF16 | fg.Y_F16),     # out != Y
+           ("fgemm_addmm_gate", fg.F16 | fg.OUT_BF16),                               # out != Y (f16)
+           ("fgemm_bias_residual_relu", fg.BF16 | fg.Y_F16),                          # out bf16, R f16
+           ("fgemm_addmm_gate", fg.F16 | 0x3000)]                                    # unknown Y code
+    for name, word in bad:
+        assert fg.call_status(name, None, None, None, None, None, 4, 4, 4, word, None) == \
+            fg.ERR_UNSUPPORTED_DTYPE, (name, hex(word))
+    assert fg.call_status("fgemm_bias_relu", None, None, None, None, 4, 4, 4,
+                          fg.F16 | fg.Y_BF16, None) == fg.ERR_UNSUPPORTED_DTYPE
+    # accepted words (the call then fails on the NULL buffers, not on the type)
+    for word in (fg.E4M3 | fg.BIAS_F32 | fg.OUT_F16 | fg.Y_F16,
+                 fg.E4M3 | fg.BIAS_BF16 | fg.OUT_F32 | fg.Y_BF16, fg.F16 | fg.Y_BF16 | fg.OUT_BF16):
+        assert fg.call_status("fgemm_addmm_gate", None, None, None, None, None, 4, 4, 4, word,
+                              None) == fg.ERR_INVALID_VALUE, hex(word)

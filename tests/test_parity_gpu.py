@@ -44,9 +44,10 @@ def run_fused(p, M, N, K, ab, bt, ot, gate=False, opts=None, out=None):
     return out, path
 
 
-def oracle_run(p, M, N, K, ab, bt, ot, gate=False, rows=None):
+def oracle_run(p, M, N, K, ab, bt, ot, gate=False, rows=None, y_type=None):
     if gate:
-        return oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, ab, bt, ot, rows=rows)
+        return oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, ab, bt, ot, rows=rows,
+                                 y_type=y_type)
     return oracle.bias_relu(p.A, p.B, p.bias, M, N, K, ab, bt, ot, rows=rows)
 
 
@@ -380,7 +381,65 @@ def test_fp8_operands_random_tolerance():
     check_close(down(out, BF16), ref, K, BF16, bias64=oracle.decode(p.bias, F32), what="fp8")
 
 
+FP8_GATE_CASES = [  # M, N, K, opts, expected path
+    (300, 528, 256, {"cta_pair": 2}, 1), (300, 528, 256, {"cta_pair": 1, "max_ctas": 20}, 1),
+    (777, 1296, 1344, None, 1),  # K > 1024: CTA pairs, Y staged one 4 KB chunk at a time
+    (513, 1040, 640, None, 1),   # 512 < K <= 1024: CTA pairs, one Y block per warp
+    (96, 1040, 512, None, 1),    # M <= 128: single CTAs (fp8 operands take the tensor-core path)
+    (7, 40, 24, None, 3), (300, 520, 200, None, 3)]  # N not a multiple of 16: CUDA cores
+
+
+@pytest.mark.parametrize("M,N,K,opts,want_path", FP8_GATE_CASES)
+def test_fp8_gate_and_residual_integer_bit_exact(M, N, K, opts, want_path):
+    # "Optimizing GEMM + Activation on CDNA4 with TLX", "Future Work" (FP8 precision): the
+    # projection on fp8 e4m3 operands, Y (or R) and the output 16-bit.  Integer inputs are exact
+    # in e4m3 and every sum is exact in fp32, so the only rounding is the output's.
+    for yt, ot in ((F16, F16), (BF16, BF16), (F16, F32)):
+        for epi in ("gate", "residual"):
+            p = gen.integer_problem(M, N, K, E4M3, F32, seed=M + K + yt, gate=True, y_type=yt)
+            A, B, bias, Y = up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32), up(p.Y, yt)
+            out = torch.full((M, N), float("nan"), dtype=torch_dtype(ot), device="cuda")
+            word = dtype_word(E4M3, F32, ot, yt)
+            if epi == "gate":
+                path = fg.fgemm_addmm_gate_ex(A, B, bias, Y, out, M, N, K, word, opts=opts)
+                ref = oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, E4M3, F32, ot, y_type=yt)
+            else:
+                path = fg.fgemm_bias_residual_relu_ex(A, B, bias, Y, out, M, N, K, word, opts=opts)
+                ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, E4M3, F32, ot,
+                                                y_type=yt)
+            torch.cuda.synchronize()
+            assert path == want_path, (epi, yt, ot)
+            got = down(out, ot)
+            if not _same_values(got, ref.out, ot):
+                bad = np.argwhere(oracle.decode(got, ot) != oracle.decode(ref.out, ot))
+                pytest.fail(f"{epi} Y {yt} out {ot}: {len(bad)} mismatches, first at {bad[:5].tolist()}")
+
+
+def test_fp8_gate_k_zero_and_16_bit_operands_with_another_y_type():
+    # K = 0: out = bias + bias * Y with Y of its own type; and 16-bit operands with a Y type of
+    # the other 16-bit format (the output then takes Y's type)
+    M, N = 37, 80
+    p = gen.integer_problem(M, N, 0, E4M3, F32, seed=3, gate=True, y_type=BF16)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    path = fg.fgemm_addmm_gate_ex(None, None, up(p.bias, F32), up(p.Y, BF16), out, M, N, 0,
+                                  dtype_word(E4M3, F32, BF16, BF16))
+    torch.cuda.synchronize()
+    assert path == fg.PATH_KZERO
+    ref = oracle.addmm_gate(None, None, p.bias, p.Y, M, N, 0, E4M3, F32, BF16, y_type=BF16)
+    assert _same_values(down(out, BF16), ref.out, BF16)
+    for (M, N, K), want_path in (((300, 520, 200), 1), ((16, 1032, 512), 2), ((7, 44, 9), 3)):
+        p = gen.integer_problem(M, N, K, F16, F16, seed=K, gate=True, y_type=BF16)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        path = fg.fgemm_addmm_gate_ex(up(p.A, F16), up(p.B, F16), up(p.bias, F16), up(p.Y, BF16),
+                                      out, M, N, K, dtype_word(F16, F16, BF16, BF16))
+        torch.cuda.synchronize()
+        assert path == want_path
+        ref = oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, F16, F16, BF16, y_type=BF16)
+        assert _same_values(down(out, BF16), ref.out, BF16), (M, N, K)
+
+
 def test_fp8_operands_refused_where_unsupported():
+    # the gate with fp8 operands needs the Y type: without it Y would be fp8, which is refused
     st = fg.call_status("fgemm_addmm_gate", None, None, None, None, None, 4, 4, 4,
                         fg.E4M3 | fg.BIAS_F32 | fg.OUT_BF16, None)
     assert st == fg.ERR_UNSUPPORTED_DTYPE
@@ -612,7 +671,7 @@ def test_bias_init_full_size_gate_sampled_rows():
     rows = sample_rows(w.M)
     ref = oracle_run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type, gate=True, rows=rows)
     check_close(down(out, w.out_type)[rows], ref, w.K, w.out_type,
-                Y64=oracle.decode(x.Y[rows], w.ab_type), bias64=oracle.decode(x.bias, w.bias_type),
+                Y64=oracle.decode(x.Y[rows], w.y_type), bias64=oracle.decode(x.bias, w.bias_type),
                 what="gate bias-init")
 
 
@@ -720,7 +779,8 @@ def test_unfused_chain_matches_oracle(inter_f32, gate):
 
 # ------------------------------------------------------------ full-size sampled --
 
-FULL = ["square_4096", "glu_gate_1024x21568x4096", "ffn_up_8192x14336x4096", "ffn_up_fp8_8192x14336x4096",
+FULL = ["square_4096", "glu_gate_1024x21568x4096", "glu_gate_fp8_1024x21568x4096",
+        "ffn_up_8192x14336x4096", "ffn_up_fp8_8192x14336x4096",
         "square_fp8_4096", "skinny_M1_8192",
         "skinny_M16_8192", "skinny_M64_8192", "skinny_M128_8192", "glu_gate_1024x21568x256",
         "glu_gate_1024x21568x512", "glu_gate_1024x21568x1024", "ragged_200x136x72"]
@@ -744,7 +804,8 @@ def launch_opts(dev_in, w, launch):
         return {}
     A, B, bias, Y, out = dev_in
     plan = fg.fgemm_plan(A, B, bias, Y, out, w.M, w.N, w.K,
-                         dtype_word(w.ab_type, w.bias_type, w.out_type), gate=Y is not None)
+                         dtype_word(w.ab_type, w.bias_type, w.out_type, w.y_type),
+                         gate=Y is not None)
     if plan["path"] != fg.PATH_TC or plan["tail_split"] == 1:
         return None
     return {"tail_split": 1}
@@ -758,7 +819,7 @@ def oracle_rows(name, x, w, rows):
     if key not in _oracle_rows:
         _oracle_rows.clear()
         _oracle_rows[key] = oracle_run(x, w.M, w.N, w.K, w.ab_type, w.bias_type, w.out_type,
-                                       gate=w.epilogue == "gate", rows=rows)
+                                       gate=w.epilogue == "gate", rows=rows, y_type=w.y_type)
     return _oracle_rows[key]
 
 
@@ -772,12 +833,12 @@ def run_full(x, w, launch, what):
     gate = w.epilogue == "gate"
     out, buf = guarded_out(w.M, w.N, w.out_type)
     dev_in = (up(x.A, w.ab_type), up(x.B, w.ab_type), up(x.bias, w.bias_type),
-              up(x.Y, w.ab_type) if gate else None, out)
+              up(x.Y, w.y_type) if gate else None, out)
     opts = launch_opts(dev_in, w, launch)
     if opts is None:
         return None
     A, B, bias, Y, _ = dev_in
-    word = dtype_word(w.ab_type, w.bias_type, w.out_type)
+    word = dtype_word(w.ab_type, w.bias_type, w.out_type, w.y_type)
     if gate:
         fg.fgemm_addmm_gate_ex(A, B, bias, Y, out, w.M, w.N, w.K, word, opts=opts or None)
     else:
@@ -804,14 +865,14 @@ def test_full_size_workloads(name, launch):
     rows = sample_rows(w.M)
     ref = oracle_rows(name, x, w, rows)
     got = down(out, w.out_type)[rows]
-    Y64 = oracle.decode(x.Y[rows], w.ab_type) if gate else None
+    Y64 = oracle.decode(x.Y[rows], w.y_type) if gate else None
     b64 = oracle.decode(x.bias, w.bias_type)
     check_close(got, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what=f"{name}/{launch}")
     if launch == "bench":
         # negative control: an output that left out the GEMM term must fail the per-element bound
         fake = oracle.gemm_epilogue(x.A, x.B, x.bias, w.M, w.N, w.K, w.ab_type, w.bias_type,
                                     w.out_type, oracle.EPI_GATE if gate else oracle.EPI_RELU,
-                                    Y=x.Y, rows=rows, mutant=oracle.MUT_DROP_GEMM)
+                                    Y=x.Y, rows=rows, mutant=oracle.MUT_DROP_GEMM, y_type=w.y_type)
         with pytest.raises(AssertionError):
             check_close(fake.out, ref, w.K, w.out_type, Y64=Y64, bias64=b64, what="bias-only control")
 
