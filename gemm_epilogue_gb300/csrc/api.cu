@@ -340,7 +340,8 @@ SkPlan plan_skinny(const Call& c, const DevShape& d) {
   SkPlan s{};
   s.mpad = static_cast<int>((c.M + 15) / 16 * 16);
   s.tiles_n = static_cast<int>((c.N + skinny_block_n() - 1) / skinny_block_n());
-  const int kb = static_cast<int>((c.K + 63) / 64);
+  const int kelems = c.t.ab == ELEM_E4M3 ? 128 : 64;  // K per stage: one 128-byte row of A
+  const int kb = static_cast<int>((c.K + kelems - 1) / kelems);
   const int want_stages = c.opts ? c.opts->stages : 0;
   int nt = (c.opts && c.opts->skinny_tiles > 0) ? c.opts->skinny_tiles : 1;
   for (;; --nt) {
@@ -440,8 +441,10 @@ int run_tc(const Call& c, DeviceInfo* d) {
 int run_skinny(const Call& c, DeviceInfo* d) {
   const SkPlan s = plan_skinny(c, shape_of(d));
   CUtensorMap tmB, tmA;
-  if (!encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, 64, 64) ||
-      !encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, static_cast<uint32_t>(s.mpad), 64))
+  // one 128-byte row of K per stage: B as 64 x 64 boxes (16-bit) or one 128 x 128 box (fp8)
+  const uint32_t kelems = c.t.ab == ELEM_E4M3 ? 128u : 64u;
+  if (!encode_2d(&tmB, c.t.ab, c.B, c.K, c.N, kelems, kelems) ||
+      !encode_2d(&tmA, c.t.ab, c.A, c.M, c.K, static_cast<uint32_t>(s.mpad), kelems))
     return FGEMM_ERR_LAUNCH;
   SkParams p{};
   p.M = static_cast<int>(c.M);
@@ -499,12 +502,11 @@ int choose_path(const Call& c, int* out_path) {
     else if (!tc_eligible(c))
       path = FGEMM_PATH_GENERIC;
     else
-      path = (c.M <= skinny_max_m() && c.t.ab != ELEM_E4M3) ? FGEMM_PATH_SKINNY : FGEMM_PATH_TC;
+      path = c.M <= skinny_max_m() ? FGEMM_PATH_SKINNY : FGEMM_PATH_TC;
   } else {
     path = forced;
     if (path == FGEMM_PATH_TC && (c.K == 0 || !tc_eligible(c))) return FGEMM_ERR_INVALID_VALUE;
-    if (path == FGEMM_PATH_SKINNY &&
-        (c.K == 0 || !tc_eligible(c) || c.M > skinny_max_m() || c.t.ab == ELEM_E4M3))
+    if (path == FGEMM_PATH_SKINNY && (c.K == 0 || !tc_eligible(c) || c.M > skinny_max_m()))
       return FGEMM_ERR_INVALID_VALUE;
     if (path == FGEMM_PATH_KZERO && (c.K != 0 || c.epi == EPI_NONE)) return FGEMM_ERR_INVALID_VALUE;
   }

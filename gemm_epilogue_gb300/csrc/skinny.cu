@@ -98,10 +98,14 @@ __device__ __forceinline__ void st_any(void* p, int64_t i, int type, float v) {
   }
 }
 
-template <int EPI>
+// F8: fp8 e4m3 operands (tcgen05 kind::f8f6f4, 32 K per MMA): one 128-byte K row of a stage is
+// 128 K elements, and B arrives as one 128 K-row x 128 N-column box per tile (the same bytes as
+// the two 64 x 64 boxes of 16-bit operands), so half the HBM bytes of B per output column.
+template <int EPI, bool F8 = false>
 __global__ void __launch_bounds__(MAX_THREADS, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
                   const SkParams p) {
+  constexpr int KBLK = F8 ? 2 * BK : BK;  // K elements per stage (one 128-byte row of A)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -127,7 +131,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   const uint32_t rank = (S > 1) ? cluster_ctarank() : 0u;
   const int W = BN * nt;  // output columns of this CTA
   const int n0 = static_cast<int>(blockIdx.x / S) * W;
-  const int KB = (p.K + BK - 1) / BK;
+  const int KB = (p.K + KBLK - 1) / KBLK;
   const int kb0 = static_cast<int>(static_cast<int64_t>(KB) * rank / S);
   const int kb1 = static_cast<int>(static_cast<int64_t>(KB) * (rank + 1) / S);
   const int nkb = kb1 - kb0;
@@ -183,9 +187,14 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
           }
           continue;
         }
-        for (int c = 0; c < 2 * nt; ++c)
-          tma_load_2d(dst + c * B_BOX_BYTES, &tmB, fb, n0 + 64 * c, kb * BK, pol_b);
-        tma_load_2d(dst + static_cast<uint32_t>(nt) * B_TILE_BYTES, &tmA, fb, kb * BK, 0, pol_a);
+        if constexpr (F8) {
+          for (int c = 0; c < nt; ++c)  // one 128 x 128 fp8 box per tile
+            tma_load_2d(dst + c * B_TILE_BYTES, &tmB, fb, n0 + BN * c, kb * KBLK, pol_b);
+        } else {
+          for (int c = 0; c < 2 * nt; ++c)
+            tma_load_2d(dst + c * B_BOX_BYTES, &tmB, fb, n0 + 64 * c, kb * KBLK, pol_b);
+        }
+        tma_load_2d(dst + static_cast<uint32_t>(nt) * B_TILE_BYTES, &tmA, fb, kb * KBLK, 0, pol_a);
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == static_cast<uint32_t>(stages)) {
@@ -212,13 +221,18 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
         const uint32_t b_addr = sbase + stage * sbytes;                            // B^T, N-major
         const uint32_t a_addr = b_addr + static_cast<uint32_t>(nt) * B_TILE_BYTES;  // A^T, K-major
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
+        for (int k = 0; k < 4; ++k) {  // 32 bytes of K per MMA: 16 16-bit or 32 fp8 elements
           const uint64_t db = sdesc_sw128(a_addr + 32u * k, 16u, 1024u);
           for (int t = 0; t < nt; ++t) {
-            const uint64_t da =
-                sdesc_sw128(b_addr + t * B_TILE_BYTES + 2048u * k, B_BOX_BYTES, 1024u);
-            umma_f16(tmem_base + static_cast<uint32_t>(t * p.mpad), da, db, p.idesc,
-                     (kb > kb0 || k > 0) ? 1u : 0u);
+            // B^T (MN-major): 16 (32 fp8) K rows of 128 bytes per MMA; 64-column boxes for
+            // 16-bit operands, one 128-column box for fp8
+            const uint64_t da = sdesc_sw128(b_addr + t * B_TILE_BYTES + (F8 ? 4096u : 2048u) * k,
+                                            F8 ? B_TILE_BYTES : B_BOX_BYTES, 1024u);
+            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+            if constexpr (F8)
+              umma_f8_cg<1>(tmem_base + static_cast<uint32_t>(t * p.mpad), da, db, p.idesc, acc);
+            else
+              umma_f16(tmem_base + static_cast<uint32_t>(t * p.mpad), da, db, p.idesc, acc);
           }
         }
         umma_commit(bar(BAR_EMPTY + stage));
@@ -349,10 +363,10 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
   }
 }
 
-template <int EPI>
+template <int EPI, bool F8>
 cudaError_t launch_one(const CUtensorMap& tb, const CUtensorMap& ta, const SkParams& p, int ctas,
                        cudaStream_t s) {
-  auto k = skinny_kernel<EPI>;
+  auto k = skinny_kernel<EPI, F8>;
   const uint32_t smem = smem_bytes(p.mpad, p.nt, p.split, p.stages);
   // Per device: the shared-memory opt-in is set once.  Host threads may race on a first call;
   // setting the attribute twice is harmless, and the flag is atomic.
@@ -395,12 +409,21 @@ uint32_t skinny_smem_bytes(int mpad, int nt, int split, int stages) {
 
 cudaError_t launch_skinny(int epi, const CUtensorMap& tmB, const CUtensorMap& tmA, const SkParams& p,
                           int ctas, cudaStream_t s) {
+  if (p.ab_type == ELEM_E4M3) {
+    switch (epi) {
+      case EPI_RELU: return sk::launch_one<EPI_RELU, true>(tmB, tmA, p, ctas, s);
+      case EPI_GATE: return sk::launch_one<EPI_GATE, true>(tmB, tmA, p, ctas, s);
+      case EPI_RESID: return sk::launch_one<EPI_RESID, true>(tmB, tmA, p, ctas, s);
+      case EPI_QUANT: return sk::launch_one<EPI_QUANT, true>(tmB, tmA, p, ctas, s);
+      default: return cudaErrorNotSupported;
+    }
+  }
   switch (epi) {
-    case EPI_RELU: return sk::launch_one<EPI_RELU>(tmB, tmA, p, ctas, s);
-    case EPI_GATE: return sk::launch_one<EPI_GATE>(tmB, tmA, p, ctas, s);
-    case EPI_RESID: return sk::launch_one<EPI_RESID>(tmB, tmA, p, ctas, s);
-    case EPI_QUANT: return sk::launch_one<EPI_QUANT>(tmB, tmA, p, ctas, s);
-    default: return sk::launch_one<EPI_NONE>(tmB, tmA, p, ctas, s);
+    case EPI_RELU: return sk::launch_one<EPI_RELU, false>(tmB, tmA, p, ctas, s);
+    case EPI_GATE: return sk::launch_one<EPI_GATE, false>(tmB, tmA, p, ctas, s);
+    case EPI_RESID: return sk::launch_one<EPI_RESID, false>(tmB, tmA, p, ctas, s);
+    case EPI_QUANT: return sk::launch_one<EPI_QUANT, false>(tmB, tmA, p, ctas, s);
+    default: return sk::launch_one<EPI_NONE, false>(tmB, tmA, p, ctas, s);
   }
 }
 

@@ -92,6 +92,10 @@ WORKLOADS["glu_gate_fp8_1024x21568x4096"] = Workload("glu_gate_fp8_1024x21568x40
 for _m in (1, 16, 64, 128):
     WORKLOADS[f"skinny_M{_m}_8192"] = Workload(f"skinny_M{_m}_8192", _m, 8192, 8192, BF16, BF16,
                                                BF16, "bias_relu", 1.0 / 90.0, "normal", 4)
+# decode-like shapes with fp8 e4m3 operands (half the bytes of B), fp32 bias, bf16 out
+for _m in (1, 16, 64, 128):
+    WORKLOADS[f"skinny_fp8_M{_m}_8192"] = Workload(f"skinny_fp8_M{_m}_8192", _m, 8192, 8192, E4M3,
+                                                   F32, BF16, "bias_relu", 1.0 / 8.0, "normal", 9)
 
 
 def quantize(x: np.ndarray, t: int) -> np.ndarray:

@@ -336,7 +336,7 @@ def test_quant_random_within_one_fp8_step():
 
 FP8_CASES = [  # M, N, K, opts, expected path
     (300, 528, 256, {"cta_pair": 2}, 1), (300, 528, 256, {"cta_pair": 1, "max_ctas": 20}, 1),
-    (777, 1296, 336, None, 1), (96, 1040, 512, None, 1), (7, 40, 24, None, 3),
+    (777, 1296, 336, None, 1), (96, 1040, 512, None, 2), (7, 40, 24, None, 3),
     (300, 520, 200, None, 3)]
 
 
@@ -385,7 +385,7 @@ FP8_GATE_CASES = [  # M, N, K, opts, expected path
     (300, 528, 256, {"cta_pair": 2}, 1), (300, 528, 256, {"cta_pair": 1, "max_ctas": 20}, 1),
     (777, 1296, 1344, None, 1),  # K > 1024: CTA pairs, Y staged one 4 KB chunk at a time
     (513, 1040, 640, None, 1),   # 512 < K <= 1024: CTA pairs, one Y block per warp
-    (96, 1040, 512, None, 1),    # M <= 128: single CTAs (fp8 operands take the tensor-core path)
+    (96, 1040, 512, None, 2),    # M <= 128: the swap-AB skinny kernel
     (7, 40, 24, None, 3), (300, 520, 200, None, 3)]  # N not a multiple of 16: CUDA cores
 
 
@@ -754,6 +754,40 @@ def test_pair_and_single_cta_agree():
         check_close(down(x, F16), ref, K, F16, bias64=oracle.decode(p.bias, F16), what="pair/single")
 
 
+SKINNY_FP8_SHAPES = [(1, 144, 128, 1), (5, 272, 512, 3), (16, 1040, 2048, 4), (33, 400, 256, 2),
+                     (64, 144, 32, 4), (100, 528, 1024, 8), (128, 1040, 512, 2)]
+
+
+@pytest.mark.parametrize("M,N,K,split", SKINNY_FP8_SHAPES)
+@pytest.mark.parametrize("tiles", [1, 2])
+def test_skinny_fp8_integer_bit_exact(M, N, K, split, tiles):
+    # fp8 e4m3 operands on the swap-AB kernel (kind::f8f6f4, 128 K elements per stage): bias +
+    # ReLU, the gate with a 16-bit Y, and the quantized output; (64, 144, 32, 4) leaves three of
+    # the four CTAs of each cluster without a K block
+    o = {"split_k": split, "skinny_tiles": tiles}
+    for bt, ot in ((F32, BF16), (BF16, F32)):
+        p = gen.integer_problem(M, N, K, E4M3, bt, seed=M + N + K + split)
+        out = torch.empty(M, N, dtype=torch_dtype(ot), device="cuda")
+        path = fg.fgemm_bias_relu_ex(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, bt), out, M, N, K,
+                                     dtype_word(E4M3, bt, ot), opts=o)
+        torch.cuda.synchronize()
+        assert path == fg.PATH_SKINNY
+        assert _same_values(down(out, ot), oracle.bias_relu(p.A, p.B, p.bias, M, N, K, E4M3, bt, ot).out, ot)
+    p = gen.integer_problem(M, N, K, E4M3, F32, seed=M + K, gate=True, y_type=F16)
+    out = torch.empty(M, N, dtype=torch.float16, device="cuda")
+    fg.fgemm_addmm_gate_ex(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32), up(p.Y, F16), out, M, N,
+                           K, dtype_word(E4M3, F32, F16, F16), opts=o)
+    torch.cuda.synchronize()
+    ref = oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, E4M3, F32, F16, y_type=F16)
+    assert _same_values(down(out, F16), ref.out, F16)
+    p = gen.integer_problem(M, N, K, E4M3, F32, seed=M + 7)
+    out = torch.empty(M, N, dtype=torch.uint8, device="cuda")
+    fg.fgemm_bias_relu_quant_ex(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32), out, M, N, K,
+                                fg.E4M3 | fg.BIAS_F32 | fg.OUT_E4M3, 0.25, opts=o)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), oracle.bias_relu_quant(p.A, p.B, p.bias, M, N, K, E4M3, F32, 0.25).out)
+
+
 # -------------------------------------------------------------- unfused chain --
 
 @pytest.mark.parametrize("inter_f32", [0, 1])
@@ -782,7 +816,8 @@ def test_unfused_chain_matches_oracle(inter_f32, gate):
 FULL = ["square_4096", "glu_gate_1024x21568x4096", "glu_gate_fp8_1024x21568x4096",
         "ffn_up_8192x14336x4096", "ffn_up_fp8_8192x14336x4096",
         "square_fp8_4096", "skinny_M1_8192",
-        "skinny_M16_8192", "skinny_M64_8192", "skinny_M128_8192", "glu_gate_1024x21568x256",
+        "skinny_M16_8192", "skinny_M64_8192", "skinny_M128_8192", "skinny_fp8_M1_8192",
+        "skinny_fp8_M16_8192", "skinny_fp8_M64_8192", "skinny_fp8_M128_8192", "glu_gate_1024x21568x256",
         "glu_gate_1024x21568x512", "glu_gate_1024x21568x1024", "ragged_200x136x72"]
 
 _made = {}

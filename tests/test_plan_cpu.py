@@ -80,8 +80,11 @@ def test_fp8_operands():
     # two 128-element K rows per stage, each on its own full barrier
     assert (p["path"], p["cluster"], p["tail_split"], p["work_items"]) == (fg.PATH_TC, 2, 1, 256)
     assert (p["k_rows"], p["row_barriers"]) == (2, 1)
-    # fp8 operands never take the skinny path
-    assert plan(64, 4096, 4096, word)["path"] == fg.PATH_TC
+    # decode-like shapes with fp8 operands take the swap-AB skinny kernel as well: 128 K elements
+    # per stage, so the same K split over the cluster as 16-bit operands with half the K
+    p = plan(64, 8192, 8192, word)
+    q = plan(64, 8192, 4096, fg.BF16)
+    assert p["path"] == fg.PATH_SKINNY and (p["grid"], p["cluster"]) == (q["grid"], q["cluster"])
 
 
 @pytest.mark.parametrize("M", [1, 16, 64, 128])
