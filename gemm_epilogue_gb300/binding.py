@@ -48,7 +48,8 @@ class Opts(ctypes.Structure):
                 ("skinny_tiles", ctypes.c_int), ("stages", ctypes.c_int),
                 ("inject_stall", ctypes.c_int), ("bias_init", ctypes.c_int),
                 ("full_last_n", ctypes.c_int), ("y_blocks", ctypes.c_int),
-                ("k_rows", ctypes.c_int), ("bias_mma", ctypes.c_int), ("pdl", ctypes.c_int)]
+                ("k_rows", ctypes.c_int), ("bias_mma", ctypes.c_int), ("pdl", ctypes.c_int),
+                ("raster", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):

@@ -192,7 +192,7 @@ int validate(const Call& c, bool* nothing) {
         o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 2 ||
         o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 3 ||
         o.k_rows < 0 || o.k_rows > 2 || o.bias_mma < 0 || o.bias_mma > 2 || o.pdl < 0 ||
-        o.pdl > 2)
+        o.pdl > 2 || o.raster < 0 || o.raster > 1)
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -420,6 +420,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   // 16 M-tiles per band: measured best on the 8192-row FFN (577-583 vs 595-605 us for 8); the
   // square and GLU shapes have at most 16 tile rows, so every value from there up is the same order
   p.group = (c.opts && c.opts->group_m > 0) ? c.opts->group_m : 16;
+  p.raster_n = (c.opts && c.opts->raster == 1) ? 1 : 0;
   p.ab_bf16 = c.t.ab == ELEM_BF16;
   p.ab_f8 = c.t.ab == ELEM_E4M3;
   p.y_bf16 = c.t.y == ELEM_BF16;

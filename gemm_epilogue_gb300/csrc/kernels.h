@@ -18,6 +18,7 @@ inline int elem_bytes(int e) { return e == ELEM_F32 ? 4 : (e == ELEM_E4M3 ? 1 : 
 struct TcParams {
   int M, N, K;
   int tiles_m, tiles_n, num_tiles, group;
+  int raster_n;    // 1: the grouped order runs over N (bands of `group` N-tiles, N fastest inside)
   // Work items: items 0 .. full_tiles-1 are whole tiles; the remaining num_tiles - full_tiles tiles
   // (the last, partial round of the persistent grid) are each cut into `tail_split` pieces along N
   // (256 / tail_split columns each) so that the last round takes a fraction of a tile's time.

@@ -142,7 +142,10 @@ __device__ __forceinline__ Work work_of(const TcParams& p, int item) {
     tile = p.full_tiles + j / split;
     piece = j % split;
   }
-  tile_of(tile, p.tiles_m, p.tiles_n, p.group, w.tm, w.tn);
+  if (p.raster_n)  // the same grouped order with the roles of M and N exchanged
+    tile_of(tile, p.tiles_n, p.tiles_m, p.group, w.tn, w.tm);
+  else
+    tile_of(tile, p.tiles_m, p.tiles_n, p.group, w.tm, w.tn);
   w.width = BN / split;
   w.col0 = w.tn * BN + piece * w.width;
   if (w.tn == p.tiles_n - 1) {  // ragged last column of tiles: only as wide as N needs

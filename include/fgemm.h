@@ -147,6 +147,10 @@ typedef struct {
                      complete (griddepcontrol.wait) before its first access to global memory, so a
                      dependency between the two stays safe.  0 = automatic (on for the skinny path
                      and for K <= 1024), 1 = on, 2 = off */
+  int raster;     /* tensor-core path: 0 = the grouped order over M ("I3. Fuse a GEMM epilogue and
+                     change tile scheduling": bands of group_m M-tiles walking N); 1 = the same
+                     order with M and N exchanged (bands of group_m N-tiles walking M), which keeps
+                     a band of B instead of A in L2 */
 } fgemm_opts;
 
 /*

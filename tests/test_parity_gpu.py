@@ -722,7 +722,8 @@ def test_grouping_and_grid_do_not_change_results(pair):
     M, N, K = 700, 1800, 128
     p = gen.random_problem(M, N, K, BF16, BF16, seed=4)
     base, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts={"cta_pair": pair})
-    for opts in ({"group_m": 1}, {"group_m": 4}, {"group_m": 3, "max_ctas": 7}, {"max_ctas": 2}):
+    for opts in ({"group_m": 1}, {"group_m": 4}, {"group_m": 3, "max_ctas": 7}, {"max_ctas": 2},
+                 {"raster": 1}, {"raster": 1, "group_m": 3}):
         out, _ = run_fused(p, M, N, K, BF16, BF16, BF16, opts=dict(opts, cta_pair=pair))
         assert torch.equal(out, base), opts
 
