@@ -297,6 +297,10 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
       t.y_blocks = want;
     else
       t.y_blocks = c.K > 1024 ? 0 : (c.K <= 256 ? 2 : 1);
+  } else if (staged_y) {
+    // single CTAs: one block per warp, or two (Y two work items ahead, for a two-stage ring)
+    const int want = c.opts ? c.opts->y_blocks : 0;
+    t.y_blocks = want == 2 ? 2 : 1;
   }
   // Two K rows per stage on CTA pairs (half the stage hand-offs; 3 stages of 64 KB instead of 6
   // of 32 KB), unless a whole staged Y block per warp leaves room for two stages only.
@@ -323,7 +327,7 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
   // 37.8 vs 35.9 us; CTA pairs at K = 1024 48.9 vs 44.1 us.
   const int bm = c.opts ? c.opts->bias_mma : 0;
   t.bias_mma = t.bias_init && staged_y && c.t.bias == c.t.ab && c.t.ab != ELEM_F32 &&
-               (!t.pair || (t.y_blocks == 1 && t.k_rows == 1)) &&
+               t.y_blocks == 1 && t.k_rows == 1 &&
                (bm == 2 || (bm == 0 && !t.pair && c.K <= 256));
   return t;
 }

@@ -76,7 +76,8 @@ constexpr uint32_t ONES_BYTES = 4096;             // 128 rows x 16 K of 16-bit o
 constexpr uint32_t BIAS_BOX_BYTES = 16 * 128;     // 16 K rows x 64 columns of 16-bit values
 template <bool PAIR, bool YS = false, int YB = 1, int KSUB = 1, bool MB = false>
 struct Cfg {
-  static_assert(YB == 1 || ((YB == 2 || YB == 0) && PAIR && YS), "Y staging variants: staged Y on CTA pairs");
+  static_assert(YB == 1 || (YB == 2 && YS) || (YB == 0 && PAIR && YS),
+                "Y staging variants: staged Y (chunk at a time on CTA pairs only)");
   static_assert(KSUB == 1 || KSUB == 2, "one or two K rows per stage");
   static constexpr uint32_t A_STAGE_BYTES = KSUB * A_ROW_BYTES;
   static constexpr uint32_t B_STAGE_BYTES = KSUB * (PAIR ? 1 : 2) * B_ROW_BYTES;  // this CTA's columns
@@ -950,7 +951,9 @@ cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const
                                const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p,
                                int grid, bool pair, cudaStream_t s) {
   if constexpr ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2) {
-    if (pair && p.y_blocks == 2) return launch_one<EPI, OUT_BYTES, true, F8, 2>(a, b, o, y, bm, p, grid, s);
+    if (p.y_blocks == 2)
+      return pair ? launch_one<EPI, OUT_BYTES, true, F8, 2>(a, b, o, y, bm, p, grid, s)
+                  : launch_one<EPI, OUT_BYTES, false, F8, 2>(a, b, o, y, bm, p, grid, s);
     if (pair && p.y_blocks == 0)  // one 4 KB chunk of Y per warp
       return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, F8, 0, 2>(a, b, o, y, bm, p, grid, s)
                            : launch_one<EPI, OUT_BYTES, true, F8, 0, 1>(a, b, o, y, bm, p, grid, s);

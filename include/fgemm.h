@@ -125,12 +125,13 @@ typedef struct {
                      Ignored by the other paths and by the plain GEMM. */
   int full_last_n; /* tensor-core path, diagnostic: 1 = run the last column of tiles at the full
                       256-column width instead of narrowing it to the columns left of N */
-  int y_blocks;   /* tensor-core path, gate and residual with 16-bit outputs on CTA pairs: how
-                     each epilogue warp stages its share of the second M x N operand: 0 =
-                     automatic (3 when K > 1024, 2 when K <= 256, else 1), 1 = the tile's 32 x 128
-                     block, one work item ahead, 2 = two such blocks, two items ahead (3-stage
-                     ring), 3 = one 32 x 64 chunk at a time (4 KB; leaves room for two-row ring
-                     stages).  Ignored elsewhere. */
+  int y_blocks;   /* tensor-core path, gate and residual with 16-bit outputs: how each epilogue
+                     warp stages its share of the second M x N operand: 0 = automatic (on CTA
+                     pairs 3 when K > 1024, 2 when K <= 256, else 1; on single CTAs 1), 1 = the
+                     tile's 32 x 128 block, one work item ahead, 2 = two such blocks, two items
+                     ahead (a 3-stage ring on pairs, 2 stages on single CTAs), 3 = one 32 x 64
+                     chunk at a time (4 KB; leaves room for two-row ring stages; CTA pairs only,
+                     else as 1).  Ignored elsewhere. */
   int k_rows;     /* tensor-core path on CTA pairs: 128-byte K rows (64 16-bit or 128 fp8
                      elements) per stage of the operand ring; 0 = automatic (2, or 1 for the
                      gate and residual with 16-bit outputs), 1 = six stages of 32 KB per SM,

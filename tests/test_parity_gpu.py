@@ -550,6 +550,33 @@ def test_k_rows_per_stage_integer_bit_exact(M, N, K, max_ctas, k_rows):
     assert np.array_equal(down(out, F16), oracle_run(p, M, N, K, F16, F16, F16, gate=True).out)
 
 
+@pytest.mark.parametrize("M,N,K,max_ctas", [(300, 520, 200, 0), (700, 1800, 200, 44), (513, 1288, 64, 12),
+                                           (1000, 2056, 504, 0)])
+def test_staged_y_two_blocks_single_cta_integer_bit_exact(M, N, K, max_ctas):
+    # Two staged Y blocks per epilogue warp on single CTAs (Y two work items ahead, a two-stage
+    # ring), with the bias added by the epilogue, written into tensor memory, or by the MMA form
+    # (which then falls back to tensor memory: its tiles have no room beside two Y blocks)
+    for bias_init, bias_mma in ((2, 0), (1, 1), (1, 2)):
+        opts = {"path": fg.PATH_TC, "cta_pair": 1, "max_ctas": max_ctas, "y_blocks": 2,
+                "bias_init": bias_init, "bias_mma": bias_mma}
+        for ab in (F16, BF16):
+            p = gen.integer_problem(M, N, K, ab, ab, seed=M + K + ab, gate=True)
+            plan = fg.fgemm_plan(up(p.A, ab), up(p.B, ab), up(p.bias, ab), up(p.Y, ab),
+                                 torch.empty(M, N, dtype=torch_dtype(ab), device="cuda"), M, N, K,
+                                 dtype_word(ab, ab, ab), gate=True, opts=opts)
+            assert (plan["cluster"], plan["y_blocks"]) == (1, 2)
+            assert plan["bias_init"] == (0 if bias_init == 2 else 1)
+            out, path = run_fused(p, M, N, K, ab, ab, ab, gate=True, opts=opts)
+            assert path == fg.PATH_TC
+            assert _same_values(down(out, ab), oracle_run(p, M, N, K, ab, ab, ab, gate=True).out, ab)
+            res = torch.empty(M, N, dtype=torch_dtype(ab), device="cuda")
+            fg.fgemm_bias_residual_relu_ex(up(p.A, ab), up(p.B, ab), up(p.bias, ab), up(p.Y, ab),
+                                           res, M, N, K, dtype_word(ab, ab, ab), opts=opts)
+            torch.cuda.synchronize()
+            ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, ab, ab, ab)
+            assert _same_values(down(res, ab), ref.out, ab)
+
+
 def _same_values(got_bits, ref_bits, t):
     """Equal as numbers (-0 == +0), every element."""
     return np.array_equal(oracle.decode(got_bits, t), oracle.decode(ref_bits, t))
