@@ -49,7 +49,7 @@ class Opts(ctypes.Structure):
                 ("inject_stall", ctypes.c_int), ("bias_init", ctypes.c_int),
                 ("full_last_n", ctypes.c_int), ("y_blocks", ctypes.c_int),
                 ("k_rows", ctypes.c_int), ("bias_mma", ctypes.c_int), ("pdl", ctypes.c_int),
-                ("raster", ctypes.c_int)]
+                ("raster", ctypes.c_int), ("epi_warps", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -58,7 +58,7 @@ class PlanInfo(ctypes.Structure):
                 ("tiles", ctypes.c_int), ("work_items", ctypes.c_int), ("tail_split", ctypes.c_int),
                 ("resident_pairs", ctypes.c_int), ("last_tile_n", ctypes.c_int),
                 ("y_blocks", ctypes.c_int), ("k_rows", ctypes.c_int), ("row_barriers", ctypes.c_int),
-                ("bias_init", ctypes.c_int)]
+                ("bias_init", ctypes.c_int), ("epi_warps", ctypes.c_int)]
 
 
 _lock = threading.Lock()

@@ -192,7 +192,8 @@ int validate(const Call& c, bool* nothing) {
         o.inject_stall < 0 || o.inject_stall > 1 || o.bias_init < 0 || o.bias_init > 2 ||
         o.full_last_n < 0 || o.full_last_n > 1 || o.y_blocks < 0 || o.y_blocks > 3 ||
         o.k_rows < 0 || o.k_rows > 2 || o.bias_mma < 0 || o.bias_mma > 2 || o.pdl < 0 ||
-        o.pdl > 2 || o.raster < 0 || o.raster > 1)
+        o.pdl > 2 || o.raster < 0 || o.raster > 1 ||
+        (o.epi_warps != 0 && o.epi_warps != 8 && o.epi_warps != 16))
       return FGEMM_ERR_INVALID_VALUE;
   }
   return FGEMM_OK;
@@ -219,6 +220,7 @@ struct TcPlan {
   bool row_bars;         // a full barrier per K row of a stage
   bool bias_init;        // the accumulator starts at the bias
   bool bias_mma;         // ... set by an extra MMA from the staged bias row
+  int epi_warps;         // epilogue warps per CTA (8, or 16 on single CTAs with a staged Y block)
 };
 
 // What the planners need to know about the device: its SM count and how many CTA pairs of the
@@ -325,6 +327,8 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
   // the tiles cost a ring stage).  Automatic for single CTAs with K <= 256 only: measured on the
   // GLU block (M = 1024, N = 21568), alternating on one GB300, K = 256 26.3 vs 26.9 us; K = 512
   // 37.8 vs 35.9 us; CTA pairs at K = 1024 48.9 vs 44.1 us.
+  // Sixteen epilogue warps (64 columns each) for single CTAs with one staged Y block per warp.
+  t.epi_warps = (!t.pair && staged_y && t.y_blocks == 1 && c.opts && c.opts->epi_warps == 16) ? 16 : 8;
   const int bm = c.opts ? c.opts->bias_mma : 0;
   t.bias_mma = t.bias_init && staged_y && c.t.bias == c.t.ab && c.t.ab != ELEM_F32 &&
                t.y_blocks == 1 && t.k_rows == 1 &&
@@ -419,6 +423,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.bias_init = t.bias_init ? 1 : 0;
   p.bias_mma = t.bias_mma ? 1 : 0;
   p.y_blocks = t.y_blocks;
+  p.epi_warps = t.epi_warps;
   p.k_rows = t.k_rows;
   p.row_bars = t.row_bars ? 1 : 0;
   // 16 M-tiles per band: measured best on the 8192-row FFN (577-583 vs 595-605 us for 8); the
@@ -757,6 +762,7 @@ int plan_info(const void* A, const void* B, const void* bias, const void* Y, con
     info->resident_pairs = t.resident;
     info->row_barriers = t.row_bars ? 1 : 0;
     info->bias_init = t.bias_init ? (t.bias_mma ? 2 : 1) : 0;
+    info->epi_warps = t.epi_warps;
   } else if (path == FGEMM_PATH_SKINNY) {
     const SkPlan s = plan_skinny(c, dev);
     info->cluster = s.split;

@@ -31,6 +31,7 @@ struct TcParams {
   int bias_mma;    // with bias_init: 1 = set by an extra MMA from the staged bias row (16-bit bias of
                    // the operand type, instances with room for it), 0 = written into TMEM
   int y_blocks;    // gate / residual with 16-bit out on CTA pairs: Y blocks per epilogue warp (1, 2)
+  int epi_warps;   // epilogue warps: 8, or 16 (single CTAs with one staged Y block per warp)
   int k_rows;      // CTA pairs: 128-byte K rows per ring stage (1, 2)
   int row_bars;    // k_rows 2: a full barrier per K row of a stage (B copied one K row at a time)
   int ab_bf16;     // operand (and Y) type: 0 = f16, 1 = bf16

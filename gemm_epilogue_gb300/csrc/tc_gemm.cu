@@ -48,8 +48,10 @@ namespace fgemm {
 namespace tc {
 
 constexpr int BM = 128, BN = 256;  // per-CTA rows, tile columns
-constexpr int EPI_WARPS = 8;  // two warpgroups: each owns half (128) of a tile's columns
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+// Epilogue warps: EW = 8 (two warpgroups, each owning half (128) of a tile's columns) or 16 (four
+// warpgroups of 64 columns each; single CTAs with a staged Y block per warp).  Threads per CTA:
+__host__ __device__ constexpr int threads_for(int ew) { return 64 + 32 * ew; }
+constexpr int THREADS = threads_for(8);  // the pair kernels
 // One K row of a stage is one 128-byte swizzle row per operand row: 64 16-bit or 128 fp8 elements.
 constexpr uint32_t A_ROW_BYTES = BM * 128;       // 16 KB: A's 128 rows x one K row
 constexpr uint32_t B_ROW_BYTES = 128 * 128;      // 16 KB: one K row of B for 128 columns
@@ -74,8 +76,10 @@ constexpr int MAX_STAGES = 6;
 // 64-column box).  ones x that tile = the bias in every row, exactly (16-bit bias, products by 1).
 constexpr uint32_t ONES_BYTES = 4096;             // 128 rows x 16 K of 16-bit ones
 constexpr uint32_t BIAS_BOX_BYTES = 16 * 128;     // 16 K rows x 64 columns of 16-bit values
-template <bool PAIR, bool YS = false, int YB = 1, int KSUB = 1, bool MB = false>
+template <bool PAIR, bool YS = false, int YB = 1, int KSUB = 1, bool MB = false, int EW = 8>
 struct Cfg {
+  static constexpr int EPI_WARPS = EW;
+  static constexpr int COLS_W = BN / (EW / 4);  // tile columns per epilogue warp
   static_assert(YB == 1 || (YB == 2 && YS) || (YB == 0 && PAIR && YS),
                 "Y staging variants: staged Y (chunk at a time on CTA pairs only)");
   static_assert(KSUB == 1 || KSUB == 2, "one or two K rows per stage");
@@ -84,7 +88,7 @@ struct Cfg {
   static constexpr uint32_t STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;
   // per epilogue warp: its 32 x 128 block of Y and results (YS), or one 32-row staging buffer
-  static constexpr uint32_t Y_BLOCK_BYTES = 2 * EPI_BUF_BYTES;  // a warp's 32 x 128 block of Y
+  static constexpr uint32_t Y_BLOCK_BYTES = (COLS_W / 64) * EPI_BUF_BYTES;  // a warp's block of Y
   // YB = 0 (staged Y): one 32 x 64 chunk of Y at a time per warp
   static constexpr uint32_t EPI_WARP_BYTES = YS ? (YB == 0 ? EPI_BUF_BYTES : YB * Y_BLOCK_BYTES) : EPI_BUF_BYTES;
   static constexpr uint32_t MB_BYTES = MB ? ONES_BYTES + (PAIR ? 2u : 4u) * BIAS_BOX_BYTES : 0u;
@@ -111,7 +115,7 @@ constexpr int BAR_ACC_FULL = 2 * MAX_STAGES;
 constexpr int BAR_ACC_EMPTY = 2 * MAX_STAGES + 2;
 constexpr int BAR_MMA_DONE = 2 * MAX_STAGES + 4;
 constexpr int BAR_Y = 2 * MAX_STAGES + 5;  // one per epilogue warp and Y block (staged Y)
-constexpr int BAR_BIAS_FULL = 2 * MAX_STAGES + 5 + 2 * 8;  // the staged bias row landed (MB)
+constexpr int BAR_BIAS_FULL = 2 * MAX_STAGES + 5 + 2 * 16;  // the staged bias row landed (MB)
 constexpr int BAR_BIAS_EMPTY = BAR_BIAS_FULL + 1;          // the bias MMA has read it
 constexpr uint32_t OFF_TMEM_SLOT = 8 * (BAR_BIAS_EMPTY + 1);
 constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 8;
@@ -183,8 +187,8 @@ __device__ __forceinline__ void bias_granule(const float (&b)[4], int j0, float 
 }
 
 template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1,
-          bool MB = false>
-__global__ void __launch_bounds__(THREADS, 1)
+          bool MB = false, int EW = 8>
+__global__ void __launch_bounds__(threads_for(EW), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmY,
                    const __grid_constant__ CUtensorMap tmBias, const TcParams p) {
@@ -193,7 +197,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int NG = CH / G;           // granules per chunk (8)
   // the gate's Y and the residual R are staged the same way (16-bit outputs)
   constexpr bool YS = (EPI == EPI_GATE || EPI == EPI_RESID) && (OUT_BYTES == 2);
-  using C = Cfg<PAIR, YS, YB, KSUB, MB>;
+  using C = Cfg<PAIR, YS, YB, KSUB, MB, EW>;
+  constexpr int EPI_WARPS = EW;
+  static_assert(EW == 8 || (EW == 16 && !PAIR && YS && YB == 1), "16 epilogue warps: single CTAs with one staged Y block");
   static_assert(!MB || !F8, "the bias MMA is a kind::f16 MMA");
   // Operand element size: one K row of a stage is one 128-byte swizzle row per A row (64 16-bit or
   // 128 fp8 elements); A arrives as KSUB boxes of 128 rows x one K row, B as boxes of (128 bytes
@@ -478,7 +484,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ew = warp - 2;
-    const int cbeg = (ew >> 2) * (BN / 2);  // first column (within the tile) of this warpgroup
+    const int cbeg = (ew >> 2) * C::COLS_W;  // first column (within the tile) of this warpgroup
     const uint32_t ebuf = sbase + SMEM_EPI + static_cast<uint32_t>(ew) * C::EPI_WARP_BYTES;
     const bool out_bf = p.out_type == ELEM_BF16;
     const bool y_bf = p.y_bf16 != 0;  // the gate's Y / the residual's R
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float bq[4];
         load_bias_quad(p, w.col0 + cbeg, bq);
 #pragma unroll 1
-        for (int c = cbeg; c < cbeg + BN / 2 && c < w.width; c += 16) {
+        for (int c = cbeg; c < cbeg + C::COLS_W && c < w.width; c += 16) {
           float b16[16];
           bias_granule<16>(bq, c - cbeg, b16);
           uint32_t r[16];
@@ -539,7 +545,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r0 = w.tm * C::TILE_M + static_cast<int>(rank) * BM + 32 * q;
         if (r0 >= p.M) return false;
         int nchunks = 0;
-        for (int c = cbeg; c < cbeg + BN / 2 && c < w.width; c += CH)
+        for (int c = cbeg; c < cbeg + C::COLS_W && c < w.width; c += CH)
           if (w.col0 + c < p.N) ++nchunks;
         if (nchunks == 0) return false;
         if (YHALF) nchunks = 1;
@@ -578,7 +584,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
         bool aborted = false;
 #pragma unroll 1
-        for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
+        for (int c = cbeg / CH; c < nch && c < (cbeg + C::COLS_W) / CH; ++c) {
           const int col0 = n0 + c * CH;
           if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
           if constexpr (YHALF) {
@@ -694,7 +700,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN);
 
 #pragma unroll 1
-      for (int c = cbeg / CH; c < nch && c < (cbeg + BN / 2) / CH; ++c) {
+      for (int c = cbeg / CH; c < nch && c < (cbeg + C::COLS_W) / CH; ++c) {
         const int col0 = n0 + c * CH;
         if (!rows_live || col0 >= p.N) break;  // warp-uniform; columns only grow with c
 
@@ -875,13 +881,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1,
-          bool MB = false>
+          bool MB = false, int EW = 8>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
                        const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p, int grid,
                        cudaStream_t s) {
-  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB, KSUB, MB>;
+  auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB, KSUB, MB, EW>;
   constexpr uint32_t smem =
-      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB, KSUB, MB>::SMEM_BYTES;
+      Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB, KSUB, MB, EW>::SMEM_BYTES;
   // Per device: the shared-memory opt-in is set once.  Host threads may race on a first call;
   // setting the attribute twice is harmless, and the flag is atomic.
   static std::atomic<bool> opted_in[64] = {};
@@ -894,7 +900,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads_for(EW)));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -957,6 +963,13 @@ cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const
     if (pair && p.y_blocks == 0)  // one 4 KB chunk of Y per warp
       return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, F8, 0, 2>(a, b, o, y, bm, p, grid, s)
                            : launch_one<EPI, OUT_BYTES, true, F8, 0, 1>(a, b, o, y, bm, p, grid, s);
+    // sixteen epilogue warps on single CTAs (one staged Y block each, 64 columns)
+    if (!pair && p.epi_warps == 16) {
+      if constexpr (!F8)
+        if (p.bias_init && p.bias_mma)
+          return launch_one<EPI, OUT_BYTES, false, false, 1, 1, true, 16>(a, b, o, y, bm, p, grid, s);
+      return launch_one<EPI, OUT_BYTES, false, F8, 1, 1, false, 16>(a, b, o, y, bm, p, grid, s);
+    }
     // the bias-initialised accumulator set by an extra MMA (room for its tiles in shared memory)
     if constexpr (!F8)
       if (p.bias_init && p.bias_mma && p.k_rows != 2)

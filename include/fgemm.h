@@ -152,6 +152,9 @@ typedef struct {
                      change tile scheduling": bands of group_m M-tiles walking N); 1 = the same
                      order with M and N exchanged (bands of group_m N-tiles walking M), which keeps
                      a band of B instead of A in L2 */
+  int epi_warps;  /* tensor-core path: epilogue warps per CTA: 0 = automatic (8), 8, or 16 (single
+                     CTAs with the gate or residual's Y staged one block per warp: four warps per
+                     TMEM lane quadrant, 64 columns each; else 8) */
 } fgemm_opts;
 
 /*
@@ -284,6 +287,7 @@ typedef struct {
   int bias_init;      /* tensor-core path: 0 = the bias is added after the reduction; 1 = the
                          accumulator starts at the bias, written by the epilogue warps; 2 = set by
                          the extra MMA (see fgemm_opts.bias_mma) */
+  int epi_warps;      /* tensor-core path: epilogue warps per CTA (see fgemm_opts.epi_warps) */
 } fgemm_plan_info;
 int fgemm_plan(const void* A, const void* B, const void* bias, const void* Y, const void* out,
                int64_t M, int64_t N, int64_t K, int dtype, int epilogue, const fgemm_opts* opts,

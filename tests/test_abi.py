@@ -117,7 +117,7 @@ def test_bad_options(lib):
     for field, val in (("group_m", -1), ("path", 9), ("split_k", 9), ("max_ctas", -3), ("timeout_ms", -1),
                        ("cta_pair", 3), ("tail_split", 2), ("skinny_tiles", 3), ("stages", 9),
                        ("inject_stall", 2), ("bias_init", 3), ("full_last_n", -1), ("y_blocks", 4),
-                       ("k_rows", 3), ("bias_mma", 3), ("bias_mma", -1), ("pdl", 3), ("raster", 2)):
+                       ("k_rows", 3), ("bias_mma", 3), ("bias_mma", -1), ("pdl", 3), ("raster", 2), ("epi_warps", 12)):
         o = fg.Opts()
         setattr(o, field, val)
         st = fg.call_status("fgemm_bias_relu_ex", 4096, 4096, 4096, 4096, 4, 4, 4, fg.F16, None,

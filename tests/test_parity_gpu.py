@@ -577,6 +577,42 @@ def test_staged_y_two_blocks_single_cta_integer_bit_exact(M, N, K, max_ctas):
             assert _same_values(down(res, ab), ref.out, ab)
 
 
+@pytest.mark.parametrize("M,N,K,max_ctas", [(300, 520, 200, 0), (700, 1800, 200, 44), (513, 1288, 64, 12),
+                                           (1000, 2056, 504, 0), (129, 264, 8, 0)])
+def test_sixteen_epilogue_warps_integer_bit_exact(M, N, K, max_ctas):
+    # Sixteen epilogue warps on single CTAs (four per TMEM lane quadrant, 64 columns each, one
+    # staged Y block per warp) for the gate and the residual, with the bias added after the sum,
+    # written into tensor memory, or set by the extra MMA; tail pieces and the narrowed last tile.
+    for bias_init, bias_mma in ((2, 0), (1, 1), (1, 2)):
+        opts = {"path": fg.PATH_TC, "cta_pair": 1, "max_ctas": max_ctas, "epi_warps": 16,
+                "bias_init": bias_init, "bias_mma": bias_mma}
+        for ab in (F16, BF16):
+            p = gen.integer_problem(M, N, K, ab, ab, seed=M + K + 3 * ab, gate=True)
+            plan = fg.fgemm_plan(up(p.A, ab), up(p.B, ab), up(p.bias, ab), up(p.Y, ab),
+                                 torch.empty(M, N, dtype=torch_dtype(ab), device="cuda"), M, N, K,
+                                 dtype_word(ab, ab, ab), gate=True, opts=opts)
+            assert (plan["cluster"], plan["epi_warps"]) == (1, 16)
+            out, path = run_fused(p, M, N, K, ab, ab, ab, gate=True, opts=opts)
+            assert path == fg.PATH_TC
+            assert _same_values(down(out, ab), oracle_run(p, M, N, K, ab, ab, ab, gate=True).out, ab)
+            res = torch.empty(M, N, dtype=torch_dtype(ab), device="cuda")
+            fg.fgemm_bias_residual_relu_ex(up(p.A, ab), up(p.B, ab), up(p.bias, ab), up(p.Y, ab),
+                                           res, M, N, K, dtype_word(ab, ab, ab), opts=opts)
+            torch.cuda.synchronize()
+            ref = oracle.bias_residual_relu(p.A, p.B, p.bias, p.Y, M, N, K, ab, ab, ab)
+            assert _same_values(down(res, ab), ref.out, ab)
+    # fp8 operands with a 16-bit Y
+    p = gen.integer_problem(M, N, K, E4M3, F32, seed=M + 11, gate=True, y_type=F16)
+    if N % 16 == 0 and K % 16 == 0:
+        out = torch.empty(M, N, dtype=torch.float16, device="cuda")
+        fg.fgemm_addmm_gate_ex(up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32), up(p.Y, F16), out, M, N,
+                               K, dtype_word(E4M3, F32, F16, F16),
+                               opts={"cta_pair": 1, "max_ctas": max_ctas, "epi_warps": 16})
+        torch.cuda.synchronize()
+        ref = oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, E4M3, F32, F16, y_type=F16)
+        assert _same_values(down(out, F16), ref.out, F16)
+
+
 def _same_values(got_bits, ref_bits, t):
     """Equal as numbers (-0 == +0), every element."""
     return np.array_equal(oracle.decode(got_bits, t), oracle.decode(ref_bits, t))
