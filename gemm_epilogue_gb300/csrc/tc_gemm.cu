@@ -21,8 +21,9 @@
 //               or less for the pieces of the last partial round and for the last column of tiles
 //               (narrowed to the columns left of N).  tcgen05.commit releases each smem stage
 //               (empty[s]) and hands a finished accumulator over (acc_full[b]).
-//   warps 2-9   epilogue, two warpgroups splitting the tile's columns: each warp owns the 32 TMEM
-//               lanes (rows) its warp id allows, reads its 128 bias values with one coalesced load
+//   warps 2-9   epilogue, two warpgroups splitting the tile's columns (or warps 2-17, four
+//               warpgroups of 64 columns, as an option for single CTAs with staged Y): each warp
+//               owns the 32 TMEM lanes (rows) its warp id allows, reads its bias with one coalesced load
 //               per work item (shuffled to the granules), and per 64-column chunk:
 //               tcgen05.ld -> + bias[j] -> ReLU (fmaxf), the gate fma(x, y, x), the residual, or
 //               the fp8 scale-and-clamp -> one round-to-nearest conversion -> 128-byte-swizzled
@@ -31,7 +32,8 @@
 //               (Epilogue Fusion)", "Pitfalls": after the K loop, masked with j < N), or, with the
 //               bias-initialised accumulator ("Optimizing GEMM + Activation on CDNA4 with TLX",
 //               V4; the default for short K loops), written into the free TMEM buffer before its
-//               tile's first MMA.  For the gate (and the residual add, "Variants") the second
+//               tile's first MMA, or set there by one extra MMA (a 128 x 16 tile of ones times a
+//               16-row tile whose first K row is the bias row, staged by TMA).  For the gate (and the residual add, "Variants") the second
 //               M x N operand is prefetched by TMA into the epilogue's own buffers while the main
 //               loop runs (a whole 8 KB block per warp a work item ahead, or one 4 KB chunk at a
 //               time on long K loops), and the result is written over it and stored from there;
@@ -492,7 +494,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
     const bool add_bias = !p.bias_init;  // else the accumulator already holds the bias
     // Bias-initialised accumulator ("Optimizing GEMM + Activation on CDNA4 with TLX", V4: the
     // accumulator starts at the bias instead of zero): this warp writes bias[col] into every lane
-    // (row) of its quarter and every column of its half of buffer bb for work item t, then hands
+    // (row) of its quarter and every column it owns of buffer bb for work item t, then hands
     // the buffer to the MMA warp, whose first MMA of the tile accumulates onto it.
     auto release_acc = [&](int t, int bb) {
       if (bias_tmem && t < p.num_items) {
