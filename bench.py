@@ -640,7 +640,13 @@ def run_sweep(args):
                         {"bias_init": 1}, {"bias_init": 2}]
         if args.sweep_variants:
             variants = json.loads(args.sweep_variants)
+        # Every variant is timed from a cool start: a second of back-to-back load lowers the SM
+        # clock (power cap) for a while after it ends, which would bias whichever variant came
+        # next.  So the half-second sustained timing of the defaults runs after all the short
+        # timings of the workload, and a pause follows every timing.
+        sustained = None
         for opts in variants:
+            time.sleep(args.sweep_cooldown)
             g = (opts or {}).get("group_m")
             try:
                 prob.plan(opts)
@@ -656,15 +662,21 @@ def run_sweep(args):
                  "path": fg.PATH_NAMES.get(path), "us": ms * 1e3, "us_stream_loop": ms_stream * 1e3,
                  "tflops": t, "gbs": gbs, "roofline_frac": t_roof / (ms * 1e-3),
                  "pct_bf16_peak": 100 * t / pk["bf16_tflops"], "pct_hbm": 100 * gbs / pk["hbm_gbs"]}
-            if opts is None:  # the defaults also as the bench line times them: half a second
-                ms_s, _, reps, _ = time_steps_graph(prob, min(steps, 20), 3, stream, opts=opts,
-                                                     min_seconds=0.5)
-                r["us_sustained"] = ms_s * 1e3
-                r["roofline_frac_sustained"] = max(
-                    w.flops / (tensor_peak(pk, w, True) * 1e12),
-                    w.unavoidable_bytes() / (pk["hbm_gbs"] * 1e9)) / (ms_s * 1e-3)
+            if opts is None:
+                sustained = r
             results.append(r)
             print(json.dumps(r), file=sys.stderr, flush=True)
+        if sustained is not None:  # the defaults also as the bench line times them: half a second
+            time.sleep(args.sweep_cooldown)
+            ms_s, _, reps, _ = time_steps_graph(prob, min(steps, 20), 3, stream, opts=None,
+                                                 min_seconds=0.5)
+            sustained["us_sustained"] = ms_s * 1e3
+            sustained["roofline_frac_sustained"] = max(
+                w.flops / (tensor_peak(pk, w, True) * 1e12),
+                w.unavoidable_bytes() / (pk["hbm_gbs"] * 1e9)) / (ms_s * 1e-3)
+            print(json.dumps({"workload": name, "us_sustained": sustained["us_sustained"]}),
+                  file=sys.stderr, flush=True)
+            time.sleep(2 * args.sweep_cooldown)
         if unf:
             ms, _ = time_steps(prob, steps, 3, stream, unfused=True)
             r = {"workload": name, "variant": "unfused", "us": ms * 1e3,
@@ -703,6 +715,8 @@ def main():
                     help="also write the sweep's results as one JSON file at this path")
     ap.add_argument("--sweep-cpu", action="store_true",
                     help="also time the fp64 oracle on a bounded sample of every swept workload")
+    ap.add_argument("--sweep-cooldown", type=float, default=1.0,
+                    help="seconds of idle GPU before each sweep timing (clock recovery)")
     ap.add_argument("--sweep-variants", default="",
                     help='JSON list of fgemm_opts dicts (null = defaults) replacing the sweep\'s own')
     args = ap.parse_args()

@@ -376,16 +376,16 @@ SkPlan plan_skinny(const Call& c, const DevShape& d) {
   return s;
 }
 
-// Programmatic dependent launch (fgemm_opts.pdl): automatic for the short kernels, where the
-// launch gap and set-up between consecutive kernels (about 1.5 us) is a visible share.  Measured
-// on one GB300, CUDA-graph replay of back-to-back calls: GLU block M = 1024, N = 21568, K = 256 /
-// 512 / 1024: 26.1 -> 25.4, 35.8 -> 34.8, 43.8 -> 41.8 us; skinny N = K = 8192, M = 1 / 128:
-// 24.5 -> 24.0, 29.4 -> 28.6 us.  With long K loops it measured slower (4096^3 80.4 -> 82-84.5 us,
-// GLU block K = 4096 124.5 -> 132 us), so it stays off there.
-int pdl_of(const Call& c, bool skinny) {
+// Programmatic dependent launch (fgemm_opts.pdl), on by default on both paths: the launch gap
+// and set-up between consecutive kernels (about 1.5 us) overlap the previous kernel's last CTAs.
+// Measured on one GB300, CUDA-graph replay of back-to-back calls, each variant timed after a
+// second of idle GPU: GLU block M = 1024, N = 21568, K = 256 / 512 / 1024 25.5 -> 24.9,
+// 35.3 -> 34.5, 43.2 -> 41.8 us; 4096^3 80.3 -> 79.6 us, fp8 4096^3 48.0 -> 46.7 us, fp8 GLU block
+// K = 4096 67.8 -> 66.4 us, FFN 8192 x 14336 x 4096 551.6 -> 547.5 us; skinny N = K = 8192,
+// M = 1 / 128 24.5 -> 24.0, 29.4 -> 28.6 us.
+int pdl_of(const Call& c) {
   const int want = c.opts ? c.opts->pdl : 0;
-  if (want != 0) return want == 1 ? 1 : 0;
-  return (skinny || c.K <= 1024) ? 1 : 0;
+  return want == 2 ? 0 : 1;
 }
 
 int run_tc(const Call& c, DeviceInfo* d) {
@@ -443,7 +443,7 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
   p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
-  p.pdl = pdl_of(c, false);
+  p.pdl = pdl_of(c);
   return status_of(
       launch_tc(c.epi, tmA, tmB, tmO, tmY, tmBias, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
 }
@@ -479,7 +479,7 @@ int run_skinny(const Call& c, DeviceInfo* d) {
   p.timeout_ns = static_cast<uint64_t>(tmo_ms) * 1000000ull;
   p.err = d->err;
   p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
-  p.pdl = pdl_of(c, true);
+  p.pdl = pdl_of(c);
   if (!skinny_fits(s.mpad, s.nt, s.split, s.stages)) return FGEMM_ERR_INVALID_VALUE;
   return status_of(launch_skinny(c.epi, tmB, tmA, p, s.groups * s.split, c.stream));
 }

@@ -146,8 +146,8 @@ typedef struct {
                      the kernel's set-up (barriers, tensor memory) may run while the previous
                      kernel in the stream is finishing, and the kernel waits for that kernel to
                      complete (griddepcontrol.wait) before its first access to global memory, so a
-                     dependency between the two stays safe.  0 = automatic (on for the skinny path
-                     and for K <= 1024), 1 = on, 2 = off */
+                     dependency between the two stays safe.  0 = automatic (on), 1 = on,
+                     2 = off */
   int raster;     /* tensor-core path: 0 = the grouped order over M ("I3. Fuse a GEMM epilogue and
                      change tile scheduling": bands of group_m M-tiles walking N); 1 = the same
                      order with M and N exchanged (bands of group_m N-tiles walking M), which keeps

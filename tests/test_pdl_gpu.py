@@ -1,8 +1,7 @@
-"""Programmatic dependent launch (fgemm_opts.pdl, on by default for short K loops and the skinny
-path): a call's set-up may overlap the previous kernel, but its first global-memory access waits
-for that kernel to complete.  A chain in which
-each call reads the previous call's output must therefore give the oracle's result, launched one
-by one and from a captured CUDA graph."""
+"""Programmatic dependent launch (fgemm_opts.pdl, on by default): a call's set-up may overlap the
+previous kernel, but its first global-memory access waits for that kernel to complete.  A chain in
+which each call reads the previous call's output must therefore give the oracle's result, launched
+one by one and from a captured CUDA graph."""
 import numpy as np
 import pytest
 
@@ -29,8 +28,9 @@ def built():
     assert fg.fgemm_device_status() == 0
 
 
-# tensor-core pairs, tensor-core single CTAs, skinny
-CASES = [(700, 1800, 1024, {"cta_pair": 2}), (300, 520, 200, {"cta_pair": 1}), (16, 1032, 512, {})]
+# tensor-core pairs (a short and a long K loop), tensor-core single CTAs, skinny
+CASES = [(700, 1800, 1024, {"cta_pair": 2}), (520, 1032, 2112, {}), (300, 520, 200, {"cta_pair": 1}),
+         (16, 1032, 512, {})]
 
 
 @pytest.mark.parametrize("M,N,K,sel", CASES)
@@ -43,7 +43,7 @@ def test_chain_reads_the_previous_output(M, N, K, sel, graph, pdl):
     A, B, bias = up(p.A, BF16), up(p.B, BF16), up(p.bias, BF16)
     out1 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     out2 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
-    opts = dict(sel, pdl=pdl)  # 0: the automatic choice, which is on for these short K loops
+    opts = dict(sel, pdl=pdl)  # 0: the automatic choice, which is on
     stream = torch.cuda.Stream()
 
     def chain():
