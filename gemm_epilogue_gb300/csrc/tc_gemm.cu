@@ -297,12 +297,42 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   if (PAIR) cluster_sync();  // the peer signals the even CTA's barriers: both must be initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int num_kb = (p.K + KB_ELEMS - 1) / KB_ELEMS;
   // Up to here only this CTA's shared and tensor memory were touched; with programmatic
   // dependent launch that set-up overlaps the previous kernel in the stream, and global memory is
-  // touched only after it has completed.
+  // read only after it has completed.  Single CTAs prefetch their first work item into L2 before
+  // that -- the first ring stages' operands (up to two rings' worth) and the warps' first Y --
+  // in the time the previous kernel's last CTAs leave: a prefetch only moves lines into L2, which
+  // stays coherent with whatever that kernel still writes.  Measured on one GB300 (graph replay,
+  // alternating builds): GLU block M = 1024, N = 21568, K = 256 / 512 (single CTAs) 25.6 -> 25.1,
+  // 35.0 -> 34.1 us; on CTA pairs it measured slower (K = 1024 42.4 -> 43.6 us, 4096^3 80.9 ->
+  // 81.5 us), so pairs do not prefetch.
+  if (!PAIR && p.pdl && unit < p.num_items) {
+    const Work w0 = work_of(p, unit);
+    if (warp == 0 && lane == 0) {
+      const int m0 = w0.tm * C::TILE_M + static_cast<int>(rank) * BM;
+      const int cols = PAIR ? w0.width / 2 : w0.width;
+      const int nb0 = w0.col0 + static_cast<int>(rank) * cols;
+      const int boxes = (cols + BOXC - 1) / BOXC;
+      const int nkb = num_kb < 2 * STAGES ? num_kb : 2 * STAGES;
+      for (int kb = 0; kb < nkb; ++kb)
+        for (int r = 0; r < KSUB; ++r) {
+          const int kx = kb * KB_ELEMS + r * KROW;
+          tma_prefetch_2d(&tmA, kx, m0);
+          if (rowbar || r == 0)
+            for (int c = 0; c < boxes; ++c) tma_prefetch_2d(&tmB, nb0 + BOXC * c, kx);
+        }
+    }
+    if (YS && warp >= 2 && warp < 2 + EPI_WARPS && lane == 0) {
+      const int cb = ((warp - 2) >> 2) * C::COLS_W;
+      const int r0 = w0.tm * C::TILE_M + static_cast<int>(rank) * BM + 32 * (warp & 3);
+      if (r0 < p.M)
+        for (int c = cb; c < cb + C::COLS_W && c < w0.width; c += 64)
+          if (w0.col0 + c < p.N) tma_prefetch_2d(&tmY, w0.col0 + c, r0);
+    }
+  }
   grid_dependency_wait();
 
-  const int num_kb = (p.K + KB_ELEMS - 1) / KB_ELEMS;
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
@@ -318,6 +348,10 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       uint32_t bias_items = 0;  // bias rows copied (bias MMA)
       bool ok = true;
       for (int t = unit; ok && t < p.num_items; t += units) {
+        // This CTA's last work item: the next kernel in the stream may launch (its CTAs become
+        // resident as this kernel's CTAs exit and prefetch their first data while the others
+        // finish; it reads global memory only after this kernel has completed).
+        if (t + units >= p.num_items) grid_dependents_launch();
         const Work wk = work_of(p, t);
         const int m0 = wk.tm * C::TILE_M + static_cast<int>(rank) * BM;
         // each CTA of a pair stages half of the piece's columns
@@ -869,8 +903,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   }
 
   // ------------------------------------------------------------ teardown
-  // The next kernel in the stream may begin its set-up (measured: letting it start as soon as
-  // this kernel has begun gains nothing on short K loops and slows the skinny kernel at M = 1).
+  // (also here, for a CTA without work items)
   grid_dependents_launch();
   tc_fence_before();
   __syncthreads();
