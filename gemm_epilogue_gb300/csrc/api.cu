@@ -135,7 +135,8 @@ CUtensorMapDataType tma_type(int e) {
 
 // Row-major matrix of `rows` x `cols` elements; box of box_rows x box_cols, 128-byte swizzle.
 bool encode_2d(CUtensorMap* m, int elem, const void* base, int64_t rows, int64_t cols,
-               uint32_t box_rows, uint32_t box_cols) {
+               uint32_t box_rows, uint32_t box_cols,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -143,7 +144,7 @@ bool encode_2d(CUtensorMap* m, int elem, const void* base, int64_t rows, int64_t
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, tma_type(elem), 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -265,9 +266,10 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
   const bool allow = !(c.opts && c.opts->tail_split == 1);
   if (allow && rem > 0 && t.num_tiles > units) {
     // fp8 outputs are stored 128 columns at a time: pieces stay >= 128 columns wide; fp8
-    // operands stage B in 128-column boxes per CTA: pieces stay >= 128 columns per CTA
+    // operands stage B in 128-column boxes per CTA, so single CTAs keep pieces of >= 128
+    // columns, and pairs' 128-column pieces (64 per CTA) take B as 64-byte-swizzled boxes
     int max_split = (t.pair || c.t.out == ELEM_E4M3) ? 2 : 4;
-    if (c.t.ab == ELEM_E4M3) max_split = t.pair ? 1 : 2;
+    if (c.t.ab == ELEM_E4M3 && !t.pair) max_split = 2;
     while (split * 2 <= max_split && rem * split * 2 <= units) split *= 2;
   }
   t.tail_split = split;
@@ -408,6 +410,12 @@ int run_tc(const Call& c, DeviceInfo* d) {
   }
   CUtensorMap tmBias = tmO;  // unused unless the bias MMA runs
   if (t.bias_mma && !encode_2d(&tmBias, c.t.bias, c.bias, 1, c.N, 1, 64)) return FGEMM_ERR_LAUNCH;
+  CUtensorMap tmB64 = tmB;  // fp8 pairs' column pieces: 64-column, 64-byte-swizzled B boxes
+  if (t.pair && c.t.ab == ELEM_E4M3 && t.tail_split > 1 &&
+      !encode_2d(&tmB64, c.t.ab, c.B, c.K, c.N,
+                 kb_elems * static_cast<uint32_t>(t.row_bars ? 1 : t.k_rows), 64,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
+    return FGEMM_ERR_LAUNCH;
   TcParams p{};
   p.M = static_cast<int>(c.M);
   p.N = static_cast<int>(c.N);
@@ -445,7 +453,8 @@ int run_tc(const Call& c, DeviceInfo* d) {
   p.inject_stall = (c.opts && c.opts->inject_stall) ? 1 : 0;
   p.pdl = pdl_of(c);
   return status_of(
-      launch_tc(c.epi, tmA, tmB, tmO, tmY, tmBias, p, t.units * (t.pair ? 2 : 1), t.pair, c.stream));
+      launch_tc(c.epi, tmA, tmB, tmO, tmY, tmBias, tmB64, p, t.units * (t.pair ? 2 : 1), t.pair,
+                c.stream));
 }
 
 int run_skinny(const Call& c, DeviceInfo* d) {

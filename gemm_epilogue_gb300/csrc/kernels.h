@@ -68,9 +68,12 @@ struct SimtParams {
 // tmY: the gate's Y (M x N, operand type, 32 x 64 boxes, 128-byte swizzle); any map otherwise.
 // tmBias: the bias as a 1 x N tensor (64-column boxes, 128-byte swizzle) for the bias MMA; any
 // map otherwise.
+// tmB64: fp8 operands on CTA pairs, B as 64-column boxes with 64-byte swizzle (the column pieces
+// of the last round, 64 columns per CTA); any map otherwise.
 cudaError_t launch_tc(int epi, const CUtensorMap& tmA, const CUtensorMap& tmB,
                       const CUtensorMap& tmOut, const CUtensorMap& tmY, const CUtensorMap& tmBias,
-                      const TcParams& p, int grid, bool pair, cudaStream_t s);
+                      const CUtensorMap& tmB64, const TcParams& p, int grid, bool pair,
+                      cudaStream_t s);
 // How many CTA pairs of the pair-mode kernel can be resident at once (clusters need two free SMs
 // in one GPC); cached per process.
 int tc_max_active_pairs(int epi, int out_type);

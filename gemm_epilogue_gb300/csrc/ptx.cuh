@@ -248,6 +248,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same for a 64-byte-swizzled tile (8-row x 64-byte swizzle atoms, 512 bytes each).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(4) << 61;
+  return d;
+}
+
 // Shared-memory matrix descriptor for a tile without swizzle, made of 8-row x 16-byte core
 // matrices (each 128 contiguous bytes): lbo = byte distance between core matrices adjacent along
 // K, sbo = byte distance between core matrices adjacent along M / N (layout field 0).

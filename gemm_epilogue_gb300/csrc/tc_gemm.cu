@@ -193,7 +193,8 @@ template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KS
 __global__ void __launch_bounds__(threads_for(EW), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmY,
-                   const __grid_constant__ CUtensorMap tmBias, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmBias,
+                   const __grid_constant__ CUtensorMap tmB64, const TcParams p) {
   constexpr int CH = 128 / OUT_BYTES;  // output columns per 128-byte staging row
   constexpr int G = 16 / OUT_BYTES;    // columns per 16-byte granule
   constexpr int NG = CH / G;           // granules per chunk (8)
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (F8 && PAIR && p.tail_split > 1) tma_prefetch_desc(&tmB64);
     tma_prefetch_desc(&tmOut);
     if (YS) tma_prefetch_desc(&tmY);
   }
@@ -381,9 +383,12 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
           ++bias_items;
           return true;
         };
+        // fp8 operands on pairs, a column piece (64 columns per CTA): B as one 64-byte-wide box
+        // per K row set with 64-byte swizzle (tmB64), half a 128-byte box's bytes
+        const bool b64 = F8 && PAIR && cols == 64;
+        const uint32_t b_bytes = b64 ? BBOX_ROW / 2 : static_cast<uint32_t>(boxes) * BBOX_ROW;
         // bytes per full barrier: one K row, or the whole stage (both CTAs of a pair)
-        const uint32_t tx = (PAIR ? 2u : 1u) * (A_ROW_BYTES + static_cast<uint32_t>(boxes) * BBOX_ROW) *
-                            static_cast<uint32_t>(KSUB / nfb);
+        const uint32_t tx = (PAIR ? 2u : 1u) * (A_ROW_BYTES + b_bytes) * static_cast<uint32_t>(KSUB / nfb);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(bar(BAR_EMPTY + stage), phase ^ 1u, abort_flag, tmo, p.err,
                          SITE_PROD_EMPTY)) {
@@ -408,9 +413,13 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
             } else if constexpr (PAIR) {
               const uint32_t lfb = lead_bar(fi);
               tma_load_2d_pair(a_dst + r * A_ROW_BYTES, &tmA, lfb, kx, m0, pol_a);
-              if (b_now)
-                for (int c = 0; c < boxes; ++c)
-                  tma_load_2d_pair(b_dst + c * BBOX + b_off, &tmB, lfb, nb0 + BOXC * c, kx, pol_b);
+              if (b_now) {
+                if (b64)  // K rows of 64 bytes: a K row set of the stage every BBOX_ROW / 2
+                  tma_load_2d_pair(b_dst + b_off / 2, &tmB64, lfb, nb0, kx, pol_b);
+                else
+                  for (int c = 0; c < boxes; ++c)
+                    tma_load_2d_pair(b_dst + c * BBOX + b_off, &tmB, lfb, nb0 + BOXC * c, kx, pol_b);
+              }
             } else {
               tma_load_2d(a_dst + r * A_ROW_BYTES, &tmA, bar(fi), kx, m0, pol_a);
               if (b_now)
@@ -452,6 +461,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
       for (int t = unit; ok && t < p.num_items; t += units, ++it) {
         // MMA N = the piece's width (all tiles but the tail pieces: 256)
         const int width = work_of(p, t).width;
+        // fp8 pairs' column pieces: B in 64-byte-swizzled K rows (8 rows x 64 bytes per atom)
+        const bool b64 = F8 && PAIR && width == 128;
         const uint32_t idesc = (p.idesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(width >> 3) << 17);
         const int b = it & 1;
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
@@ -493,8 +504,10 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
             for (int k = r * KPR; k < (r + 1) * KPR; ++k) {  // 32 bytes of K per MMA
               const uint64_t ad =
                   sdesc_sw128(a_addr + (k / KPR) * A_ROW_BYTES + 32u * (k % KPR), 16u, 1024u);
-              // MN-major B: one column box (BBOX bytes) apart along N, 1 KB per 8 K rows
-              const uint64_t bd = sdesc_sw128(b_addr + B_KADV * k, BBOX, 1024u);
+              // MN-major B: one column box (BBOX bytes) apart along N, 1 KB per 8 K rows (or, for
+              // the 64-byte-wide boxes, one atom along N and 512 bytes per 8 K rows)
+              const uint64_t bd = b64 ? sdesc_sw64(b_addr + (B_KADV / 2) * k, BBOX, 512u)
+                                      : sdesc_sw128(b_addr + B_KADV * k, BBOX, 1024u);
               const uint32_t acc = (p.bias_init | kb | k) != 0 ? 1u : 0u;  // bias: already in D
               if constexpr (F8)
                 umma_f8_cg<CG>(d_tmem, ad, bd, idesc, acc);
@@ -918,8 +931,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
 template <int EPI, int OUT_BYTES, bool PAIR, bool F8 = false, int YB = 1, int KSUB = 1,
           bool MB = false, int EW = 8>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                       const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p, int grid,
-                       cudaStream_t s) {
+                       const CUtensorMap& y, const CUtensorMap& bm, const CUtensorMap& b64,
+                       const TcParams& p, int grid, cudaStream_t s) {
   auto k = tc_gemm_kernel<EPI, OUT_BYTES, PAIR, F8, YB, KSUB, MB, EW>;
   constexpr uint32_t smem =
       Cfg<PAIR, (EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2, YB, KSUB, MB, EW>::SMEM_BYTES;
@@ -947,7 +960,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, o, y, bm, p);
+  return cudaLaunchKernelEx(&cfg, k, a, b, o, y, bm, b64, p);
 }
 
 // A persistent grid must be co-resident: clusters of two need two free SMs in one GPC, so the
@@ -989,31 +1002,31 @@ int max_pairs() {
 
 template <int EPI, int OUT_BYTES, bool F8 = false>
 cudaError_t launch_pair_or_not(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                               const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p,
-                               int grid, bool pair, cudaStream_t s) {
+                               const CUtensorMap& y, const CUtensorMap& bm, const CUtensorMap& b64,
+                               const TcParams& p, int grid, bool pair, cudaStream_t s) {
   if constexpr ((EPI == EPI_GATE || EPI == EPI_RESID) && OUT_BYTES == 2) {
     if (p.y_blocks == 2)
-      return pair ? launch_one<EPI, OUT_BYTES, true, F8, 2>(a, b, o, y, bm, p, grid, s)
-                  : launch_one<EPI, OUT_BYTES, false, F8, 2>(a, b, o, y, bm, p, grid, s);
+      return pair ? launch_one<EPI, OUT_BYTES, true, F8, 2>(a, b, o, y, bm, b64, p, grid, s)
+                  : launch_one<EPI, OUT_BYTES, false, F8, 2>(a, b, o, y, bm, b64, p, grid, s);
     if (pair && p.y_blocks == 0)  // one 4 KB chunk of Y per warp
-      return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, F8, 0, 2>(a, b, o, y, bm, p, grid, s)
-                           : launch_one<EPI, OUT_BYTES, true, F8, 0, 1>(a, b, o, y, bm, p, grid, s);
+      return p.k_rows == 2 ? launch_one<EPI, OUT_BYTES, true, F8, 0, 2>(a, b, o, y, bm, b64, p, grid, s)
+                           : launch_one<EPI, OUT_BYTES, true, F8, 0, 1>(a, b, o, y, bm, b64, p, grid, s);
     // sixteen epilogue warps on single CTAs (one staged Y block each, 64 columns)
     if (!pair && p.epi_warps == 16) {
       if constexpr (!F8)
         if (p.bias_init && p.bias_mma)
-          return launch_one<EPI, OUT_BYTES, false, false, 1, 1, true, 16>(a, b, o, y, bm, p, grid, s);
-      return launch_one<EPI, OUT_BYTES, false, F8, 1, 1, false, 16>(a, b, o, y, bm, p, grid, s);
+          return launch_one<EPI, OUT_BYTES, false, false, 1, 1, true, 16>(a, b, o, y, bm, b64, p, grid, s);
+      return launch_one<EPI, OUT_BYTES, false, F8, 1, 1, false, 16>(a, b, o, y, bm, b64, p, grid, s);
     }
     // the bias-initialised accumulator set by an extra MMA (room for its tiles in shared memory)
     if constexpr (!F8)
       if (p.bias_init && p.bias_mma && p.k_rows != 2)
-        return pair ? launch_one<EPI, OUT_BYTES, true, false, 1, 1, true>(a, b, o, y, bm, p, grid, s)
-                    : launch_one<EPI, OUT_BYTES, false, false, 1, 1, true>(a, b, o, y, bm, p, grid, s);
+        return pair ? launch_one<EPI, OUT_BYTES, true, false, 1, 1, true>(a, b, o, y, bm, b64, p, grid, s)
+                    : launch_one<EPI, OUT_BYTES, false, false, 1, 1, true>(a, b, o, y, bm, b64, p, grid, s);
   }
-  if (pair && p.k_rows == 2) return launch_one<EPI, OUT_BYTES, true, F8, 1, 2>(a, b, o, y, bm, p, grid, s);
-  return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, bm, p, grid, s)
-              : launch_one<EPI, OUT_BYTES, false, F8>(a, b, o, y, bm, p, grid, s);
+  if (pair && p.k_rows == 2) return launch_one<EPI, OUT_BYTES, true, F8, 1, 2>(a, b, o, y, bm, b64, p, grid, s);
+  return pair ? launch_one<EPI, OUT_BYTES, true, F8>(a, b, o, y, bm, b64, p, grid, s)
+              : launch_one<EPI, OUT_BYTES, false, F8>(a, b, o, y, bm, b64, p, grid, s);
 }
 
 }  // namespace tc
@@ -1033,32 +1046,32 @@ int tc_block_m() { return tc::BM; }
 int tc_block_n() { return tc::BN; }
 
 cudaError_t launch_tc(int epi, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& o,
-                      const CUtensorMap& y, const CUtensorMap& bm, const TcParams& p, int grid,
-                      bool pair, cudaStream_t s) {
+                      const CUtensorMap& y, const CUtensorMap& bm, const CUtensorMap& b64,
+                      const TcParams& p, int grid, bool pair, cudaStream_t s) {
   const bool f32 = p.out_type == ELEM_F32;
   if (p.ab_f8) {  // fp8 operands: bias + ReLU, the gate and the residual (16-bit / fp32 out),
                   // and the quantized epilogue
-    if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1, true>(a, b, o, y, bm, p, grid, pair, s);
+    if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1, true>(a, b, o, y, bm, b64, p, grid, pair, s);
     switch (epi) {
-      case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4, true>(a, b, o, y, bm, p, grid, pair, s)
-                                : tc::launch_pair_or_not<EPI_RELU, 2, true>(a, b, o, y, bm, p, grid, pair, s);
-      case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4, true>(a, b, o, y, bm, p, grid, pair, s)
-                                : tc::launch_pair_or_not<EPI_GATE, 2, true>(a, b, o, y, bm, p, grid, pair, s);
-      case EPI_RESID: return f32 ? tc::launch_pair_or_not<EPI_RESID, 4, true>(a, b, o, y, bm, p, grid, pair, s)
-                                 : tc::launch_pair_or_not<EPI_RESID, 2, true>(a, b, o, y, bm, p, grid, pair, s);
+      case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4, true>(a, b, o, y, bm, b64, p, grid, pair, s)
+                                : tc::launch_pair_or_not<EPI_RELU, 2, true>(a, b, o, y, bm, b64, p, grid, pair, s);
+      case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4, true>(a, b, o, y, bm, b64, p, grid, pair, s)
+                                : tc::launch_pair_or_not<EPI_GATE, 2, true>(a, b, o, y, bm, b64, p, grid, pair, s);
+      case EPI_RESID: return f32 ? tc::launch_pair_or_not<EPI_RESID, 4, true>(a, b, o, y, bm, b64, p, grid, pair, s)
+                                 : tc::launch_pair_or_not<EPI_RESID, 2, true>(a, b, o, y, bm, b64, p, grid, pair, s);
       default: return cudaErrorNotSupported;
     }
   }
-  if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1>(a, b, o, y, bm, p, grid, pair, s);
+  if (epi == EPI_QUANT) return tc::launch_pair_or_not<EPI_QUANT, 1>(a, b, o, y, bm, b64, p, grid, pair, s);
   switch (epi) {
-    case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, y, bm, p, grid, pair, s)
-                              : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, y, bm, p, grid, pair, s);
-    case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4>(a, b, o, y, bm, p, grid, pair, s)
-                              : tc::launch_pair_or_not<EPI_GATE, 2>(a, b, o, y, bm, p, grid, pair, s);
-    case EPI_RESID: return f32 ? tc::launch_pair_or_not<EPI_RESID, 4>(a, b, o, y, bm, p, grid, pair, s)
-                               : tc::launch_pair_or_not<EPI_RESID, 2>(a, b, o, y, bm, p, grid, pair, s);
-    default: return f32 ? tc::launch_pair_or_not<EPI_NONE, 4>(a, b, o, y, bm, p, grid, pair, s)
-                        : tc::launch_pair_or_not<EPI_NONE, 2>(a, b, o, y, bm, p, grid, pair, s);
+    case EPI_RELU: return f32 ? tc::launch_pair_or_not<EPI_RELU, 4>(a, b, o, y, bm, b64, p, grid, pair, s)
+                              : tc::launch_pair_or_not<EPI_RELU, 2>(a, b, o, y, bm, b64, p, grid, pair, s);
+    case EPI_GATE: return f32 ? tc::launch_pair_or_not<EPI_GATE, 4>(a, b, o, y, bm, b64, p, grid, pair, s)
+                              : tc::launch_pair_or_not<EPI_GATE, 2>(a, b, o, y, bm, b64, p, grid, pair, s);
+    case EPI_RESID: return f32 ? tc::launch_pair_or_not<EPI_RESID, 4>(a, b, o, y, bm, b64, p, grid, pair, s)
+                               : tc::launch_pair_or_not<EPI_RESID, 2>(a, b, o, y, bm, b64, p, grid, pair, s);
+    default: return f32 ? tc::launch_pair_or_not<EPI_NONE, 4>(a, b, o, y, bm, b64, p, grid, pair, s)
+                        : tc::launch_pair_or_not<EPI_NONE, 2>(a, b, o, y, bm, b64, p, grid, pair, s);
   }
 }
 

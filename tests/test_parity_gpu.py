@@ -358,6 +358,46 @@ def test_fp8_operands_integer_bit_exact(M, N, K, opts, want_path):
             pytest.fail(f"{len(bad)} mismatches, first at {bad[:5].tolist()}")
 
 
+# fp8 operands on CTA pairs with the last round cut into 128-column pieces: 64 columns of B per
+# CTA, staged as 64-byte-swizzled boxes (M, N, K, grid cap, epilogue)
+FP8_PIECE_CASES = [(1280, 1024, 2048, 16, "relu"), (1000, 848, 1152, 10, "relu"),
+                   (1280, 1024, 1024, 16, "gate"), (777, 1296, 1344, 14, "quant")]
+
+
+@pytest.mark.parametrize("M,N,K,mc,epi", FP8_PIECE_CASES)
+def test_fp8_pair_column_pieces_integer_bit_exact(M, N, K, mc, epi):
+    opts = {"cta_pair": 2, "max_ctas": mc}
+    gate = epi == "gate"
+    p = gen.integer_problem(M, N, K, E4M3, F32, seed=M + N, gate=gate, y_type=F16 if gate else None)
+    A, B, bias = up(p.A, E4M3), up(p.B, E4M3), up(p.bias, F32)
+    if epi == "quant":
+        ot, word = E4M3, fg.E4M3 | fg.BIAS_F32 | fg.OUT_E4M3
+    else:
+        ot = F16 if gate else BF16
+        word = dtype_word(E4M3, F32, ot, F16 if gate else None)
+    Y = up(p.Y, F16) if gate else None
+    probe = torch.empty(M, N, dtype=torch.uint8 if ot == E4M3 else torch_dtype(ot), device="cuda")
+    plan = fg.fgemm_plan(A, B, bias, Y, probe, M, N, K, word, gate=gate, opts=opts,
+                         epilogue=fg.EPI_RELU_QUANT if epi == "quant" else None)
+    assert plan["cluster"] == 2 and plan["tail_split"] == 2, plan
+    out, buf = guarded_out(M, N, ot)
+    if gate:
+        fg.fgemm_addmm_gate_ex(A, B, bias, Y, out, M, N, K, word, opts=opts)
+        ref = oracle.addmm_gate(p.A, p.B, p.bias, p.Y, M, N, K, E4M3, F32, ot, y_type=F16)
+    elif epi == "quant":
+        fg.fgemm_bias_relu_quant_ex(A, B, bias, out, M, N, K, word, 0.5, opts=opts)
+        ref = oracle.bias_relu_quant(p.A, p.B, p.bias, M, N, K, E4M3, F32, 0.5)
+    else:
+        fg.fgemm_bias_relu_ex(A, B, bias, out, M, N, K, word, opts=opts)
+        ref = oracle.bias_relu(p.A, p.B, p.bias, M, N, K, E4M3, F32, ot)
+    torch.cuda.synchronize()
+    check_guarded(buf, M, N, ot, epi)
+    got = down(out, ot)
+    if not _same_values(got, ref.out, ot):
+        bad = np.argwhere(got != ref.out)
+        pytest.fail(f"{epi}: {len(bad)} mismatches, first at {bad[:5].tolist()}")
+
+
 def test_fp8_operands_quantized_output_bit_exact():
     M, N, K = 300, 528, 256
     p = gen.integer_problem(M, N, K, E4M3, F32, seed=9)

@@ -76,9 +76,10 @@ def test_gate_glu_block_short_k():
 def test_fp8_operands():
     word = fg.E4M3 | fg.BIAS_F32 | fg.OUT_BF16
     p = plan(4096, 4096, 4096, word)
-    # fp8 operands on pairs stage B in 128-column boxes per CTA: no tail pieces (256 items);
-    # two 128-element K rows per stage, each on its own full barrier
-    assert (p["path"], p["cluster"], p["tail_split"], p["work_items"]) == (fg.PATH_TC, 2, 1, 256)
+    # fp8 operands on pairs: the 28 tiles of the last round are cut in two like 16-bit operands'
+    # (64 columns of B per CTA, in 64-byte-swizzled boxes): 228 + 56 = 284 items; two
+    # 128-element K rows per stage, each on its own full barrier
+    assert (p["path"], p["cluster"], p["tail_split"], p["work_items"]) == (fg.PATH_TC, 2, 2, 284)
     assert (p["k_rows"], p["row_barriers"]) == (2, 1)
     # decode-like shapes with fp8 operands take the swap-AB skinny kernel as well: 128 K elements
     # per stage, so the same K split over the cluster as 16-bit operands with half the K
