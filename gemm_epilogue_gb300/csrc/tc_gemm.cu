@@ -916,7 +916,8 @@ __global__ void __launch_bounds__(threads_for(EW), 1)
   }
 
   // ------------------------------------------------------------ teardown
-  // (also here, for a CTA without work items)
+  // The next kernel may launch: the producer allowed it when this CTA began its last work item;
+  // a CTA without work items allows it here.
   grid_dependents_launch();
   tc_fence_before();
   __syncthreads();
