@@ -318,9 +318,9 @@ TcPlan plan_tc(const Call& c, const DevShape& d) {
   // with staged Y, slower on the plain 16-bit FFN shape, equal on 4096^3.
   t.row_bars = t.k_rows > 1 && (c.t.ab == ELEM_E4M3 || staged_y);
   // Bias-initialised accumulator: on by default for short K loops (K <= 1024), where the epilogue
-  // sets the pace and moving the bias out of it pays (GLU block, M = 1024, N = 21568: K = 256
-  // 27.2 vs 28.3 us, K = 1024 44.6 vs 45.1 us); with long K loops the bias write lengthens the
-  // accumulator hand-off instead (4096^3: 90.3 vs 88.1 us).
+  // sets the pace and moving the bias out of it pays (GLU block, M = 1024, N = 21568, on vs off,
+  // each timed after an idle second: K = 256 / 512 / 1024 24.9 vs 26.4, 34.5 vs 35.1, 41.8 vs
+  // 42.0 us); with long K loops it does not (4096^3 80.9 vs 80.3 us).
   const int bi = c.opts ? c.opts->bias_init : 0;
   t.bias_init = c.epi != EPI_NONE && (bi == 1 || (bi == 0 && c.K <= 1024));
   // Set by one extra MMA (ones x the staged bias row) instead of by the epilogue warps, where the
