@@ -11,7 +11,9 @@
 //               deep as the epilogue's buffers allow (three 64 KB stages with two K rows on pairs,
 //               else up to six of 32 KB); completion counted in bytes on full[s] (with fp8
 //               operands and staged Y, a full barrier per K row of the stage, B then copied one
-//               K row at a time, so the first row's MMAs start while the second lands); out-of-range
+//               K row at a time, so the first row's MMAs start while the second lands; the fp8
+//               column pieces of the last round on pairs, 64 columns per CTA, take B as
+//               64-byte-wide boxes with 64-byte swizzle); out-of-range
 //               rows / columns / K are zero-filled by TMA, which is the M/N/K tail mask of
 //               "I3. Fuse a GEMM epilogue and change tile scheduling" ("Tiles and grouped
 //               ownership": A's M/K edges, B's K/N edges).
