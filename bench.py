@@ -78,12 +78,22 @@ def strip_comments(src: str) -> str:
     return "".join(out)
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel and launch code (comments and layout excluded): recorded ncu traffic
-    counts only while this matches the hash stored with it."""
+# The sources a kernel's DRAM traffic depends on: its own file, the shared device helpers and
+# parameter structs, and the host code that plans and launches it.
+KERNEL_SOURCES = {
+    "tc_gemm_kernel": ["api.cu", "kernels.h", "ptx.cuh", "tc_gemm.cu", "tile_order.h"],
+    "skinny_kernel": ["api.cu", "kernels.h", "ptx.cuh", "skinny.cu"],
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of a kernel's device and launch code (every source file when `kernel` is None;
+    comments and layout excluded): recorded ncu traffic counts only while this matches the hash
+    stored with it."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "gemm_epilogue_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    files = KERNEL_SOURCES[kernel] if kernel else sorted(os.listdir(d))
+    for f in files:
         with open(os.path.join(d, f), encoding="utf-8") as fh:
             code = " ".join(strip_comments(fh.read()).split())  # layout and comments excluded
             h.update(f.encode() + code.encode())
@@ -98,7 +108,7 @@ def recorded_traffic(workload: str, kernel: str):
     with open(p) as f:
         d = json.load(f)
     e = d.get(workload, {}).get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 

@@ -51,17 +51,39 @@ def test_recorded_traffic_needs_the_current_sources(tmp_path, monkeypatch):
     (prof / "traffic.json").write_text(json.dumps(
         {"square_4096": {"tc_gemm_kernel": {"dram_bytes_per_launch": 123, "source_hash": "abc"}}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc")
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel=None: "abc")
     assert bench.recorded_traffic("square_4096", "tc_gemm_kernel") == 123
     assert bench.recorded_traffic("square_4096", "skinny_kernel") is None
     assert bench.recorded_traffic("glu_gate_1024x21568x4096", "tc_gemm_kernel") is None
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "changed")
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel=None: "changed")
     assert bench.recorded_traffic("square_4096", "tc_gemm_kernel") is None
 
 
 def test_source_hash_covers_every_kernel_file():
     h = bench.kernel_source_hash()
     assert len(h) == 16 and int(h, 16) >= 0
+    import os
+    csrc = os.path.join(bench.ROOT, "gemm_epilogue_gb300", "csrc")
+    for kernel, files in bench.KERNEL_SOURCES.items():
+        assert all(os.path.exists(os.path.join(csrc, f)) for f in files), kernel
+        assert len(bench.kernel_source_hash(kernel)) == 16
+
+
+def test_a_kernels_hash_follows_only_its_own_sources(tmp_path, monkeypatch):
+    import os
+    import shutil
+    src = os.path.join(bench.ROOT, "gemm_epilogue_gb300", "csrc")
+    dst = tmp_path / "gemm_epilogue_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    tc, sk = bench.kernel_source_hash("tc_gemm_kernel"), bench.kernel_source_hash("skinny_kernel")
+    with open(dst / "skinny.cu", "a") as f:
+        f.write("\nint an_added_line;\n")
+    assert bench.kernel_source_hash("tc_gemm_kernel") == tc
+    assert bench.kernel_source_hash("skinny_kernel") != sk
+    with open(dst / "ptx.cuh", "a") as f:  # shared by both
+        f.write("\nint another_line;\n")
+    assert bench.kernel_source_hash("tc_gemm_kernel") != tc
 
 
 def test_tensor_peak_per_operand_type():
