@@ -145,9 +145,10 @@ typedef struct {
   int pdl;        /* tensor-core and skinny paths: launch with programmatic stream serialization:
                      the kernel's set-up (barriers, tensor memory) may run while the previous
                      kernel in the stream is finishing, and the kernel waits for that kernel to
-                     complete (griddepcontrol.wait) before its first access to global memory, so a
-                     dependency between the two stays safe.  0 = automatic (on), 1 = on,
-                     2 = off */
+                     complete (griddepcontrol.wait) before it copies or stores any global data, so
+                     a dependency between the two stays safe (before the wait it may prefetch its
+                     first inputs into L2, which stays coherent with that kernel's writes).
+                     0 = automatic (on), 1 = on, 2 = off */
   int raster;     /* tensor-core path: 0 = the grouped order over M ("I3. Fuse a GEMM epilogue and
                      change tile scheduling": bands of group_m M-tiles walking N); 1 = the same
                      order with M and N exchanged (bands of group_m N-tiles walking M), which keeps
